@@ -1,0 +1,188 @@
+"""Seeded synthetic inputs for the decode attention core.
+
+This module is the only code shared by the CUDA path's tests/benchmark and the
+fp64 oracle's tests.  It draws inputs; it holds none of the attention
+arithmetic.
+
+Recipe (gemma-4-31B Model Spec: ``attn.qk_norm`` and ``attn.v_norm`` rows of the
+"Compute-graph nodes" table, eps 1e-6; "Tensors of the main nodes" table,
+``attn.core`` row, for the shapes):
+
+* every head vector of q, k and v is drawn N(0, 1) in fp32, divided by its root
+  mean square sqrt(mean(x^2) + 1e-6) (unit weight), then rounded to bf16
+  (round-to-nearest-even) -- the state in which the attention core receives
+  them after the per-head norms;
+* sequence lengths come from ``numpy.random.default_rng(seed)``;
+* tensor values come from ``torch.Generator(device).manual_seed(seed * 16 + id)``
+  with a fixed id per tensor, drawn in fixed-size chunks so the values depend on
+  the seed, the shape and the device only;
+* paged caches use 16-position pages whose physical ids are a seeded random
+  permutation; block-table entries past a sequence's last page hold -1.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+# Layer geometries of the Model Spec's two attention-core rows.
+SLIDING = dict(H=32, KVH=16, D=256, window=1024)  # slidingDecodeGQA
+GLOBAL = dict(H=32, KVH=4, D=512, window=0)       # decodeGQA
+PAGE_SIZE = 16                                    # "Shape domain" row of "At a glance"
+
+_RMS_EPS = 1e-6
+_CHUNK_ELEMS = 1 << 27
+
+_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "k_pages": 4, "v_pages": 5}
+
+
+def rms_normalised_bf16(shape, seed: int, device="cpu") -> torch.Tensor:
+    """bf16 tensor whose last-dim vectors are N(0,1) draws scaled to unit RMS."""
+    shape = tuple(int(s) for s in shape)
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    if out.numel() == 0:
+        return out
+    d = shape[-1]
+    rows = out.numel() // d
+    flat = out.view(rows, d)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    step = max(1, _CHUNK_ELEMS // d)
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        x = torch.randn((r1 - r0, d), generator=gen, device=device, dtype=torch.float32)
+        x = x * torch.rsqrt(x.square().mean(dim=-1, keepdim=True) + _RMS_EPS)
+        flat[r0:r1].copy_(x)
+    return out
+
+
+def tensor_seed(seed: int, name: str) -> int:
+    return int(seed) * 16 + _TENSOR_IDS[name]
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """uint16 numpy view (on the host) of a bf16 tensor's bit patterns."""
+    if t.dtype != torch.bfloat16:
+        raise TypeError("expected a bf16 tensor")
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# Sequence lengths of the five benchmark workloads
+# ----------------------------------------------------------------------------
+
+def lengths_fixed(value: int, batch: int):
+    return lambda rng: np.full(batch, value, dtype=np.int32)
+
+
+def lengths_uniform(lo: int, hi: int, batch: int):
+    """Integers uniform on [lo, hi] inclusive."""
+    return lambda rng: rng.integers(lo, hi, size=batch, endpoint=True).astype(np.int32)
+
+
+def lengths_lognormal(median: float, sigma: float, lo: int, hi: int, batch: int):
+    """round(exp(ln(median) + sigma * z)), z ~ N(0, 1), clipped to [lo, hi]."""
+    def draw(rng):
+        z = rng.standard_normal(batch)
+        x = np.rint(np.exp(math.log(median) + sigma * z))
+        return np.clip(x, lo, hi).astype(np.int32)
+    return draw
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic workload: a geometry (or two, for the paged mix) and lengths."""
+    name: str
+    description: str
+    B: int
+    S: int                   # cache capacity in positions (contiguous) / max length (paged)
+    seed: int
+    lengths: object = field(repr=False)
+    layers: tuple = ()       # ("sliding",) / ("global",) / ("sliding", "global")
+    paged: bool = False
+
+    def seq_lens(self) -> np.ndarray:
+        return self.lengths(np.random.default_rng(self.seed))
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("sliding_b1_s2048", "slidingDecodeGQA single step, B=1, seq_len 2048",
+                 B=1, S=2048, seed=0, lengths=lengths_fixed(2048, 1), layers=("sliding",)),
+        Workload("global_b8_s8192", "decodeGQA, B=8, seq_lens uniform on [1, 8192]",
+                 B=8, S=8192, seed=1, lengths=lengths_uniform(1, 8192, 8), layers=("global",)),
+        Workload("sliding_b64_s32768", "slidingDecodeGQA batched, B=64, seq_lens uniform on [1, 32768]",
+                 B=64, S=32768, seed=2, lengths=lengths_uniform(1, 32768, 64), layers=("sliding",)),
+        Workload("global_b16_s131072", "decodeGQA long context, B=16, seq_lens uniform on [65536, 131072]",
+                 B=16, S=131072, seed=3, lengths=lengths_uniform(65536, 131072, 16),
+                 layers=("global",)),
+        Workload("paged_mixed_b256", "paged mixed batch, B=256, lognormal seq_lens (median 4096, "
+                 "sigma 1) clipped to [1, 65536]; one sliding and one global call",
+                 B=256, S=65536, seed=4, lengths=lengths_lognormal(4096, 1.0, 1, 65536, 256),
+                 layers=("sliding", "global"), paged=True),
+    ]
+}
+
+
+def geometry(layer: str) -> dict:
+    return dict(SLIDING if layer == "sliding" else GLOBAL)
+
+
+# ----------------------------------------------------------------------------
+# Case builders
+# ----------------------------------------------------------------------------
+
+def contiguous_case(B: int, S: int, H: int, KVH: int, D: int, seq_lens, seed: int,
+                    device="cpu") -> dict:
+    """q [B,H,D], k/v [B,S,KVH,D] (bf16) and seq_lens [B] (int32, on ``device``)."""
+    lens = torch.as_tensor(np.asarray(seq_lens, dtype=np.int32), device=device)
+    return dict(
+        q=rms_normalised_bf16((B, H, D), tensor_seed(seed, "q"), device),
+        k=rms_normalised_bf16((B, S, KVH, D), tensor_seed(seed, "k"), device),
+        v=rms_normalised_bf16((B, S, KVH, D), tensor_seed(seed, "v"), device),
+        seq_lens=lens,
+    )
+
+
+def page_table(seq_lens, seed: int, max_pages: int | None = None,
+               page_size: int = PAGE_SIZE, spare_pages: int = 0):
+    """Seeded random page assignment.
+
+    Returns (block_table int32 [B, max_pages], P).  Sequence b owns
+    ceil(L_b / page_size) pages; the physical ids of all owned pages are a random
+    permutation of [0, P) with P = total owned pages + ``spare_pages``.  Entries
+    past a sequence's last page are -1.
+    """
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    need = (lens + page_size - 1) // page_size
+    if max_pages is None:
+        max_pages = max(1, int(need.max()) if len(need) else 1)
+    total = int(need.sum())
+    P = max(1, total + int(spare_pages))
+    rng = np.random.default_rng(seed + 1_000_003)
+    perm = rng.permutation(P).astype(np.int32)
+    bt = np.full((len(lens), max_pages), -1, dtype=np.int32)
+    off = 0
+    for b, n in enumerate(need):
+        bt[b, :n] = perm[off:off + n]
+        off += n
+    return bt, P
+
+
+def paged_case(B: int, H: int, KVH: int, D: int, seq_lens, seed: int, max_pages: int | None = None,
+               device="cpu", spare_pages: int = 0, table=None) -> dict:
+    """q [B,H,D], page pools [P,16,KVH,D] (bf16), block_table [B,max_pages], seq_lens [B]."""
+    if table is None:
+        table = page_table(seq_lens, seed, max_pages, PAGE_SIZE, spare_pages)
+    bt, P = table
+    lens = torch.as_tensor(np.asarray(seq_lens, dtype=np.int32), device=device)
+    return dict(
+        q=rms_normalised_bf16((B, H, D), tensor_seed(seed, "q"), device),
+        k_pages=rms_normalised_bf16((P, PAGE_SIZE, KVH, D), tensor_seed(seed, "k_pages"), device),
+        v_pages=rms_normalised_bf16((P, PAGE_SIZE, KVH, D), tensor_seed(seed, "v_pages"), device),
+        block_table=torch.as_tensor(bt, device=device),
+        seq_lens=lens,
+    )
+

@@ -1,0 +1,317 @@
+/*
+ * fp64 CPU oracle for the Gemma-4-31B decode-step attention core ("attn.core").
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or helper with the CUDA path, and the CUDA path never calls it.
+ *
+ * What it computes (gemma-4-31B Model Spec, "Compute-graph nodes" table,
+ * rows `attn.core` / slidingDecodeGQA and `attn.core` / decodeGQA):
+ *
+ *   o[b,h] = sum_{s in range(b)} softmax_s( 1 * <q[b,h], k[b,s,h/g]> ) * v[b,s,h/g]
+ *
+ * with g = H / KVH query heads per KV head (2 for sliding layers, 8 for global
+ * layers) and attention scale exactly 1.  The attended range follows the masks
+ * of the "Gemma 4 31B-it Text Architecture" page, "Compact form", with the new
+ * token's K/V
+ * appended before attention, so the query position is t = L_b - 1 (full layers
+ * attend to every s with s <= t, sliding layers to s in the half-open interval
+ * (t - 1024, t]):
+ *
+ *   window == 0 : s in [0, L_b)
+ *   window  > 0 : s in [max(0, L_b - window), L_b)
+ *
+ * Per (b, h) the oracle follows the plain definition, in double precision, over
+ * the exact real values of the bf16 inputs:
+ *   1. score_s = sum_d q[b,h,d] * k[b,s,kvh,d]           (scale 1)
+ *   2. m       = max_s score_s
+ *   3. e_s     = exp(score_s - m)
+ *   4. l       = sum_s e_s
+ *   5. o[b,h,d] = (sum_s e_s * v[b,s,kvh,d]) / l
+ * The compact form fixes the softmax precision at fp32 or better; the oracle
+ * computes the exact result up to fp64 rounding.
+ * An empty range (L_b == 0) gives o = 0 (the empty sum).
+ *
+ * Inputs are bf16 bit patterns (uint16).  A bf16 value is the upper half of an
+ * IEEE binary32, so widening is exact.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL (-1)
+#define ORACLE_ENOMEM (-2)
+
+/* Exact widening of a bf16 bit pattern: the 16 bits are the high half of a
+ * binary32 value. */
+static double bf16_bits_to_double(uint16_t bits)
+{
+    uint32_t w = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* Attended range of sequence b (Compact form masks, append-before-attend). */
+static void attended_range(int64_t L, int window, int64_t *lo, int64_t *hi)
+{
+    *hi = L;
+    *lo = (window > 0 && L > window) ? L - window : 0;
+}
+
+/*
+ * Softmax-weighted sum over an explicit list of key/value rows.
+ *   q_row : D doubles
+ *   k_row(j), v_row(j) : pointers to D bf16 values of the j-th attended key/value
+ *   n     : number of attended rows
+ *   scores: scratch of n doubles
+ *   out   : D doubles
+ * Steps 1-5 of the definition above, one after the other.
+ */
+typedef const uint16_t *(*row_fn)(const void *ctx, int64_t j);
+
+static void attend(const double *q_row, int D, int64_t n, row_fn k_row, row_fn v_row,
+                   const void *ctx, double *scores, double *out)
+{
+    int d;
+    int64_t j;
+    for (d = 0; d < D; ++d) out[d] = 0.0;
+    if (n <= 0) return; /* empty sum */
+
+    /* 1. scores, scale 1 */
+    for (j = 0; j < n; ++j) {
+        const uint16_t *kr = k_row(ctx, j);
+        double s = 0.0;
+        for (d = 0; d < D; ++d) s += q_row[d] * bf16_bits_to_double(kr[d]);
+        scores[j] = s;
+    }
+    /* 2. max */
+    double m = scores[0];
+    for (j = 1; j < n; ++j)
+        if (scores[j] > m) m = scores[j];
+    /* 3. exponentials, 4. normaliser */
+    double l = 0.0;
+    for (j = 0; j < n; ++j) {
+        scores[j] = exp(scores[j] - m);
+        l += scores[j];
+    }
+    /* 5. weighted sum of values, divided by the normaliser */
+    for (j = 0; j < n; ++j) {
+        const uint16_t *vr = v_row(ctx, j);
+        const double e = scores[j];
+        for (d = 0; d < D; ++d) out[d] += e * bf16_bits_to_double(vr[d]);
+    }
+    for (d = 0; d < D; ++d) out[d] /= l;
+}
+
+/* ---- contiguous cache: k, v are [B, S, KVH, D] holding positions [pos_base, pos_base+S) ---- */
+typedef struct {
+    const uint16_t *k, *v;
+    int64_t b, kvh, lo, pos_base, S;
+    int KVH, D;
+} contig_ctx;
+
+static const uint16_t *contig_k(const void *c, int64_t j)
+{
+    const contig_ctx *x = (const contig_ctx *)c;
+    int64_t s = x->lo + j - x->pos_base;
+    return x->k + ((x->b * x->S + s) * x->KVH + x->kvh) * x->D;
+}
+static const uint16_t *contig_v(const void *c, int64_t j)
+{
+    const contig_ctx *x = (const contig_ctx *)c;
+    int64_t s = x->lo + j - x->pos_base;
+    return x->v + ((x->b * x->S + s) * x->KVH + x->kvh) * x->D;
+}
+
+/*
+ * q:        [B, H, D] bf16 bits
+ * k, v:     [B, S, KVH, D] bf16 bits; row s of the array is position pos_base + s
+ * seq_lens: [B] absolute lengths, 0 <= L_b, and every attended position must lie
+ *           in [pos_base, pos_base + S)
+ * window:   0 = full history (decodeGQA); > 0 = the last `window` positions
+ * out:      [B, H, D] doubles
+ * nthreads: OpenMP threads (<= 0: the runtime default)
+ * Returns 0, or a negative code for arguments outside the definition.
+ */
+int oracle_gqa_decode_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const int32_t *seq_lens, int B, int S, int H, int KVH, int D,
+                          int window, int64_t pos_base, int nthreads, double *out)
+{
+    int b;
+    if (B < 0 || S < 0 || H <= 0 || KVH <= 0 || D <= 0 || window < 0) return ORACLE_EINVAL;
+    if (H % KVH != 0) return ORACLE_EINVAL;
+    for (b = 0; b < B; ++b) {
+        int64_t lo, hi;
+        if (seq_lens[b] < 0) return ORACLE_EINVAL;
+        attended_range(seq_lens[b], window, &lo, &hi);
+        if (hi > lo && (lo < pos_base || hi > pos_base + S)) return ORACLE_EINVAL;
+    }
+    const int g = H / KVH;
+    const int64_t pairs = (int64_t)B * H;
+    int64_t max_n = 1;
+    for (b = 0; b < B; ++b) {
+        int64_t lo, hi;
+        attended_range(seq_lens[b], window, &lo, &hi);
+        if (hi - lo > max_n) max_n = hi - lo;
+    }
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#endif
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)max_n);
+        double *q_row = (double *)malloc(sizeof(double) * (size_t)D);
+        const int have_scratch = scores != NULL && q_row != NULL;
+        int64_t p;
+        /* every thread reaches the work-sharing loop (it ends in a barrier) */
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (p = 0; p < pairs; ++p) {
+            if (!have_scratch) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+                err = ORACLE_ENOMEM;
+                continue;
+            }
+            {
+                const int64_t bb = p / H, h = p % H;
+                int64_t lo, hi;
+                int d;
+                attended_range(seq_lens[bb], window, &lo, &hi);
+                for (d = 0; d < D; ++d) q_row[d] = bf16_bits_to_double(q[(bb * H + h) * D + d]);
+                contig_ctx c = {k, v, bb, h / g, lo, pos_base, S, KVH, D};
+                attend(q_row, D, hi - lo, contig_k, contig_v, &c, scores, out + (bb * H + h) * D);
+            }
+        }
+        free(scores);
+        free(q_row);
+    }
+    (void)nthreads;
+    return err;
+}
+
+/* ---- paged cache: pools [P, page_size, KVH, D]; position s of sequence b lives at
+ *      page block_table[b][s / page_size], slot s % page_size ---- */
+typedef struct {
+    const uint16_t *k, *v;
+    const int32_t *bt_row;
+    int64_t kvh, lo;
+    int page_size, KVH, D;
+} paged_ctx;
+
+static const uint16_t *paged_row(const uint16_t *pool, const paged_ctx *x, int64_t j)
+{
+    int64_t s = x->lo + j;
+    int64_t page = x->bt_row[s / x->page_size];
+    int64_t slot = s % x->page_size;
+    return pool + ((page * x->page_size + slot) * x->KVH + x->kvh) * x->D;
+}
+static const uint16_t *paged_k(const void *c, int64_t j)
+{
+    const paged_ctx *x = (const paged_ctx *)c;
+    return paged_row(x->k, x, j);
+}
+static const uint16_t *paged_v(const void *c, int64_t j)
+{
+    const paged_ctx *x = (const paged_ctx *)c;
+    return paged_row(x->v, x, j);
+}
+
+/*
+ * Paged variant ("Shape domain" row of the Model Spec: page size 16).
+ * k_pages, v_pages: [P, page_size, KVH, D] bf16 bits
+ * block_table:      [B, max_pages] page ids
+ * A sequence whose attended range references a page id outside [0, P) gets NaN
+ * for all of its heads (the ABI's convention for a corrupt block table).
+ */
+int oracle_gqa_decode_paged_f64(const uint16_t *q, const uint16_t *k_pages,
+                                const uint16_t *v_pages, const int32_t *block_table,
+                                const int32_t *seq_lens, int B, int P, int max_pages,
+                                int page_size, int H, int KVH, int D, int window,
+                                int nthreads, double *out)
+{
+    int b;
+    if (B < 0 || P <= 0 || max_pages <= 0 || page_size <= 0 || H <= 0 || KVH <= 0 || D <= 0 ||
+        window < 0)
+        return ORACLE_EINVAL;
+    if (H % KVH != 0) return ORACLE_EINVAL;
+    int64_t max_n = 1;
+    for (b = 0; b < B; ++b) {
+        int64_t lo, hi;
+        if (seq_lens[b] < 0 || (int64_t)seq_lens[b] > (int64_t)max_pages * page_size)
+            return ORACLE_EINVAL;
+        attended_range(seq_lens[b], window, &lo, &hi);
+        if (hi - lo > max_n) max_n = hi - lo;
+    }
+    const int g = H / KVH;
+    const int64_t pairs = (int64_t)B * H;
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#endif
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)max_n);
+        double *q_row = (double *)malloc(sizeof(double) * (size_t)D);
+        const int have_scratch = scores != NULL && q_row != NULL;
+        int64_t p;
+        /* every thread reaches the work-sharing loop (it ends in a barrier) */
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (p = 0; p < pairs; ++p) {
+            if (!have_scratch) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+                err = ORACLE_ENOMEM;
+                continue;
+            }
+            {
+                const int64_t bb = p / H, h = p % H;
+                const int32_t *bt_row = block_table + bb * (int64_t)max_pages;
+                double *o = out + (bb * H + h) * D;
+                int64_t lo, hi, s;
+                int d, bad = 0;
+                attended_range(seq_lens[bb], window, &lo, &hi);
+                for (s = lo; s < hi; s += 1) {
+                    int32_t page = bt_row[s / page_size];
+                    if (page < 0 || page >= P) {
+                        bad = 1;
+                        break;
+                    }
+                }
+                if (bad) {
+                    for (d = 0; d < D; ++d) o[d] = NAN;
+                    continue;
+                }
+                for (d = 0; d < D; ++d) q_row[d] = bf16_bits_to_double(q[(bb * H + h) * D + d]);
+                paged_ctx c = {k_pages, v_pages, bt_row, h / g, lo, page_size, KVH, D};
+                attend(q_row, D, hi - lo, paged_k, paged_v, &c, scores, o);
+            }
+        }
+        free(scores);
+        free(q_row);
+    }
+    (void)nthreads;
+    return err;
+}
+
+/* Threads the OpenMP runtime would use by default (for reporting). */
+int oracle_default_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

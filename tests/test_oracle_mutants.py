@@ -1,0 +1,105 @@
+"""Mutation check of the oracle pins (CPU only).
+
+Each case compiles a copy of the oracle's C source with one plausible mistake
+planted in it, then runs every pin of ``test_oracle_pins`` against that copy.
+The pins must reject every mutant: at least one of them fails (an assertion or a
+rejected call).  The real oracle passes them all (``test_oracle_pins``).
+"""
+import itertools
+import os
+
+import pytest
+
+import oracle
+import tests.test_oracle_pins as pins
+
+MUTANTS = {
+    "window_start_one_late": (
+        "*lo = (window > 0 && L > window) ? L - window : 0;",
+        "*lo = (window > 0 && L > window) ? L - window + 1 : 0;"),
+    "window_start_one_early": (
+        "*lo = (window > 0 && L > window) ? L - window : 0;",
+        "*lo = (window > 0 && L > window + 1) ? L - window - 1 : 0;"),
+    "window_ignored": (
+        "*lo = (window > 0 && L > window) ? L - window : 0;",
+        "*lo = 0;"),
+    "scale_inverse_sqrt_d": (
+        "        scores[j] = s;\n",
+        "        scores[j] = s / sqrt((double)D);\n"),
+    "head_map_modulo": (
+        "contig_ctx c = {k, v, bb, h / g,",
+        "contig_ctx c = {k, v, bb, h % KVH,"),
+    "paged_head_map_modulo": (
+        "paged_ctx c = {k_pages, v_pages, bt_row, h / g,",
+        "paged_ctx c = {k_pages, v_pages, bt_row, h % KVH,"),
+    "no_max_subtraction": (
+        "scores[j] = exp(scores[j] - m);",
+        "scores[j] = exp(scores[j]);"),
+    "keys_and_values_swapped": (
+        "const uint16_t *kr = k_row(ctx, j);",
+        "const uint16_t *kr = v_row(ctx, j);"),
+    "value_row_misaligned": (
+        "const uint16_t *vr = v_row(ctx, j);",
+        "const uint16_t *vr = v_row(ctx, (j + 1) % n);"),
+    "normaliser_dropped": (
+        "for (d = 0; d < D; ++d) out[d] /= l;",
+        "(void)l;"),
+    "first_term_of_normaliser_dropped": (
+        "        l += scores[j];\n",
+        "        l += (j > 0) ? scores[j] : 0.0;\n"),
+    "last_key_dropped": (
+        "attend(q_row, D, hi - lo, contig_k",
+        "attend(q_row, D, hi - lo - (hi - lo > 1), contig_k"),
+    "paged_slot_shifted": (
+        "int64_t slot = s % x->page_size;",
+        "int64_t slot = (s + 1) % x->page_size;"),
+    "paged_page_index_off": (
+        "int64_t page = x->bt_row[s / x->page_size];",
+        "int64_t page = x->bt_row[(s + 1) / x->page_size];"),
+    "query_transposed": (
+        "q_row[d] = bf16_bits_to_double(q[(bb * H + h) * D + d]);\n                contig_ctx",
+        "q_row[d] = bf16_bits_to_double(q[(d % H) * D + (bb * H + h) % D]);\n                contig_ctx"),
+    "empty_range_not_zero": (
+        "if (n <= 0) return; /* empty sum */",
+        "if (n <= 0) { for (d = 0; d < D; ++d) out[d] = 1.0; return; }"),
+}
+
+
+def _expand(fn):
+    """All argument combinations of a pin's pytest parametrize marks."""
+    marks = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
+    if not marks:
+        return [{}]
+    axes = []
+    for m in marks:
+        names = [n.strip() for n in m.args[0].split(",")]
+        values = m.args[1]
+        axes.append([dict(zip(names, v if len(names) > 1 else (v,))) for v in values])
+    out = []
+    for combo in itertools.product(*axes):
+        d = {}
+        for part in combo:
+            d.update(part)
+        out.append(d)
+    return out
+
+
+PIN_FUNCS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    before, after = MUTANTS[name]
+    src = oracle.source_text()
+    assert src.count(before) == 1, f"mutation site for {name} not found exactly once"
+    so = oracle.compile_variant(src.replace(before, after), os.path.join(tmp_path, f"m_{name}.so"))
+    mutant = oracle.OracleLibrary(so)
+    failed = []
+    for fn in PIN_FUNCS:
+        for kwargs in _expand(fn):
+            try:
+                fn(mutant, **kwargs)
+            except (AssertionError, ValueError):
+                failed.append(fn.__name__)
+                break
+    assert failed, f"no pin rejects mutant {name}"

@@ -1,0 +1,386 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+Each test ties the oracle to a closed form, an invariant of the definition, an
+independent brute-force formulation, or a library routine (torch SDPA in
+float64).  Chosen so that a plausible slip in the oracle -- a wrong window
+bound, a wrong head mapping, a 1/sqrt(D) scale, a missing max subtraction,
+swapped k/v, a k row paired with the wrong v row, a wrong page index -- fails at
+least one of them.
+
+Definition pinned (gemma-4-31B Model Spec, "Compute-graph nodes", the two
+``attn.core`` rows; masks and append-before-attend from the "Gemma 4 31B-it
+Text Architecture" page, "Compact form").
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = []
+
+RNG = np.random.default_rng(12345)
+
+
+def to_bits(x) -> np.ndarray:
+    """Round float values to bf16 (RNE) and return the bit patterns."""
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def to_vals(bits: np.ndarray) -> np.ndarray:
+    """Exact real values (float64) of bf16 bit patterns."""
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def exact_bits(x) -> np.ndarray:
+    """Bits of values that must be exactly representable in bf16."""
+    b = to_bits(x)
+    assert np.array_equal(to_vals(b), np.asarray(x, dtype=np.float64)), "value not bf16-exact"
+    return b
+
+
+def random_case(B, S, H, KVH, D, seed=0):
+    rng = np.random.default_rng(seed)
+    q = to_bits(rng.standard_normal((B, H, D)))
+    k = to_bits(rng.standard_normal((B, S, KVH, D)))
+    v = to_bits(rng.standard_normal((B, S, KVH, D)))
+    return q, k, v
+
+
+def window_range(L, W):
+    return (max(0, L - W) if W > 0 else 0), L
+
+
+# ---------------------------------------------------------------------------
+# closed forms
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("window", [0, 8])
+def test_constant_values_give_that_value(oracle_lib, window):
+    """If v[b, s, kvh] is the same vector c for every s, o[b, h] = c[h // g]."""
+    B, S, H, KVH, D = 3, 37, 8, 2, 16
+    q, k, _ = random_case(B, S, H, KVH, D, seed=1)
+    c = to_bits(RNG.standard_normal((B, KVH, D)))
+    v = np.broadcast_to(c[:, None, :, :], (B, S, KVH, D)).copy()
+    lens = [37, 5, 1]
+    out = oracle_lib.gqa_decode_f64(q, k, v, lens, window)
+    g = H // KVH
+    for b in range(B):
+        for h in range(H):
+            np.testing.assert_allclose(out[b, h], to_vals(c[b, h // g]), rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("window", [0, 1, 1024])
+def test_length_one_returns_first_value(oracle_lib, window):
+    """One attended key has weight exactly 1: o[b, h] = v[b, 0, h // g]."""
+    B, S, H, KVH, D = 2, 4, 32, 4, 32
+    q, k, v = random_case(B, S, H, KVH, D, seed=2)
+    out = oracle_lib.gqa_decode_f64(q, k, v, [1, 1], window)
+    g = H // KVH
+    for b in range(B):
+        for h in range(H):
+            assert np.array_equal(out[b, h], to_vals(v[b, 0, h // g]))
+
+
+@pytest.mark.parametrize("L,W", [(1, 0), (5, 0), (10, 4), (37, 16), (16, 16), (17, 16), (3, 16)])
+def test_zero_query_gives_window_mean(oracle_lib, L, W):
+    """q = 0 makes every score 0, so o is the plain mean of v over the attended range."""
+    B, S, H, KVH, D = 1, 40, 4, 2, 8
+    _, k, v = random_case(B, S, H, KVH, D, seed=3)
+    q = np.zeros((B, H, D), dtype=np.uint16)
+    out = oracle_lib.gqa_decode_f64(q, k, v, [L], W)
+    lo, hi = window_range(L, W)
+    vv = to_vals(v)
+    for h in range(H):
+        expect = vv[0, lo:hi, h // (H // KVH)].mean(axis=0)
+        np.testing.assert_allclose(out[0, h], expect, rtol=1e-13, atol=1e-15)
+
+
+def test_two_keys_logistic_closed_form_scale_one(oracle_lib):
+    """Two keys: o = v0 + (v1 - v0) * sigmoid(s1 - s0) with s_j = <q, k_j> (scale 1).
+
+    Scores are built from one-hot vectors so they are known without a dot
+    product: q = a e_0, k_j = x_j e_0, so s_j = a x_j exactly.
+    """
+    D, H, KVH = 8, 2, 1
+    a, x0, x1 = 1.5, 0.25, 2.0
+    q = np.zeros((1, H, D)); q[0, :, 0] = a
+    k = np.zeros((1, 2, KVH, D)); k[0, 0, 0, 0] = x0; k[0, 1, 0, 0] = x1
+    v = RNG.standard_normal((1, 2, KVH, D))
+    qb, kb, vb = exact_bits(q), exact_bits(k), to_bits(v)
+    out = oracle_lib.gqa_decode_f64(qb, kb, vb, [2], 0)
+    vv = to_vals(vb)
+    sig = 1.0 / (1.0 + math.exp(-(a * x1 - a * x0)))
+    expect = vv[0, 0, 0] + (vv[0, 1, 0] - vv[0, 0, 0]) * sig
+    for h in range(H):
+        np.testing.assert_allclose(out[0, h], expect, rtol=1e-14, atol=1e-15)
+    # a 1/sqrt(D) scale would give a visibly different weight
+    sig_scaled = 1.0 / (1.0 + math.exp(-(a * x1 - a * x0) / math.sqrt(D)))
+    assert abs(sig - sig_scaled) > 0.1
+
+
+def test_huge_logits_do_not_overflow(oracle_lib):
+    """Scores of +-1024: without subtracting the max, exp overflows to inf/NaN.
+
+    Head 0 (q = +1024 e_0) must return v at the one key equal to e_0; head 1
+    (q = -1024 e_0) gives that key weight exp(-1024) = 0 in double, so o is the
+    mean of the other values.
+    """
+    D, H, KVH, L, j = 8, 2, 1, 9, 4
+    q = np.zeros((1, H, D)); q[0, 0, 0] = 1024.0; q[0, 1, 0] = -1024.0
+    k = np.zeros((1, L, KVH, D)); k[0, j, 0, 0] = 1.0
+    vb = to_bits(RNG.standard_normal((1, L, KVH, D)))
+    out = oracle_lib.gqa_decode_f64(exact_bits(q), exact_bits(k), vb, [L], 0)
+    vv = to_vals(vb)
+    assert np.all(np.isfinite(out))
+    assert np.array_equal(out[0, 0], vv[0, j, 0])
+    others = np.delete(vv[0, :, 0], j, axis=0).mean(axis=0)
+    np.testing.assert_allclose(out[0, 1], others, rtol=1e-13, atol=1e-15)
+
+
+def test_empty_range_is_zero(oracle_lib):
+    """L_b = 0: the empty sum, o = 0 (never NaN)."""
+    q, k, v = random_case(3, 8, 8, 4, 16, seed=4)
+    out = oracle_lib.gqa_decode_f64(q, k, v, [0, 3, 0], 0)
+    assert np.all(out[0] == 0) and np.all(out[2] == 0)
+    assert np.all(np.isfinite(out[1])) and np.any(out[1] != 0)
+
+
+def test_empty_batch(oracle_lib):
+    q = np.zeros((0, 8, 16), np.uint16)
+    k = np.zeros((0, 4, 4, 16), np.uint16)
+    out = oracle_lib.gqa_decode_f64(q, k, k, np.zeros(0, np.int32), 0)
+    assert out.shape == (0, 8, 16)
+
+
+# ---------------------------------------------------------------------------
+# invariants
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H,KVH", [(32, 16), (32, 4)])
+def test_gqa_head_mapping(oracle_lib, H, KVH):
+    """Changing KV head kvh changes exactly the query heads h with h // g == kvh."""
+    B, S, D = 2, 12, 16
+    g = H // KVH
+    q, k, v = random_case(B, S, H, KVH, D, seed=5)
+    base = oracle_lib.gqa_decode_f64(q, k, v, [12, 7], 0)
+    for kvh in [0, KVH // 2, KVH - 1]:
+        k2, v2 = k.copy(), v.copy()
+        k2[0, :, kvh] = to_bits(RNG.standard_normal((S, D)))
+        v2[0, :, kvh] = to_bits(RNG.standard_normal((S, D)))
+        out = oracle_lib.gqa_decode_f64(q, k2, v2, [12, 7], 0)
+        changed = {h for h in range(H) if not np.array_equal(out[0, h], base[0, h])}
+        assert changed == {h for h in range(H) if h // g == kvh}
+        assert np.array_equal(out[1], base[1])
+
+
+def test_window_at_least_length_equals_full(oracle_lib):
+    """Any window >= L reads every position, so it equals the full-history result."""
+    B, S, H, KVH, D = 3, 50, 8, 2, 16
+    q, k, v = random_case(B, S, H, KVH, D, seed=6)
+    lens = [50, 20, 1]
+    full = oracle_lib.gqa_decode_f64(q, k, v, lens, 0)
+    for W in [50, 64, 1024]:
+        assert np.array_equal(oracle_lib.gqa_decode_f64(q, k, v, lens, W), full)
+    assert not np.array_equal(oracle_lib.gqa_decode_f64(q, k, v, lens, 49)[0], full[0])
+
+
+@pytest.mark.parametrize("L,W", [(50, 16), (17, 16), (16, 16), (1030, 1024), (1025, 1024)])
+def test_window_equals_full_on_the_last_positions(oracle_lib, L, W):
+    """Sliding over [L-W, L) equals full attention over a cache holding only those rows."""
+    S, H, KVH, D = L, 4, 2, 8
+    q, k, v = random_case(1, S, H, KVH, D, seed=7)
+    sliding = oracle_lib.gqa_decode_f64(q, k, v, [L], W)
+    lo = max(0, L - W)
+    sliced = oracle_lib.gqa_decode_f64(q, k[:, lo:].copy(), v[:, lo:].copy(), [L - lo], 0)
+    assert np.array_equal(sliding, sliced)
+    # the same rows addressed through pos_base
+    based = oracle_lib.gqa_decode_f64(q, k[:, lo:].copy(), v[:, lo:].copy(), [L], W, pos_base=lo)
+    assert np.array_equal(sliding, based)
+
+
+def test_output_is_a_convex_combination(oracle_lib):
+    """Each coordinate of o lies between the min and max of v over the attended rows."""
+    B, S, H, KVH, D = 4, 30, 8, 4, 16
+    q, k, v = random_case(B, S, H, KVH, D, seed=8)
+    lens, W = [30, 12, 5, 29], 10
+    out = oracle_lib.gqa_decode_f64(q, k, v, lens, W)
+    vv = to_vals(v)
+    for b, L in enumerate(lens):
+        lo, hi = window_range(L, W)
+        for h in range(H):
+            rows = vv[b, lo:hi, h // (H // KVH)]
+            assert np.all(out[b, h] >= rows.min(axis=0) - 1e-12)
+            assert np.all(out[b, h] <= rows.max(axis=0) + 1e-12)
+
+
+def test_permuting_positions_consistently_changes_nothing(oracle_lib):
+    """Softmax attention is a function of the set of (k, v) pairs: reordering them
+    (the same permutation for k and v) leaves o unchanged up to rounding, and
+    pairing keys with other rows' values does not."""
+    S, H, KVH, D = 24, 8, 2, 16
+    q, k, v = random_case(1, S, H, KVH, D, seed=9)
+    base = oracle_lib.gqa_decode_f64(q, k, v, [S], 0)
+    perm = np.random.default_rng(1).permutation(S)
+    out = oracle_lib.gqa_decode_f64(q, k[:, perm].copy(), v[:, perm].copy(), [S], 0)
+    np.testing.assert_allclose(out, base, rtol=1e-12, atol=1e-14)
+    mismatched = oracle_lib.gqa_decode_f64(q, k, v[:, perm].copy(), [S], 0)
+    assert np.max(np.abs(mismatched - base)) > 1e-3
+
+
+def test_keys_and_values_play_different_roles(oracle_lib):
+    """Swapping the k and v tensors changes the result (they are not interchangeable)."""
+    q, k, v = random_case(1, 20, 4, 2, 8, seed=10)
+    a = oracle_lib.gqa_decode_f64(q, k, v, [20], 0)
+    b = oracle_lib.gqa_decode_f64(q, v, k, [20], 0)
+    assert np.max(np.abs(a - b)) > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# independent formulations
+# ---------------------------------------------------------------------------
+
+def brute_force(q, k, v, lens, W):
+    """Explicit [H, S] score matrix with a boolean mask built from the query position
+    t = L - 1 (causal s <= t, and t - W < s for a window), softmax over the
+    masked row with scipy, then a matrix product with repeat-expanded V."""
+    from scipy.special import softmax
+    qv, kv, vv = to_vals(q), to_vals(k), to_vals(v)
+    B, H, D = qv.shape
+    _, S, KVH, _ = kv.shape
+    g = H // KVH
+    out = np.zeros((B, H, D))
+    for b in range(B):
+        t = lens[b] - 1
+        s = np.arange(S)
+        mask = s <= t
+        if W > 0:
+            mask &= s > t - W
+        k_rep = np.repeat(kv[b], g, axis=1)  # [S, H, D]: head h reads kv head h // g
+        v_rep = np.repeat(vv[b], g, axis=1)
+        scores = np.einsum("hd,shd->hs", qv[b], k_rep)
+        scores[:, ~mask] = -np.inf
+        p = softmax(scores, axis=-1)
+        out[b] = np.einsum("hs,shd->hd", p, v_rep)
+    return out
+
+
+@pytest.mark.parametrize("H,KVH,D,W", [(32, 16, 8, 0), (32, 16, 16, 5), (32, 4, 8, 0),
+                                       (32, 4, 16, 7), (32, 16, 256, 1024), (32, 4, 512, 0)])
+def test_brute_force_explicit_mask(oracle_lib, H, KVH, D, W):
+    B, S = 3, 40
+    q, k, v = random_case(B, S, H, KVH, D, seed=11 + D + W)
+    lens = [40, 13, 1]
+    out = oracle_lib.gqa_decode_f64(q, k, v, lens, W)
+    ref = brute_force(q, k, v, lens, W)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-13)
+
+
+def test_brute_force_window_edges(oracle_lib):
+    """Lengths around the 1024 window: 1023, 1024, 1025, 1040 (tiny D)."""
+    B, S, H, KVH, D, W = 4, 1040, 4, 2, 8, 1024
+    q, k, v = random_case(B, S, H, KVH, D, seed=12)
+    # make the positions just outside the window stand out so an off-by-one shows
+    k[:, :, :, :] = to_bits(to_vals(k) * 0.5)
+    lens = [1023, 1024, 1025, 1040]
+    out = oracle_lib.gqa_decode_f64(q, k, v, lens, W)
+    ref = brute_force(q, k, v, lens, W)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-13)
+    # and a window shifted by one position is detectably different
+    for b, L in enumerate(lens[2:], start=2):
+        off_by_one = oracle_lib.gqa_decode_f64(q, k, v, lens, W + 1)
+        assert np.max(np.abs(off_by_one[b] - out[b])) > 1e-6
+
+
+@pytest.mark.parametrize("H,KVH,W", [(32, 16, 1024), (32, 4, 0), (32, 16, 6)])
+def test_torch_sdpa_float64(oracle_lib, H, KVH, W):
+    """torch.nn.functional.scaled_dot_product_attention in float64 on CPU, scale=1,
+    with a boolean mask and K/V expanded to the query heads."""
+    B, S, D = 3, 33, 32
+    q, k, v = random_case(B, S, H, KVH, D, seed=13)
+    lens = [33, 20, 2]
+    out = oracle_lib.gqa_decode_f64(q, k, v, lens, W)
+    g = H // KVH
+    qt = torch.from_numpy(to_vals(q))[:, :, None, :]                      # [B, H, 1, D]
+    kt = torch.from_numpy(to_vals(k)).permute(0, 2, 1, 3).repeat_interleave(g, dim=1)
+    vt = torch.from_numpy(to_vals(v)).permute(0, 2, 1, 3).repeat_interleave(g, dim=1)
+    pos = torch.arange(S)
+    mask = torch.zeros(B, 1, 1, S, dtype=torch.bool)
+    for b, L in enumerate(lens):
+        lo, hi = window_range(L, W)
+        mask[b, 0, 0] = (pos >= lo) & (pos < hi)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=1.0)
+    np.testing.assert_allclose(out, ref[:, :, 0, :].numpy(), rtol=1e-11, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# paged indexing
+# ---------------------------------------------------------------------------
+
+def scatter_to_pages(k, v, lens, page_size=16, spare=3, seed=0):
+    """Copy each sequence's rows into randomly numbered pages; return pools + table."""
+    B, S, KVH, D = k.shape
+    need = [(L + page_size - 1) // page_size for L in lens]
+    P = sum(need) + spare
+    perm = np.random.default_rng(seed).permutation(P)
+    max_pages = max(1, (S + page_size - 1) // page_size)
+    bt = np.full((B, max_pages), -1, np.int32)
+    kp = np.full((P, page_size, KVH, D), 0x7FC0, np.uint16)   # bf16 NaN everywhere unused
+    vp = np.full((P, page_size, KVH, D), 0x7FC0, np.uint16)
+    off = 0
+    for b, L in enumerate(lens):
+        for j in range(need[b]):
+            page = perm[off]
+            off += 1
+            bt[b, j] = page
+            n = min(page_size, L - j * page_size)
+            kp[page, :n] = k[b, j * page_size:j * page_size + n]
+            vp[page, :n] = v[b, j * page_size:j * page_size + n]
+    return kp, vp, bt
+
+
+@pytest.mark.parametrize("H,KVH,D,W", [(32, 16, 16, 0), (32, 16, 16, 20), (32, 4, 32, 0)])
+def test_paged_equals_contiguous(oracle_lib, H, KVH, D, W):
+    """A permuted page table holding the same rows gives the identical result, and
+    NaN in every slot no attended position maps to changes nothing."""
+    B, S = 4, 70
+    q, k, v = random_case(B, S, H, KVH, D, seed=14)
+    lens = [70, 33, 16, 1]
+    kp, vp, bt = scatter_to_pages(k, v, lens)
+    paged = oracle_lib.gqa_decode_paged_f64(q, kp, vp, bt, lens, W)
+    contig = oracle_lib.gqa_decode_f64(q, k, v, lens, W)
+    assert np.array_equal(paged, contig)
+
+
+def test_paged_bad_page_id_gives_nan_for_that_sequence(oracle_lib):
+    B, S, H, KVH, D = 3, 40, 8, 2, 16
+    q, k, v = random_case(B, S, H, KVH, D, seed=15)
+    lens = [40, 40, 40]
+    kp, vp, bt = scatter_to_pages(k, v, lens)
+    bt[1, 1] = kp.shape[0] + 5
+    out = oracle_lib.gqa_decode_paged_f64(q, kp, vp, bt, lens, 0)
+    assert np.all(np.isnan(out[1]))
+    assert np.all(np.isfinite(out[0])) and np.all(np.isfinite(out[2]))
+    # a bad id on a page the window never reaches is never looked at
+    bt2 = bt.copy(); bt2[1, 1] = bt[0, 1]
+    bt2[2, 0] = -7
+    out2 = oracle_lib.gqa_decode_paged_f64(q, kp, vp, bt2, lens, 16)
+    assert np.all(np.isfinite(out2))
+
+
+def test_oracle_rejects_ranges_outside_the_cache(oracle_lib):
+    q, k, v = random_case(1, 8, 4, 2, 8, seed=16)
+    with pytest.raises(ValueError):
+        oracle_lib.gqa_decode_f64(q, k, v, [9], 0)
+    with pytest.raises(ValueError):
+        oracle_lib.gqa_decode_f64(q, k, v, [-1], 0)
+    with pytest.raises(ValueError):   # window start before pos_base
+        oracle_lib.gqa_decode_f64(q, k, v, [8], 0, pos_base=1)
+
+
+def test_thread_count_does_not_change_results(oracle_lib):
+    q, k, v = random_case(2, 64, 32, 4, 64, seed=17)
+    a = oracle_lib.gqa_decode_f64(q, k, v, [64, 50], 0, nthreads=1)
+    b = oracle_lib.gqa_decode_f64(q, k, v, [64, 50], 0, nthreads=4)
+    assert np.array_equal(a, b)
