@@ -1,0 +1,202 @@
+"""ctypes binding of libgqadecode.so -- argument marshalling only.
+
+Every function here has the name of the C entry point it calls (include/gqa_decode.h)
+and does nothing but check tensor metadata, pick the current CUDA stream and pass
+raw device pointers.  All of the attention arithmetic runs in the library's CUDA
+kernels; there is no fallback: if the library cannot be built or loaded, the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+GQA_OK = 0
+GQA_ERR_INVALID_ARGUMENT = 1
+GQA_ERR_UNSUPPORTED = 2
+GQA_ERR_WORKSPACE = 3
+GQA_ERR_CUDA = 4
+
+GQA_OUT_BF16 = 0
+GQA_OUT_F32 = 1
+
+GQA_DEVICE_WAIT_TIMEOUT = 1
+GQA_DEVICE_BAD_PAGE = 2
+GQA_DEVICE_BAD_LENGTH = 4
+
+PAGE_SIZE = 16
+
+EXPORTED_SYMBOLS = ("gqa_workspace_size", "gqa_workspace_init", "gqa_decode", "gqa_decode_paged",
+                    "gqa_device_status", "gqa_status_string")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GQAError(RuntimeError):
+    """A gqa_* call returned a status other than GQA_OK."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {gqa_status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_needed: bool = True) -> ctypes.CDLL:
+    """Load libgqadecode.so (building it first when missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_needed and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(_build.LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {_build.LIB_PATH}")
+        lib = ctypes.CDLL(_build.LIB_PATH)
+        vp, sz, ci = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        lib.gqa_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
+        lib.gqa_workspace_size.restype = sz
+        lib.gqa_workspace_init.argtypes = [vp, sz, vp]
+        lib.gqa_workspace_init.restype = ci
+        lib.gqa_decode.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, ci, vp, sz, vp]
+        lib.gqa_decode.restype = ci
+        lib.gqa_decode_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, vp,
+                                         ci, vp, sz, vp]
+        lib.gqa_decode_paged.restype = ci
+        lib.gqa_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+        lib.gqa_device_status.restype = ci
+        lib.gqa_status_string.argtypes = [ci]
+        lib.gqa_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def gqa_status_string(status: int) -> str:
+    return load_library().gqa_status_string(int(status)).decode()
+
+
+def gqa_workspace_size(B: int, max_seq: int, H: int, KVH: int, D: int, window: int) -> int:
+    return int(load_library().gqa_workspace_size(B, max_seq, H, KVH, D, window))
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check(fn: str, status: int):
+    if status != GQA_OK:
+        raise GQAError(fn, status)
+
+
+def gqa_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    """Zero a caller-owned workspace before its first use."""
+    st = load_library().gqa_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                           _stream_handle(stream, workspace.device))
+    _check("gqa_workspace_init", st)
+
+
+def new_workspace(B: int, max_seq: int, H: int, KVH: int, D: int, window: int,
+                  device=None, stream=None) -> torch.Tensor:
+    """Allocate (torch caching allocator) and zero a workspace for this call shape."""
+    n = gqa_workspace_size(B, max_seq, H, KVH, D, window)
+    if n == 0:
+        raise GQAError("gqa_workspace_size", GQA_ERR_INVALID_ARGUMENT)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    gqa_workspace_init(ws, stream)
+    return ws
+
+
+def _out_code(out: torch.Tensor) -> int:
+    if out.dtype == torch.float32:
+        return GQA_OUT_F32
+    if out.dtype == torch.bfloat16:
+        return GQA_OUT_BF16
+    raise TypeError("out must be bf16 or fp32")
+
+
+def _require(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _check_tensor(name, t, dtype, ndim):
+    _require(isinstance(t, torch.Tensor), f"{name} must be a torch.Tensor")
+    _require(t.is_cuda, f"{name} must be on a CUDA device")
+    _require(t.dtype == dtype, f"{name} must be {dtype}")
+    _require(t.dim() == ndim, f"{name} must have {ndim} dims")
+    _require(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def gqa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
+               window: int, out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+               workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """attn.core over a contiguous cache: q [B,H,D], k/v [B,S,KVH,D] (bf16), seq_lens int32 [B]."""
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("k", k, torch.bfloat16, 4)
+    _check_tensor("v", v, torch.bfloat16, 4)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    B, H, D = q.shape
+    _, S, KVH, _ = k.shape
+    _require(tuple(k.shape) == (B, S, KVH, D) and v.shape == k.shape, "k/v shape mismatch")
+    _require(seq_lens.shape[0] == B, "seq_lens must have B entries")
+    if out is None:
+        out = torch.empty((B, H, D), dtype=out_dtype, device=q.device)
+    _check_tensor("out", out, out.dtype, 3)
+    _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().gqa_decode(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, S, H, KVH, D, int(window), _ptr(out),
+        _out_code(out), _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
+    _check("gqa_decode", st)
+    return out
+
+
+def gqa_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                     block_table: torch.Tensor, seq_lens: torch.Tensor, window: int,
+                     out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """attn.core over a paged cache: pools [P,16,KVH,D], block_table int32 [B,max_pages]."""
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("k_pages", k_pages, torch.bfloat16, 4)
+    _check_tensor("v_pages", v_pages, torch.bfloat16, 4)
+    _check_tensor("block_table", block_table, torch.int32, 2)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    B, H, D = q.shape
+    P, page_size, KVH, _ = k_pages.shape
+    _require(v_pages.shape == k_pages.shape and k_pages.shape[3] == D, "page pool shape mismatch")
+    _require(block_table.shape[0] == B and seq_lens.shape[0] == B, "batch size mismatch")
+    if out is None:
+        out = torch.empty((B, H, D), dtype=out_dtype, device=q.device)
+    _check_tensor("out", out, out.dtype, 3)
+    _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().gqa_decode_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), B, P,
+        block_table.shape[1], page_size, H, KVH, D, int(window), _ptr(out), _out_code(out),
+        _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
+    _check("gqa_decode_paged", st)
+    return out
+
+
+def gqa_device_status(workspace: torch.Tensor | None = None, stream=None) -> int:
+    """Read and clear the device status word (GQA_DEVICE_* bits); synchronises the stream."""
+    flags = ctypes.c_uint32(0)
+    dev = workspace.device if workspace is not None else torch.device("cuda", torch.cuda.current_device())
+    st = load_library().gqa_device_status(_ptr(workspace), ctypes.byref(flags),
+                                          _stream_handle(stream, dev))
+    _check("gqa_device_status", st)
+    return int(flags.value)

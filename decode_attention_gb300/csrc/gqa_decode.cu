@@ -1,0 +1,296 @@
+// C ABI of libgqadecode.so: argument checks, workspace handling, TMA tensor
+// maps and the kernel launch.  See include/gqa_decode.h for the contract.
+//
+// Operation: the decode-step attention core `attn.core` of gemma-4-31B (Model
+// Spec, "Compute-graph nodes", the slidingDecodeGQA and decodeGQA rows; tensor
+// shapes from "Tensors of the main nodes"; 16-position pages from "At a glance",
+// Shape domain row).
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "gqa_decode.h"
+#include "launch.h"
+
+namespace {
+
+using gqa::kMaxCtas;
+
+enum class Geometry { kNone, kSliding, kGlobal };
+
+Geometry geometry_of(int H, int KVH, int D) {
+    if (H == 32 && KVH == 16 && D == 256) return Geometry::kSliding;   // slidingDecodeGQA
+    if (H == 32 && KVH == 4 && D == 512) return Geometry::kGlobal;     // decodeGQA
+    return Geometry::kNone;
+}
+
+int heads_per_kv(Geometry g) { return g == Geometry::kSliding ? 2 : 8; }
+
+// ---- workspace layout --------------------------------------------------------
+// [0, 256)            status word (uint32) + reserved
+// [256, 16640)        per-(b, kvh) arrival counters, 4096 x uint32
+// [ml_off, ...)       softmax partial (m, l): slots x G x 2 floats
+// [acc_off, ...)      softmax partial acc:    slots x G x D floats
+// slots = kMaxCtas + B * KVH bounds the pieces one call can store (CTA i stores
+// the piece of segment u at slot i + u).
+constexpr size_t kFlagsOff = 0;
+constexpr size_t kCountersOff = 256;
+constexpr size_t kMaxSegments = static_cast<size_t>(GQA_MAX_BATCH) * 16;
+constexpr size_t kHeaderBytes = kCountersOff + kMaxSegments * sizeof(uint32_t);
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WorkspaceLayout {
+    size_t ml_off, acc_off, total;
+};
+
+WorkspaceLayout layout_for(int B, int KVH, int G, int D) {
+    const size_t slots = static_cast<size_t>(kMaxCtas) + static_cast<size_t>(B) * KVH;
+    WorkspaceLayout w;
+    w.ml_off = align256(kHeaderBytes);
+    w.acc_off = align256(w.ml_off + slots * G * 2 * sizeof(float));
+    w.total = align256(w.acc_off + slots * G * D * sizeof(float));
+    return w;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---- per-device state -----------------------------------------------------------
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::mutex mu;
+    int sm_count = 0;
+    void* ws = nullptr;          // library-owned workspace
+    size_t ws_bytes = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// 4-D view of a K or V cache for 16-row TMA boxes of one KV head, 128-byte
+// swizzled in shared memory as [D/64 chunks][16 rows][64 elements]:
+//   dim 0: 64 elements of the head dim (contiguous)
+//   dim 1: 16-row axis -- cache positions (contiguous) or page slots (paged)
+//   dim 2: 64-element chunk of the KVH*D row (stride 128 B)
+//   dim 3: sequence (contiguous) or page (paged)
+bool encode_kv_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t outer, int KVH,
+                   int D) {
+    const uint64_t row_bytes = static_cast<uint64_t>(KVH) * D * 2;
+    cuuint64_t dims[4] = {64, rows, static_cast<cuuint64_t>(KVH) * (D / 64), outer};
+    cuuint64_t strides[3] = {row_bytes, 128, row_bytes * rows};
+    cuuint32_t box[4] = {64, gqa::kBoxRows, static_cast<cuuint32_t>(D / 64), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct CallShape {
+    Geometry geo;
+    int B, H, KVH, D, window;
+};
+
+gqa_status_t check_common(const CallShape& c, const void* q, const void* out,
+                          const int32_t* seq_lens, gqa_out_dtype_t out_dtype) {
+    if (c.B < 0 || c.B > GQA_MAX_BATCH || c.window < 0) return GQA_ERR_INVALID_ARGUMENT;
+    if (out_dtype != GQA_OUT_BF16 && out_dtype != GQA_OUT_F32) return GQA_ERR_INVALID_ARGUMENT;
+    if (c.geo == Geometry::kNone) return GQA_ERR_UNSUPPORTED;
+    if (c.B == 0) return GQA_OK;
+    if (!q || !out || !seq_lens) return GQA_ERR_INVALID_ARGUMENT;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(seq_lens, 4))
+        return GQA_ERR_INVALID_ARGUMENT;
+    return GQA_OK;
+}
+
+// Resolves the workspace (caller's or library-owned) and the device's SM count.
+gqa_status_t prepare(const CallShape& c, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream, void** ws_out, WorkspaceLayout* lay, int* grid) {
+    const int G = heads_per_kv(c.geo);
+    *lay = layout_for(c.B, c.KVH, G, c.D);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+    DeviceState& ds = g_dev[dev];
+    std::lock_guard<std::mutex> lock(ds.mu);
+    if (ds.sm_count == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return GQA_ERR_CUDA;
+        ds.sm_count = n;
+    }
+    *grid = ds.sm_count < kMaxCtas ? ds.sm_count : kMaxCtas;
+    if (workspace) {
+        if (workspace_bytes < lay->total || !aligned(workspace, 256)) return GQA_ERR_WORKSPACE;
+        *ws_out = workspace;
+        return GQA_OK;
+    }
+    if (ds.ws_bytes < lay->total) {
+        if (ds.ws) {
+            cudaFree(ds.ws);   // synchronises the device: no call still uses it
+            ds.ws = nullptr;
+            ds.ws_bytes = 0;
+        }
+        void* p = nullptr;
+        if (cudaMalloc(&p, lay->total) != cudaSuccess) return GQA_ERR_CUDA;
+        if (cudaMemsetAsync(p, 0, lay->total, stream) != cudaSuccess) {
+            cudaFree(p);
+            return GQA_ERR_CUDA;
+        }
+        ds.ws = p;
+        ds.ws_bytes = lay->total;
+    }
+    *ws_out = ds.ws;
+    return GQA_OK;
+}
+
+gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, const void* v,
+                 const int32_t* block_table, const int32_t* seq_lens, uint64_t rows,
+                 uint64_t outer, int capacity, int num_pages, int max_pages, void* out,
+                 gqa_out_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream) {
+    if (!get_encode_fn()) return GQA_ERR_CUDA;
+    void* ws = nullptr;
+    WorkspaceLayout lay;
+    int grid = 0;
+    gqa_status_t st = prepare(c, workspace, workspace_bytes, stream, &ws, &lay, &grid);
+    if (st != GQA_OK) return st;
+
+    gqa::LaunchArgs a;
+    std::memset(&a, 0, sizeof a);
+    if (!encode_kv_map(&a.tm_k, k, rows, outer, c.KVH, c.D)) return GQA_ERR_CUDA;
+    if (!encode_kv_map(&a.tm_v, v, rows, outer, c.KVH, c.D)) return GQA_ERR_CUDA;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    a.p.q = static_cast<const __nv_bfloat16*>(q);
+    a.p.seq_lens = seq_lens;
+    a.p.block_table = block_table;
+    a.p.out = out;
+    a.p.ws_acc = reinterpret_cast<float*>(w + lay.acc_off);
+    a.p.ws_ml = reinterpret_cast<float*>(w + lay.ml_off);
+    a.p.ws_counters = reinterpret_cast<uint32_t*>(w + kCountersOff);
+    a.p.ws_flags = reinterpret_cast<uint32_t*>(w + kFlagsOff);
+    a.p.B = c.B;
+    a.p.H = c.H;
+    a.p.KVH = c.KVH;
+    a.p.capacity = capacity;
+    a.p.window = c.window;
+    a.p.num_pages = num_pages;
+    a.p.max_pages = max_pages;
+    a.p.out_f32 = out_dtype == GQA_OUT_F32 ? 1 : 0;
+    a.grid = grid;
+    a.stream = stream;
+    const cudaError_t e = c.geo == Geometry::kSliding ? gqa::launch_sliding(a, paged)
+                                                      : gqa::launch_global(a, paged);
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gqa_workspace_size(int B, int max_seq, int H, int KVH, int D, int window) {
+    const Geometry geo = geometry_of(H, KVH, D);
+    if (geo == Geometry::kNone || B < 0 || B > GQA_MAX_BATCH || max_seq < 1 ||
+        max_seq > GQA_MAX_SEQ || window < 0)
+        return 0;
+    return layout_for(B, KVH, heads_per_kv(geo), D).total;
+}
+
+gqa_status_t gqa_workspace_init(void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
+    if (!workspace || workspace_bytes == 0) return GQA_ERR_INVALID_ARGUMENT;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? GQA_OK
+               : GQA_ERR_CUDA;
+}
+
+gqa_status_t gqa_decode(const void* q, const void* k, const void* v, const int32_t* seq_lens,
+                        int B, int S, int H, int KVH, int D, int window, void* out,
+                        gqa_out_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
+                        gqa_stream_t stream) {
+    const CallShape c{geometry_of(H, KVH, D), B, H, KVH, D, window};
+    if (S < 1 || S > GQA_MAX_SEQ) return GQA_ERR_INVALID_ARGUMENT;
+    gqa_status_t st = check_common(c, q, out, seq_lens, out_dtype);
+    if (st != GQA_OK || B == 0) return st;
+    if (!k || !v || !aligned(k, 16) || !aligned(v, 16)) return GQA_ERR_INVALID_ARGUMENT;
+    return run(c, false, q, k, v, nullptr, seq_lens, static_cast<uint64_t>(S),
+               static_cast<uint64_t>(B), S, 0, 0, out, out_dtype, workspace, workspace_bytes,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                              const int32_t* block_table, const int32_t* seq_lens, int B, int P,
+                              int max_pages, int page_size, int H, int KVH, int D, int window,
+                              void* out, gqa_out_dtype_t out_dtype, void* workspace,
+                              size_t workspace_bytes, gqa_stream_t stream) {
+    const CallShape c{geometry_of(H, KVH, D), B, H, KVH, D, window};
+    if (page_size != GQA_PAGE_SIZE || P < 1 || max_pages < 1 ||
+        static_cast<int64_t>(max_pages) * GQA_PAGE_SIZE > GQA_MAX_SEQ)
+        return GQA_ERR_INVALID_ARGUMENT;
+    gqa_status_t st = check_common(c, q, out, seq_lens, out_dtype);
+    if (st != GQA_OK || B == 0) return st;
+    if (!k_pages || !v_pages || !block_table || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+        !aligned(block_table, 4))
+        return GQA_ERR_INVALID_ARGUMENT;
+    return run(c, true, q, k_pages, v_pages, block_table, seq_lens, GQA_PAGE_SIZE,
+               static_cast<uint64_t>(P), max_pages * GQA_PAGE_SIZE, P, max_pages, out, out_dtype,
+               workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t gqa_device_status(void* workspace, uint32_t* flags, gqa_stream_t stream) {
+    if (!flags) return GQA_ERR_INVALID_ARGUMENT;
+    *flags = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!workspace) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+            return GQA_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(g_dev[dev].mu);
+        workspace = g_dev[dev].ws;
+        if (!workspace) return cudaStreamSynchronize(s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GQA_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, static_cast<uint8_t*>(workspace) + kFlagsOff, sizeof word,
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemsetAsync(workspace, 0, kHeaderBytes, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return GQA_ERR_CUDA;
+    }
+    *flags = word;
+    return GQA_OK;
+}
+
+const char* gqa_status_string(gqa_status_t status) {
+    switch (status) {
+        case GQA_OK: return "GQA_OK";
+        case GQA_ERR_INVALID_ARGUMENT: return "GQA_ERR_INVALID_ARGUMENT";
+        case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED";
+        case GQA_ERR_WORKSPACE: return "GQA_ERR_WORKSPACE";
+        case GQA_ERR_CUDA: return "GQA_ERR_CUDA";
+    }
+    return "GQA_ERR_UNKNOWN";
+}
+
+}  // extern "C"

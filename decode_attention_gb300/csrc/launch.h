@@ -1,0 +1,31 @@
+// Internal interface between the C-ABI host code and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kernels/decode_kernel.cuh"
+
+namespace gqa {
+
+// Grid size bound used to size workspaces independently of the device.
+constexpr int kMaxCtas = 1024;
+
+struct LaunchArgs {
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+    DecodeParams p;
+    int grid;
+    cudaStream_t stream;
+};
+
+// Kernel launchers, one translation unit per geometry.  Each sets its kernels'
+// shared-memory limit on first use on a device and launches one persistent grid.
+cudaError_t launch_sliding(const LaunchArgs& a, bool paged);
+cudaError_t launch_global(const LaunchArgs& a, bool paged);
+
+// Bytes of dynamic shared memory each geometry's kernel requests.
+size_t smem_bytes_sliding();
+size_t smem_bytes_global();
+
+}  // namespace gqa

@@ -1,0 +1,163 @@
+/*
+ * gqa_decode.h -- C ABI of libgqadecode.so, the GB300 (sm_103a) decode-step
+ * attention core of the Gemma-4-31B text decoder.
+ *
+ * Operation (gemma-4-31B Model Spec, "Compute-graph nodes" table, the two
+ * `attn.core` rows; tensor shapes from "Tensors of the main nodes", `attn.core`
+ * row; masks and append-before-attend from the "Gemma 4 31B-it Text
+ * Architecture" page, "Compact form"):
+ *
+ *   for each sequence b < B and query head h < H, with g = H / KVH and
+ *   kvh = floor(h / g):
+ *     attended positions  A_b = [lo_b, L_b),  L_b = seq_lens[b],
+ *                         lo_b = max(0, L_b - window) if window > 0, else 0
+ *     o[b,h,:] = sum_{s in A_b} w_s * v[b,s,kvh,:],
+ *     w_s      = exp(<q[b,h,:], k[b,s,kvh,:]>) / sum_{s' in A_b} exp(<q[b,h,:], k[b,s',kvh,:]>)
+ *
+ *   The attention scale is exactly 1 (no 1/sqrt(D)) and there is no logit
+ *   soft-cap (the Model Spec applies its soft-cap to the final logits only).
+ *   seq_lens[b] counts the current token, whose K/V row is already in the cache
+ *   (the query sits at position L_b - 1).  An empty range (L_b == 0) gives o = 0.
+ *
+ *   Supported geometries (the two attn.core rows):
+ *     slidingDecodeGQA: H = 32, KVH = 16, D = 256, window = 1024 (any window >= 0 accepted)
+ *     decodeGQA:        H = 32, KVH =  4, D = 512, window = 0    (any window >= 0 accepted)
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is DEVICE memory of the current CUDA device, owned by
+ *     the caller.  The library keeps no pointer past the call.
+ *   - bf16 means IEEE bfloat16 (1-8-7), row-major, densely packed, 16-byte
+ *     aligned base address.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).  Host-side
+ *     argument checks happen before anything is enqueued; a failed check
+ *     returns an error and enqueues nothing.
+ *   - Data-dependent problems are not trapped.  seq_lens and block tables live on
+ *     the device and are never read by the host: a length outside
+ *     [0, capacity] is clamped into it, and a block-table entry outside [0, P)
+ *     on an attended page turns that sequence's output into NaN.  Both raise a
+ *     bit in the device status word (gqa_device_status).
+ *   - Results are deterministic: the same inputs on the same GPU model give
+ *     bit-identical outputs (no floating-point atomics).
+ */
+#ifndef GQA_DECODE_H
+#define GQA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle (cudaStream_t is `struct CUstream_st *`). */
+typedef struct CUstream_st *gqa_stream_t;
+
+typedef enum {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, size out of the shape domain */
+    GQA_ERR_UNSUPPORTED = 2,      /* (H, KVH, D) is not one of the two attn.core geometries */
+    GQA_ERR_WORKSPACE = 3,        /* caller workspace smaller than gqa_workspace_size() */
+    GQA_ERR_CUDA = 4              /* a CUDA runtime/driver call failed (launch, allocation, ...) */
+} gqa_status_t;
+
+typedef enum {
+    GQA_OUT_BF16 = 0, /* o written as bf16 (round to nearest even from the fp32 result) */
+    GQA_OUT_F32 = 1   /* o written as fp32 */
+} gqa_out_dtype_t;
+
+/* Bits of the device status word (see gqa_device_status). */
+#define GQA_DEVICE_WAIT_TIMEOUT 1u /* a pipeline wait gave up after ~2 s; outputs invalid */
+#define GQA_DEVICE_BAD_PAGE 2u     /* an attended block-table entry was outside [0, P) */
+#define GQA_DEVICE_BAD_LENGTH 4u   /* a seq_lens entry was outside [0, capacity] and was clamped */
+
+/* Limits of the shape domain (Model Spec, "At a glance" table, Shape domain row:
+ * B in [1, 256], S in [1, 262144], page size 16). */
+#define GQA_MAX_BATCH 256
+#define GQA_MAX_SEQ 262144
+#define GQA_PAGE_SIZE 16
+
+/*
+ * Bytes of device scratch that one call with these sizes needs when the caller
+ * supplies the workspace (split-softmax partials, per-(b,kvh) arrival counters
+ * and the device status word).  The bound depends on B, H, KVH and D only; S and
+ * window are accepted so callers can pass the full call shape.  Returns 0 when
+ * the arguments are outside the supported domain (the matching gqa_decode call
+ * would fail its argument check).  Pure host arithmetic: no CUDA call.
+ */
+size_t gqa_workspace_size(int B, int max_seq, int H, int KVH, int D, int window);
+
+/*
+ * Prepare a caller-owned workspace for first use: zero-fills `workspace_bytes`
+ * bytes on `stream`.  Required once before the first gqa_decode* call that uses
+ * the workspace, and again after gqa_device_status reported a nonzero word.
+ * Every completed call leaves the workspace ready for the next one.
+ */
+gqa_status_t gqa_workspace_init(void *workspace, size_t workspace_bytes, gqa_stream_t stream);
+
+/*
+ * attn.core over a contiguous KV cache.
+ *
+ *   q         bf16 [B, H, D]
+ *   k, v      bf16 [B, S, KVH, D]; row s of sequence b is cache position s.
+ *             k and v may alias (both are only read).
+ *   seq_lens  int32 [B] (device), L_b in [0, S]
+ *   window    0 = full history (decodeGQA); > 0 = the last `window` positions
+ *             (slidingDecodeGQA uses 1024)
+ *   out       [B, H, D], bf16 or fp32 per out_dtype; must not overlap the inputs
+ *   workspace device scratch of at least gqa_workspace_size(B, S, H, KVH, D, window)
+ *             bytes, prepared by gqa_workspace_init; NULL = use a library-owned
+ *             per-device buffer (grown on demand with cudaMalloc, which
+ *             synchronises the device; calls that share it must not run
+ *             concurrently on different streams)
+ *
+ * Only positions in [lo_b, L_b) are read from k and v; q, k, v, seq_lens are
+ * never written.  B == 0 is a valid empty batch: GQA_OK, nothing enqueued.
+ * Errors: GQA_ERR_INVALID_ARGUMENT (null or non-16-byte-aligned pointer,
+ * B outside [0, 256], S outside [1, 262144], window < 0, unknown out_dtype),
+ * GQA_ERR_UNSUPPORTED, GQA_ERR_WORKSPACE, GQA_ERR_CUDA.
+ */
+gqa_status_t gqa_decode(const void *q, const void *k, const void *v, const int32_t *seq_lens,
+                        int B, int S, int H, int KVH, int D, int window, void *out,
+                        gqa_out_dtype_t out_dtype, void *workspace, size_t workspace_bytes,
+                        gqa_stream_t stream);
+
+/*
+ * attn.core over a paged KV cache (16-position pages, Model Spec "At a glance",
+ * Shape domain row).
+ *
+ *   q                 bf16 [B, H, D]
+ *   k_pages, v_pages  bf16 [P, 16, KVH, D]: page p, slot j holds one cache
+ *                     position for every KV head
+ *   block_table       int32 [B, max_pages] (device): position s of sequence b is
+ *                     slot s % 16 of page block_table[b, s / 16].  Only the
+ *                     entries of pages that hold attended positions are read;
+ *                     the rest may hold anything (e.g. -1).
+ *   seq_lens          int32 [B] (device), L_b in [0, 16 * max_pages]
+ *   page_size         must be 16
+ *   other arguments   as for gqa_decode
+ *
+ * Errors as for gqa_decode, plus GQA_ERR_INVALID_ARGUMENT for P < 1,
+ * max_pages < 1, 16 * max_pages > 262144, or page_size != 16.
+ */
+gqa_status_t gqa_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                              const int32_t *block_table, const int32_t *seq_lens, int B, int P,
+                              int max_pages, int page_size, int H, int KVH, int D, int window,
+                              void *out, gqa_out_dtype_t out_dtype, void *workspace,
+                              size_t workspace_bytes, gqa_stream_t stream);
+
+/*
+ * Read and clear the device status word of a workspace (NULL = the library-owned
+ * workspace of the current device).  Synchronises `stream`, then stores the OR
+ * of the GQA_DEVICE_* bits raised by the calls since the last read into *flags.
+ * When the word is nonzero the workspace is re-zeroed before returning.
+ */
+gqa_status_t gqa_device_status(void *workspace, uint32_t *flags, gqa_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *gqa_status_string(gqa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_DECODE_H */

@@ -1,0 +1,132 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+function ``include/gqa_decode.h`` declares, and the host-side argument checks
+return the documented status before anything touches the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import decode_attention_gb300 as gqa
+from decode_attention_gb300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa_decode.h")
+
+# Aligned addresses that are never dereferenced: every call below fails its host
+# checks (or is an empty batch) before any CUDA call.
+FAKE = 0x10000
+SLIDING = (32, 16, 256)
+GLOBAL = (32, 4, 512)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return gqa.load_library()
+
+
+def test_header_declares_the_exported_api():
+    assert declared_functions() == sorted(_native.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "GQA_OK"), (1, "GQA_ERR_INVALID_ARGUMENT"), (2, "GQA_ERR_UNSUPPORTED"),
+                       (3, "GQA_ERR_WORKSPACE"), (4, "GQA_ERR_CUDA")]:
+        assert gqa.gqa_status_string(code) == name
+    assert gqa.gqa_status_string(99) == "GQA_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    s = gqa.gqa_workspace_size(64, 32768, *SLIDING, 1024)
+    g = gqa.gqa_workspace_size(16, 131072, *GLOBAL, 0)
+    assert s > 0 and g > 0 and s % 256 == 0 and g % 256 == 0
+    # grows with the batch, independent of the sequence capacity
+    assert gqa.gqa_workspace_size(65, 32768, *SLIDING, 1024) > s
+    assert gqa.gqa_workspace_size(64, 10, *SLIDING, 1024) == s
+    # outside the domain -> 0
+    assert gqa.gqa_workspace_size(1, 100, 32, 8, 256, 0) == 0
+    assert gqa.gqa_workspace_size(257, 100, *SLIDING, 0) == 0
+    assert gqa.gqa_workspace_size(1, 0, *SLIDING, 0) == 0
+    assert gqa.gqa_workspace_size(1, 262145, *SLIDING, 0) == 0
+    assert gqa.gqa_workspace_size(1, 100, *SLIDING, -1) == 0
+
+
+def call_decode(lib, B=2, S=64, geo=SLIDING, window=0, q=FAKE, k=FAKE, v=FAKE, lens=FAKE,
+                out=FAKE, dtype=1, ws=None, ws_bytes=0):
+    H, KVH, D = geo
+    return lib.gqa_decode(q, k, v, lens, B, S, H, KVH, D, window, out, dtype, ws, ws_bytes, None)
+
+
+def call_paged(lib, B=2, P=8, max_pages=4, page_size=16, geo=GLOBAL, window=0, q=FAKE, kp=FAKE,
+               vp=FAKE, bt=FAKE, lens=FAKE, out=FAKE, dtype=0):
+    H, KVH, D = geo
+    return lib.gqa_decode_paged(q, kp, vp, bt, lens, B, P, max_pages, page_size, H, KVH, D, window,
+                                out, dtype, None, 0, None)
+
+
+def test_unsupported_geometry(lib):
+    assert call_decode(lib, geo=(32, 8, 256)) == gqa.GQA_ERR_UNSUPPORTED
+    assert call_decode(lib, geo=(16, 4, 512)) == gqa.GQA_ERR_UNSUPPORTED
+    assert call_decode(lib, geo=(32, 4, 256)) == gqa.GQA_ERR_UNSUPPORTED
+    assert call_paged(lib, geo=(32, 16, 512)) == gqa.GQA_ERR_UNSUPPORTED
+
+
+def test_invalid_arguments(lib):
+    E = gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call_decode(lib, q=None) == E
+    assert call_decode(lib, k=None) == E
+    assert call_decode(lib, v=None) == E
+    assert call_decode(lib, lens=None) == E
+    assert call_decode(lib, out=None) == E
+    assert call_decode(lib, q=FAKE + 8) == E          # q not 16-byte aligned
+    assert call_decode(lib, k=FAKE + 2) == E
+    assert call_decode(lib, out=FAKE + 4) == E
+    assert call_decode(lib, lens=FAKE + 2) == E       # int32 misaligned
+    assert call_decode(lib, B=-1) == E
+    assert call_decode(lib, B=257) == E
+    assert call_decode(lib, S=0) == E
+    assert call_decode(lib, S=262145) == E
+    assert call_decode(lib, window=-5) == E
+    assert call_decode(lib, dtype=7) == E
+
+
+def test_invalid_paged_arguments(lib):
+    E = gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call_paged(lib, page_size=32) == E
+    assert call_paged(lib, P=0) == E
+    assert call_paged(lib, max_pages=0) == E
+    assert call_paged(lib, max_pages=16385) == E       # 16 * max_pages above the shape domain
+    assert call_paged(lib, bt=None) == E
+    assert call_paged(lib, kp=FAKE + 8) == E
+    assert call_paged(lib, bt=FAKE + 2) == E
+
+
+def test_empty_batch_is_a_no_op(lib):
+    # B == 0: nothing to read or write, nothing enqueued (pointers are not examined)
+    assert call_decode(lib, B=0, q=None, k=None, v=None, lens=None, out=None) == gqa.GQA_OK
+    assert call_paged(lib, B=0, q=None, kp=None, vp=None, bt=None, lens=None, out=None) == gqa.GQA_OK
+
+
+def test_other_entry_points_reject_null(lib):
+    assert lib.gqa_workspace_init(None, 1024, None) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert lib.gqa_device_status(None, None, None) == gqa.GQA_ERR_INVALID_ARGUMENT
+
+
+def test_python_binding_validates_before_calling():
+    import torch
+    q = torch.zeros(2, 32, 256, dtype=torch.bfloat16)
+    k = torch.zeros(2, 8, 16, 256, dtype=torch.bfloat16)
+    lens = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(ValueError):     # CPU tensors are refused, no fallback
+        gqa.gqa_decode(q, k, k, lens, 1024)
