@@ -122,6 +122,12 @@ WORKLOADS = {
                  "sigma 1) clipped to [1, 65536]; one sliding and one global call",
                  B=256, S=65536, seed=4, lengths=lengths_lognormal(4096, 1.0, 1, 65536, 256),
                  layers=("sliding", "global"), paged=True),
+        # Smaller instance of the batched sliding shape for profiler captures: the same
+        # bytes per call as sliding_b64_s32768 (every sequence reads its full 1024-position
+        # window) with a 2 GB cache instead of 34 GB.
+        Workload("sliding_b64_s2048", "slidingDecodeGQA batched, B=64, every seq_len 2048 "
+                 "(profiling size)", B=64, S=2048, seed=5, lengths=lengths_fixed(2048, 64),
+                 layers=("sliding",)),
     ]
 }
 
