@@ -31,16 +31,21 @@ Geometry geometry_of(int H, int KVH, int D) {
 int heads_per_kv(Geometry g) { return g == Geometry::kSliding ? 2 : 8; }
 
 // ---- workspace layout --------------------------------------------------------
-// [0, 256)            status word (uint32) + reserved
-// [256, 16640)        per-(b, kvh) arrival counters, 4096 x uint32
+// [0, 4)              status word (uint32)
+// [64, 68)            dynamic-chunk claim counter (zero between calls)
+// [256, 65792)        per-(b, kvh) partial lists, 4096 x int4
 // [ml_off, ...)       softmax partial (m, l): slots x G x 2 floats
 // [acc_off, ...)      softmax partial acc:    slots x G x D floats
-// slots = kMaxCtas + B * KVH bounds the pieces one call can store (CTA i stores
-// the piece of segment u at slot i + u).
+// slots = kMaxCtas + B * KVH + kMaxDynUnits bounds the partials one call can
+// store: static unit j keeps its piece of segment u at slot j + u, dynamic
+// chunk k at slot kMaxCtas + B * KVH + k.
+// The status word and the claim counter must be zero before a call; every
+// completed call leaves them so.
 constexpr size_t kFlagsOff = 0;
-constexpr size_t kCountersOff = 256;
+constexpr size_t kClaimOff = 64;
+constexpr size_t kSegsOff = 256;
 constexpr size_t kMaxSegments = static_cast<size_t>(GQA_MAX_BATCH) * 16;
-constexpr size_t kHeaderBytes = kCountersOff + kMaxSegments * sizeof(uint32_t);
+constexpr size_t kHeaderBytes = kSegsOff + kMaxSegments * 16;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -49,7 +54,8 @@ struct WorkspaceLayout {
 };
 
 WorkspaceLayout layout_for(int B, int KVH, int G, int D) {
-    const size_t slots = static_cast<size_t>(kMaxCtas) + static_cast<size_t>(B) * KVH;
+    const size_t slots = static_cast<size_t>(kMaxCtas) + static_cast<size_t>(B) * KVH +
+                         gqa::kMaxDynUnits;
     WorkspaceLayout w;
     w.ml_off = align256(kHeaderBytes);
     w.acc_off = align256(w.ml_off + slots * G * 2 * sizeof(float));
@@ -186,8 +192,10 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
     a.p.out = out;
     a.p.ws_acc = reinterpret_cast<float*>(w + lay.acc_off);
     a.p.ws_ml = reinterpret_cast<float*>(w + lay.ml_off);
-    a.p.ws_counters = reinterpret_cast<uint32_t*>(w + kCountersOff);
+    a.p.ws_segs = reinterpret_cast<int4*>(w + kSegsOff);
     a.p.ws_flags = reinterpret_cast<uint32_t*>(w + kFlagsOff);
+    a.p.ws_claim = reinterpret_cast<uint32_t*>(w + kClaimOff);
+    a.p.dyn_slot_base = kMaxCtas + c.B * c.KVH;
     a.p.B = c.B;
     a.p.H = c.H;
     a.p.KVH = c.KVH;

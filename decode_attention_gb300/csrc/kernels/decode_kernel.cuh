@@ -7,24 +7,37 @@
 // of the "Gemma 4 31B-it Text Architecture" page, "Compact form", with the
 // current token appended before attention).
 //
-// Work decomposition.  A "segment" is one (b, kvh) pair with its n_b attended
-// positions; all g query heads of that KV head are served from one read of its
-// K/V rows.  The segments are laid end to end (b-major, then kvh) into one index
-// space of N = KVH * sum_b n_b positions, and CTA i of the grid takes the equal
-// share [floor(i N / G), floor((i+1) N / G)).  Every CTA derives this plan
-// itself from seq_lens (no planning kernel, no host read of device data).  The
-// piece of a segment that falls inside one CTA is a "partial"; a segment that
-// lies inside one CTA is written straight to the output, otherwise each CTA
-// stores its (m, l, acc) softmax partial in the workspace at slot i + u and the
-// last CTA to finish a segment (an atomic ticket, no waiting) merges the
-// partials with the log-sum-exp rule and writes the output.
+// Work decomposition.  A "segment" u = (b, kvh) is one KV head of one sequence
+// with its n_b attended positions; all g query heads of that KV head are served
+// from one read of its K/V rows.  Each segment is split into a static head
+// (its first sn_b positions) and a dynamic tail of dn_b chunks of c_dyn
+// positions (dn_b grows with n_b; short segments have none).
+//   * The static heads of all segments, laid end to end (b-major, then kvh),
+//     form an index space of Ns positions; CTA i owns the static unit
+//     [floor(i Ns / Ge), floor((i+1) Ns / Ge)), Ge = min(grid, Ns).
+//   * The dynamic chunks (a few per CTA in total) are claimed with an atomic
+//     counter by whichever CTA finishes its static unit first; this absorbs the
+//     uneven per-SM memory bandwidth without letting any one segment collect
+//     many pieces.
+// Every CTA derives the plan itself from seq_lens (no planning kernel, no host
+// read of device data).  The piece of a segment inside one unit is a
+// "partial".  A segment with a single partial is written straight to the
+// output; otherwise each partial stores its (m, l, acc) softmax state in the
+// workspace (static unit j at slot j + u, dynamic chunk k at slot
+// dyn_slot_base + k) and the combine kernel (combine_kernel.cuh), launched
+// right behind this one, merges them -- static units in order, then the
+// segment's dynamic chunks in order -- with the log-sum-exp rule.  Which CTA
+// processes a unit does not change its arithmetic, so results are
+// bit-reproducible.
 //
-// Data movement.  One producer warp streams K and V tiles of TP positions through
-// a ring of shared-memory stages with TMA (one 4-D box = 16 positions x D per
-// tensor, 128-byte swizzled), completion counted on mbarriers.  The consumer
-// warps run the policy's arithmetic (CUDA cores or warp mma) on each stage and
-// release it.  Every wait is bounded (~2 s); a wait that gives up sets a status
-// bit and the kernel runs to its end without further waits or global writes.
+// Data movement.  One producer thread walks the schedule and streams K and V
+// tiles of TP positions through a ring of shared-memory stages with TMA (4-D
+// boxes of 16 positions x D, 128-byte swizzled), completion counted on
+// mbarriers; with each stage it publishes a descriptor (segment, valid rows,
+// first/last tile of a partial, workspace slot).  The consumer warps follow the
+// descriptors: policy arithmetic (CUDA cores or warp mma) per tile, epilogue
+// after the last tile of a partial.  Every wait is bounded (~2 s): a wait that
+// gives up raises a status bit and all consumer warps leave together.
 #pragma once
 
 #include <cstdint>
@@ -35,10 +48,12 @@
 
 namespace gqa {
 
-constexpr int kBoxRows = 16;         // positions per TMA box (= one 16-position page)
-constexpr int kChunkElems = 64;      // bf16 per 128-byte swizzle row
-constexpr int kChunkBytes = 2048;    // one chunk of a box: 16 rows x 128 B
+constexpr int kBoxRows = 16;          // positions per TMA box (= one 16-position page)
+constexpr int kChunkElems = 64;       // bf16 per 128-byte swizzle row
+constexpr int kChunkBytes = 2048;     // one chunk of a box: 16 rows x 128 B
 constexpr int kMaxBatch = 256;
+constexpr int kMaxDynUnits = 1024;    // bound on dynamic chunks (sizes the workspace)
+constexpr int kDynChunksPerCta = 4;   // dynamic work aimed for, in chunks per CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // a wait gives up after 2 s
 constexpr uint32_t kWaitMaxRounds = 1u << 24;        // ... or after this many polling rounds
@@ -55,8 +70,10 @@ struct DecodeParams {
     void* out;                    // [B, H, D], bf16 or fp32
     float* ws_acc;                // [slots, G, D]
     float* ws_ml;                 // [slots, G, 2]
-    uint32_t* ws_counters;        // [B * KVH]
+    int4* ws_segs;                // [B * KVH] partial list per segment (SegmentParts)
     uint32_t* ws_flags;           // device status word
+    uint32_t* ws_claim;           // dynamic-chunk claim counter (reset by the combine kernel)
+    int dyn_slot_base;            // first workspace slot of the dynamic chunks (> grid + B*KVH - 2)
     int B, H, KVH;
     int capacity;                 // S, or 16 * max_pages
     int window;                   // 0 = full history
@@ -70,51 +87,74 @@ __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x <
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
 // ---------------------------------------------------------------------------
-// Plan: per-sequence attended ranges and their prefix sums (shared memory).
+// Plan (shared memory): per-sequence ranges, static/dynamic split, prefix sums
 // ---------------------------------------------------------------------------
 
 struct PlanSmem {
-    int lo[kMaxBatch];
-    int n[kMaxBatch];
-    long long pref[kMaxBatch + 1];   // pref[b] = KVH * sum_{b' < b} n_b'
+    int lo[kMaxBatch];               // first attended position
+    int n[kMaxBatch];                // attended positions
+    int sn[kMaxBatch];               // static head length of each segment of sequence b
+    int dn[kMaxBatch];               // dynamic chunks of each segment of sequence b
+    long long spref[kMaxBatch + 1];  // KVH * sum_{b' < b} sn_b'
+    int dpref[kMaxBatch + 1];        // KVH * sum_{b' < b} dn_b'
+    long long n_static;              // Ns
+    int n_dyn;                       // dynamic chunks in total
+    int c_dyn;                       // positions per dynamic chunk
+    int g_eff;                       // static units (= CTAs with work)
 };
 
-struct Partial {
-    int b, kvh;
-    int p0, p1;               // positions [p0, p1) of this CTA's piece
-    long long seg_start;      // flattened index of the segment's first position
-    int seg_len;              // n_b
-};
+// Largest b in [0, B) with pref[b] <= x (pref non-decreasing, pref[B] > x).
+template <class T>
+__device__ __forceinline__ int upper_seq(const T* pref, int B, long long x) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<long long>(pref[mid]) <= x)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
 
-// Walks the partials of one CTA's flattened range [pos, end).
-struct PartialIter {
-    long long pos, end;
-    int b;
-    __device__ PartialIter(long long begin, long long stop) : pos(begin), end(stop), b(0) {}
-    __device__ __forceinline__ bool next(const PlanSmem& pl, int B, int KVH, Partial& pt) {
-        if (pos >= end) return false;
-        while (b < B - 1 && pl.pref[b + 1] <= pos) ++b;
-        const long long rel = pos - pl.pref[b];
-        const int nb = pl.n[b];
-        const int kvh = static_cast<int>(rel / nb);
-        const int off = static_cast<int>(rel - static_cast<long long>(kvh) * nb);
-        const long long avail = end - pos;
-        const int take = static_cast<int>(avail < (nb - off) ? avail : (nb - off));
-        pt.b = b;
-        pt.kvh = kvh;
-        pt.p0 = pl.lo[b] + off;
-        pt.p1 = pt.p0 + take;
-        pt.seg_start = pl.pref[b] + static_cast<long long>(kvh) * nb;
-        pt.seg_len = nb;
-        pos += take;
-        return true;
+__device__ __forceinline__ long long static_unit_begin(const PlanSmem& pl, int j) {
+    return static_cast<long long>(j) * pl.n_static / pl.g_eff;
+}
+// static unit containing static index x (units are floor(j Ns / Ge))
+__device__ __forceinline__ int static_unit_of(const PlanSmem& pl, long long x) {
+    return static_cast<int>(((x + 1) * pl.g_eff - 1) / pl.n_static);
+}
+
+// The partials of segment (b, kvh): static units first_s..first_s+ns_parts-1,
+// then dynamic chunks dk0..dk0+nd_parts-1.
+struct SegmentParts {
+    int first_s, ns_parts, dk0, nd_parts, dyn_base;
+    __device__ __forceinline__ SegmentParts(const PlanSmem& pl, int b, int kvh, int dyn_slot_base)
+        : dyn_base(dyn_slot_base) {
+        const long long ss = pl.spref[b] + static_cast<long long>(kvh) * pl.sn[b];
+        first_s = static_unit_of(pl, ss);
+        ns_parts = static_unit_of(pl, ss + pl.sn[b] - 1) - first_s + 1;
+        dk0 = pl.dpref[b] + kvh * pl.dn[b];
+        nd_parts = pl.dn[b];
+    }
+    __device__ __forceinline__ int count() const { return ns_parts + nd_parts; }
+    __device__ __forceinline__ size_t slot(int j, int u) const {
+        return j < ns_parts ? static_cast<size_t>(first_s + j) + u
+                            : static_cast<size_t>(dyn_base) + dk0 + (j - ns_parts);
     }
 };
 
-// CTA whose share contains flattened position x (shares are floor(i N / G)).
-__device__ __forceinline__ int cta_of(long long x, long long N, int G) {
-    return static_cast<int>(((x + 1) * G - 1) / N);
-}
+// What the producer publishes with every stage.
+struct TileDesc {
+    int b, kvh;
+    int t;          // first cache position of the tile
+    int vlo, vhi;   // rows [vlo, vhi) of the tile are attended positions of this partial
+    int slot;       // workspace slot of the partial
+    int flags;
+};
+constexpr int kDescFirst = 1;   // first tile of a partial
+constexpr int kDescLast = 2;    // last tile of a partial
+constexpr int kDescDone = 4;    // no more tiles: consumers leave
 
 // ---------------------------------------------------------------------------
 // Kernel shared memory
@@ -126,13 +166,13 @@ struct alignas(1024) KernelSmem {
     uint8_t kv[Pol::STAGES][2][kTileBytes];   // [stage][K, V][box][chunk][16 rows][128 B]
     alignas(8) uint64_t full[Pol::STAGES];
     alignas(8) uint64_t empty[Pol::STAGES];
+    TileDesc desc[Pol::STAGES];
     PlanSmem plan;
     alignas(16) float acc[Pol::G][Pol::D];    // merged partial of the current piece
     float m[Pol::G];
     float l[Pol::G];
     alignas(16) typename Pol::Scratch scratch;
     int abort_flag;
-    int last_flag;
 };
 
 // Bounded mbarrier wait.  Returns false when the CTA is aborting or the wait
@@ -169,6 +209,103 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, flo
         static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(x);
 }
 
+// Four consecutive outputs starting at idx (a multiple of 4).
+__device__ __forceinline__ void store_out4(const DecodeParams& p, size_t idx, float4 x) {
+    if (p.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + idx) = x;
+    } else {
+        __nv_bfloat162* o =
+            reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + idx);
+        o[0] = __floats2bfloat162_rn(x.x, x.y);
+        o[1] = __floats2bfloat162_rn(x.z, x.w);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Plan computation (warp 0).  Lengths are clamped to [0, capacity]; the dynamic
+// share of each segment is floor(n_b * f / c_dyn) chunks with
+// f = min(1/5, kDynChunksPerCta * grid * c_dyn / N), so all segments together
+// hold about kDynChunksPerCta chunks per CTA (capped at kMaxDynUnits).  f is
+// evaluated in fp32: every CTA runs the same instructions on the same lengths,
+// so all of them derive the same split (its exact value only sets how much
+// work is dynamic).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, int grid,
+                                           int lane) {
+    constexpr int kPer = kMaxBatch / 32;
+    const int B = p.B, KVH = p.KVH;
+    long long tot = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int b = lane * kPer + j;
+        if (b < B) tot += pl.n[b];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    const long long N = tot * KVH;
+    const long long g = N < grid ? N : grid;
+    const long long share = g > 0 ? N / g : 0;
+    long long c = (share / 4) / 32 * 32;
+    c = c < 32 ? 32 : (c > 128 ? 128 : c);
+    const bool use_dyn = share >= 128;
+    const long long target = static_cast<long long>(kDynChunksPerCta) * grid < kMaxDynUnits
+                                 ? static_cast<long long>(kDynChunksPerCta) * grid
+                                 : kMaxDynUnits;
+    // chunks per attended position of a segment: f / c_dyn
+    const float chunk_rate = target * c * 5 < N
+                                 ? static_cast<float>(target) / static_cast<float>(N)
+                                 : 0.2f / static_cast<float>(c);
+    long long sloc[kPer], srun = 0;
+    int dloc[kPer], drun = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int b = lane * kPer + j;
+        int d = 0, sn = 0;
+        if (b < B) {
+            d = use_dyn ? static_cast<int>(static_cast<float>(pl.n[b]) * chunk_rate) : 0;
+            if (d * c > pl.n[b]) d = pl.n[b] / static_cast<int>(c);
+            sn = pl.n[b] - d * static_cast<int>(c);
+            pl.sn[b] = sn;
+            pl.dn[b] = d;
+        }
+        sloc[j] = srun;
+        dloc[j] = drun;
+        srun += static_cast<long long>(sn) * KVH;
+        drun += d * KVH;
+    }
+    long long sincl = srun;
+    int dincl = drun;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long ts = __shfl_up_sync(0xffffffffu, sincl, off);
+        const int td = __shfl_up_sync(0xffffffffu, dincl, off);
+        if (lane >= off) {
+            sincl += ts;
+            dincl += td;
+        }
+    }
+    const long long sexcl = sincl - srun;
+    const int dexcl = dincl - drun;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int b = lane * kPer + j;
+        if (b <= B) {
+            pl.spref[b] = sexcl + sloc[j];
+            pl.dpref[b] = dexcl + dloc[j];
+        }
+    }
+    if (lane == 31) {
+        if (B == kMaxBatch) {
+            pl.spref[kMaxBatch] = sincl;
+            pl.dpref[kMaxBatch] = dincl;
+        }
+        pl.n_static = sincl;
+        pl.n_dyn = dincl;
+        pl.c_dyn = static_cast<int>(c);
+        pl.g_eff = static_cast<int>(sincl < grid ? sincl : grid);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -192,6 +329,7 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
     const int warp = tid >> 5, lane = tid & 31;
     const int B = p.B, KVH = p.KVH, H = p.H;
     const int cta = blockIdx.x;
+    PlanSmem& pl = sm.plan;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -205,8 +343,12 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
     }
+    // Everything above touches no global memory; from here on inputs written by
+    // earlier kernels in the stream are read.
+    ptx::grid_dependency_wait();
+    ptx::allow_dependent_launch();
 
-    // ---- plan: attended ranges, clamped lengths, prefix sums ----
+    // ---- plan: clamped lengths, attended ranges, static/dynamic split ----
     for (int b = tid; b < B; b += blockDim.x) {
         int L = p.seq_lens[b];
         if (L < 0 || L > p.capacity) {
@@ -214,81 +356,77 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
             L = L < 0 ? 0 : p.capacity;
         }
         const int lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
-        sm.plan.lo[b] = lo;
-        sm.plan.n[b] = L - lo;
+        pl.lo[b] = lo;
+        pl.n[b] = L - lo;
     }
     __syncthreads();
-    if (warp == 0) {
-        // each lane sums 8 consecutive sequences, then a warp-wide inclusive scan
-        constexpr int kPer = kMaxBatch / 32;
-        long long local[kPer];
-        long long run = 0;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int b = lane * kPer + j;
-            local[j] = run;
-            run += (b < B) ? static_cast<long long>(sm.plan.n[b]) * KVH : 0;
-        }
-        long long incl = run;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const long long t = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += t;
-        }
-        const long long excl = incl - run;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int b = lane * kPer + j;
-            if (b <= B) sm.plan.pref[b] = excl + local[j];
-        }
-        if (lane == 31 && B == kMaxBatch) sm.plan.pref[kMaxBatch] = incl;
-    }
+    if (warp == 0) build_plan(pl, p, gridDim.x, lane);
     __syncthreads();
-
-    const long long N = sm.plan.pref[B];
 
     // sequences with nothing to attend produce zeros (the empty sum)
     for (int b = cta; b < B; b += gridDim.x) {
-        if (sm.plan.n[b] != 0) continue;
+        if (pl.n[b] != 0) continue;
         const size_t base = static_cast<size_t>(b) * H * D;
         for (int i = tid; i < H * D; i += blockDim.x) store_out(p, base + i, 0.0f);
     }
-    // Work is shared by min(grid, N) CTAs so that every share is non-empty: the
-    // arrival count of a segment split over CTAs [first, last] must see one
-    // piece from each of them.
-    const int num_ctas = N < static_cast<long long>(gridDim.x) ? static_cast<int>(N) : gridDim.x;
-    if (cta >= num_ctas) return;
-
-    const long long c_begin = static_cast<long long>(cta) * N / num_ctas;
-    const long long c_end = static_cast<long long>(cta + 1) * N / num_ctas;
+    // the partial list of every segment, for the combine kernel (each CTA a slice)
+    {
+        const int U = B * KVH;
+        const int u_end = static_cast<int>(static_cast<long long>(cta + 1) * U / gridDim.x);
+        for (int u = static_cast<int>(static_cast<long long>(cta) * U / gridDim.x) + tid; u < u_end;
+             u += blockDim.x) {
+            const int b = u / KVH, kvh = u - (u / KVH) * KVH;
+            int4 e = make_int4(0, 0, 0, 0);
+            if (pl.n[b] != 0 && pl.g_eff > 0) {
+                const SegmentParts sp(pl, b, kvh, p.dyn_slot_base);
+                e = make_int4(sp.first_s, sp.ns_parts, sp.dk0, sp.nd_parts);
+            }
+            p.ws_segs[u] = e;
+        }
+    }
+    if (cta >= pl.g_eff) return;   // also covers an all-empty batch
 
     const uint32_t kv_base = ptx::smem_addr(&sm.kv[0][0][0]);
     constexpr uint32_t kStageBytes = 2u * KernelSmem<Pol>::kTileBytes;
 
     if (warp == NC) {
-        // ================= producer: one thread issues all TMA =================
+        // ================= producer: one thread walks the schedule =================
         if (lane != 0) return;
         const uint64_t policy = ptx::policy_evict_first();
-        PartialIter it(c_begin, c_end);
-        Partial pt;
         uint32_t t_idx = 0;
         bool ok = true;
-        while (ok && it.next(sm.plan, B, KVH, pt)) {
-            const int t_first = kPaged ? (pt.p0 & ~(kBoxRows - 1)) : pt.p0;
-            const int chunk0 = pt.kvh * kChunksPerRow;
+
+        // Dynamic chunks are claimed one ahead: the claim for the next chunk is
+        // issued before the last tile of the current unit, so its latency
+        // overlaps the wait for a free stage.
+        const bool dynamic = pl.n_dyn > 0;
+        int claimed = -1;   // result of the claim in flight, -1 when none
+
+        // Streams the tiles of positions [p0, p1) of segment (b, kvh); returns false on abort.
+        auto emit_piece = [&](int b, int kvh, int p0, int p1, int slot, bool unit_end) -> bool {
+            const int t_first = kPaged ? (p0 & ~(kBoxRows - 1)) : p0;
+            const int chunk0 = kvh * kChunksPerRow;
             const int32_t* bt_row =
-                kPaged ? p.block_table + static_cast<size_t>(pt.b) * p.max_pages : nullptr;
-            for (int t = t_first; t < pt.p1; t += TP) {
+                kPaged ? p.block_table + static_cast<size_t>(b) * p.max_pages : nullptr;
+            for (int t = t_first; t < p1; t += TP) {
+                if (dynamic && unit_end && t + TP >= p1)
+                    claimed = static_cast<int>(atomicAdd(p.ws_claim, 1u));
                 const int s = t_idx % STAGES;
                 const uint32_t ph = (t_idx / STAGES) & 1u;
                 if (!wait_bounded(ptx::smem_addr(&sm.empty[s]), ph ^ 1u, &sm.abort_flag,
-                                  p.ws_flags)) {
-                    ok = false;
-                    break;
-                }
+                                  p.ws_flags))
+                    return false;
+                TileDesc& d = sm.desc[s];
+                d.b = b;
+                d.kvh = kvh;
+                d.t = t;
+                d.vlo = (p0 > t ? p0 : t) - t;
+                d.vhi = (p1 < t + TP ? p1 : t + TP) - t;
+                d.slot = slot;
+                d.flags = (t == t_first ? kDescFirst : 0) | (t + TP >= p1 ? kDescLast : 0);
                 int nbox = 0;
 #pragma unroll
-                for (int j = 0; j < kBoxesPerTile; ++j) nbox += (t + j * kBoxRows < pt.p1) ? 1 : 0;
+                for (int j = 0; j < kBoxesPerTile; ++j) nbox += (t + j * kBoxRows < p1) ? 1 : 0;
                 const uint32_t full_bar = ptx::smem_addr(&sm.full[s]);
                 ptx::mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(nbox) * 2u * kBoxBytes);
                 const uint32_t k_dst = kv_base + s * kStageBytes;
@@ -303,16 +441,53 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
                                          policy);
                     } else {
                         const int row = t + j * kBoxRows;
-                        ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, row, chunk0,
-                                         pt.b, policy);
-                        ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, row, chunk0,
-                                         pt.b, policy);
+                        ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, row, chunk0, b,
+                                         policy);
+                        ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, row, chunk0, b,
+                                         policy);
                     }
                 }
                 ++t_idx;
             }
+            return true;
+        };
+
+        // ---- the static unit of this CTA: pieces of consecutive static heads ----
+        long long pos = static_unit_begin(pl, cta);
+        const long long stop = static_unit_begin(pl, cta + 1);
+        while (ok && pos < stop) {
+            const int b = upper_seq(pl.spref, B, pos);
+            const int sn = pl.sn[b];
+            const long long rel = pos - pl.spref[b];
+            const int kvh = static_cast<int>(rel / sn);
+            const int off = static_cast<int>(rel - static_cast<long long>(kvh) * sn);
+            const int take = static_cast<int>(stop - pos < sn - off ? stop - pos : sn - off);
+            pos += take;
+            const int p0 = pl.lo[b] + off;
+            ok = emit_piece(b, kvh, p0, p0 + take, cta + b * KVH + kvh, pos >= stop);
         }
-        if (!ok) {
+        // ---- dynamic chunks ----
+        while (ok && dynamic) {
+            if (claimed < 0) claimed = static_cast<int>(atomicAdd(p.ws_claim, 1u));
+            const int k = claimed;
+            claimed = -1;
+            if (k >= pl.n_dyn) break;
+            const int b = upper_seq(pl.dpref, B, k);
+            const int rel = k - pl.dpref[b];
+            const int kvh = rel / pl.dn[b];
+            const int c = rel - kvh * pl.dn[b];
+            const int p0 = pl.lo[b] + pl.sn[b] + c * pl.c_dyn;
+            ok = emit_piece(b, kvh, p0, p0 + pl.c_dyn, p.dyn_slot_base + k, true);
+        }
+        if (ok) {
+            // end-of-work descriptor (a plain arrival, no bytes)
+            const int s = t_idx % STAGES;
+            const uint32_t ph = (t_idx / STAGES) & 1u;
+            if (wait_bounded(ptx::smem_addr(&sm.empty[s]), ph ^ 1u, &sm.abort_flag, p.ws_flags)) {
+                sm.desc[s].flags = kDescDone;
+                ptx::mbar_arrive(ptx::smem_addr(&sm.full[s]));
+            }
+        } else {
             // let every copy already issued land before the CTA exits
             const uint32_t first = t_idx > static_cast<uint32_t>(STAGES) ? t_idx - STAGES : 0u;
             for (uint32_t tt = first; tt < t_idx; ++tt)
@@ -321,100 +496,66 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
         return;
     }
 
-    // ===================== consumers =====================
+    // ===================== consumers: follow the descriptors =====================
     typename Pol::State st;
-    PartialIter it(c_begin, c_end);
-    Partial pt;
     uint32_t t_idx = 0;
-    bool aborted = false;
-    while (it.next(sm.plan, B, KVH, pt)) {
-        const int t_first = kPaged ? (pt.p0 & ~(kBoxRows - 1)) : pt.p0;
-        const __nv_bfloat16* q_heads = p.q + (static_cast<size_t>(pt.b) * H + pt.kvh * G) * D;
-        Pol::begin(st, q_heads, warp, lane);
-        bool bad = false;
-        const int32_t* bt_row =
-            kPaged ? p.block_table + static_cast<size_t>(pt.b) * p.max_pages : nullptr;
-        for (int t = t_first; t < pt.p1; t += TP) {
-            const int s = t_idx % STAGES;
-            const uint32_t ph = (t_idx / STAGES) & 1u;
-            if (!aborted &&
-                !wait_bounded(ptx::smem_addr(&sm.full[s]), ph, &sm.abort_flag, p.ws_flags))
-                aborted = true;
-            const int vlo = (pt.p0 > t ? pt.p0 : t) - t;
-            const int vhi = (pt.p1 < t + TP ? pt.p1 : t + TP) - t;
-            if (kPaged) {
-                for (int j = vlo >> 4; j <= (vhi - 1) >> 4; ++j) {
-                    const int page = bt_row[(t >> 4) + j];
-                    bad |= (page < 0 || page >= p.num_pages);
-                }
-            }
-            const uint32_t k_tile = kv_base + s * kStageBytes;
-            const uint32_t v_tile = k_tile + KernelSmem<Pol>::kTileBytes;
-            Pol::tile(st, k_tile, v_tile, vlo, vhi, sm.scratch, t_idx, warp, lane);
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.empty[s]));
-            ++t_idx;
+    bool bad = false;
+    const float nan = __uint_as_float(0x7fc00000u);
+    while (true) {
+        const int s = t_idx % STAGES;
+        const uint32_t ph = (t_idx / STAGES) & 1u;
+        const bool ok = wait_bounded(ptx::smem_addr(&sm.full[s]), ph, &sm.abort_flag, p.ws_flags);
+        // all consumer warps take the same exit decision
+        if (ptx::named_barrier_or(2, kConsumerThreads, !ok)) break;
+        const TileDesc d = sm.desc[s];
+        if (d.flags & kDescDone) break;
+        if (d.flags & kDescFirst) {
+            Pol::begin(st, p.q + (static_cast<size_t>(d.b) * H + d.kvh * G) * D, warp, lane);
+            bad = false;
         }
+        if (kPaged) {
+            const int32_t* bt_row = p.block_table + static_cast<size_t>(d.b) * p.max_pages;
+            for (int j = d.vlo >> 4; j <= (d.vhi - 1) >> 4; ++j) {
+                const int page = bt_row[(d.t >> 4) + j];
+                bad |= (page < 0 || page >= p.num_pages);
+            }
+        }
+        const uint32_t k_tile = kv_base + s * kStageBytes;
+        const uint32_t v_tile = k_tile + KernelSmem<Pol>::kTileBytes;
+        Pol::tile(st, k_tile, v_tile, d.vlo, d.vhi, sm.scratch, t_idx, warp, lane);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.empty[s]));
+        ++t_idx;
+        if (!(d.flags & kDescLast)) continue;
+
+        // ---------------- epilogue of a partial ----------------
         // merged (m, l, acc) of this piece -> sm.m, sm.l, sm.acc (ends with a consumer barrier)
         Pol::end(st, &sm.acc[0][0], sm.m, sm.l, sm.scratch, warp, lane);
-
-        // ---------------- epilogue ----------------
         if (bad && tid == 0) atomicOr(p.ws_flags, kFlagBadPage);
-        const int u = pt.b * KVH + pt.kvh;
-        const long long seg_end = pt.seg_start + pt.seg_len;
-        const int first = cta_of(pt.seg_start, N, num_ctas);
-        const int last = cta_of(seg_end - 1, N, num_ctas);
-        const size_t out_base = (static_cast<size_t>(pt.b) * H + pt.kvh * G) * D;
-        const float nan = __uint_as_float(0x7fc00000u);
-        if (first == last) {
-            if (!aborted) {
-                for (int i = tid; i < G * D; i += kConsumerThreads) {
-                    const int h = i / D;
-                    store_out(p, out_base + i, bad ? nan : (&sm.acc[0][0])[i] / sm.l[h]);
-                }
+        const SegmentParts sp(pl, d.b, d.kvh, p.dyn_slot_base);
+        const int nparts = sp.count();
+        const size_t out_base = (static_cast<size_t>(d.b) * H + d.kvh * G) * D;
+        const float4* acc4 = reinterpret_cast<const float4*>(&sm.acc[0][0]);
+        const float4 nan4 = make_float4(nan, nan, nan, nan);
+        if (nparts == 1) {
+            for (int i4 = tid; i4 < G * D / 4; i4 += kConsumerThreads) {
+                const float inv = 1.0f / sm.l[(i4 * 4) / D];
+                const float4 a = acc4[i4];
+                store_out4(p, out_base + static_cast<size_t>(i4) * 4,
+                           bad ? nan4 : make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
             }
         } else {
-            const size_t slot = static_cast<size_t>(cta) + u;
-            if (!aborted) {
-                float* wacc = p.ws_acc + slot * G * D;
-                for (int i = tid; i < G * D; i += kConsumerThreads)
-                    wacc[i] = bad ? nan : (&sm.acc[0][0])[i];
-                if (tid < G) {
-                    p.ws_ml[(slot * G + tid) * 2 + 0] = bad ? 0.0f : sm.m[tid];
-                    p.ws_ml[(slot * G + tid) * 2 + 1] = bad ? nan : sm.l[tid];
-                }
-                __threadfence();
-            }
-            ptx::named_barrier_sync(1, kConsumerThreads);
-            if (tid == 0) {
-                int is_last = 0;
-                if (!aborted && !sm.abort_flag) {
-                    const unsigned nparts = static_cast<unsigned>(last - first + 1);
-                    is_last = atomicInc(p.ws_counters + u, nparts - 1u) == nparts - 1u;
-                }
-                sm.last_flag = is_last;
-            }
-            ptx::named_barrier_sync(1, kConsumerThreads);
-            if (sm.last_flag) {
-                __threadfence();
-                // log-sum-exp merge of the partials of segment u, in CTA order
-                for (int i = tid; i < G * D; i += kConsumerThreads) {
-                    const int h = i / D;
-                    float M = -INFINITY;
-                    for (int j = first; j <= last; ++j)
-                        M = fmaxf(M, __ldcg(p.ws_ml + ((static_cast<size_t>(j) + u) * G + h) * 2));
-                    float num = 0.0f, den = 0.0f;
-                    for (int j = first; j <= last; ++j) {
-                        const size_t sl = static_cast<size_t>(j) + u;
-                        const float w = exp2f(__ldcg(p.ws_ml + (sl * G + h) * 2) - M);
-                        num += w * __ldcg(p.ws_acc + sl * G * D + i);
-                        den += w * __ldcg(p.ws_ml + (sl * G + h) * 2 + 1);
-                    }
-                    store_out(p, out_base + i, num / den);
-                }
+            // the combine kernel merges the partials after this grid completes
+            const size_t slot = static_cast<size_t>(d.slot);
+            float4* wacc4 = reinterpret_cast<float4*>(p.ws_acc + slot * G * D);
+            for (int i4 = tid; i4 < G * D / 4; i4 += kConsumerThreads)
+                wacc4[i4] = bad ? nan4 : acc4[i4];
+            if (tid < G) {
+                p.ws_ml[(slot * G + tid) * 2 + 0] = bad ? 0.0f : sm.m[tid];
+                p.ws_ml[(slot * G + tid) * 2 + 1] = bad ? nan : sm.l[tid];
             }
         }
-        // sm.acc / sm.last_flag are reused by the next piece
+        // sm.acc is reused by the next piece
         ptx::named_barrier_sync(1, kConsumerThreads);
     }
 }

@@ -10,6 +10,7 @@ namespace gqa {
 
 // Grid size bound used to size workspaces independently of the device.
 constexpr int kMaxCtas = 1024;
+static_assert(kMaxCtas >= 1, "grid bound");
 
 struct LaunchArgs {
     CUtensorMap tm_k;

@@ -3,10 +3,15 @@
 
 #include <mutex>
 
+#include "kernels/combine_kernel.cuh"
 #include "launch.h"
 
 namespace gqa {
 
+// Launches the main kernel and, right behind it, the combine kernel.  Both opt
+// in to programmatic dependent launch: each may start while the kernel before it
+// in the stream drains, and waits (griddepcontrol.wait) before touching global
+// memory that kernel writes.
 template <class Pol, bool kPaged>
 cudaError_t launch_decode(const LaunchArgs& a) {
     constexpr size_t kSmem = sizeof(KernelSmem<Pol>) + 1024;   // + alignment slack
@@ -24,14 +29,32 @@ cudaError_t launch_decode(const LaunchArgs& a) {
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
 
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.grid));
     cfg.blockDim = dim3((Pol::NC + 1) * 32);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = a.stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, gqa_decode_kernel<Pol, kPaged>, a.tm_k, a.tm_v, a.p);
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gqa_decode_kernel<Pol, kPaged>, a.tm_k, a.tm_v, a.p);
+    if (e != cudaSuccess) return e;
+
+    const int segments = a.p.B * a.p.KVH;
+    constexpr int kChunksPerSeg = (Pol::G * Pol::D / 4 + kCombineThreads - 1) / kCombineThreads;
+    const int items = segments * kChunksPerSeg;
+    const int cgrid = items < 4 * a.grid ? items : 4 * a.grid;
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3(static_cast<unsigned>(cgrid));
+    ccfg.blockDim = dim3(kCombineThreads);
+    ccfg.dynamicSmemBytes = 0;
+    ccfg.stream = a.stream;
+    ccfg.attrs = pdl;
+    ccfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&ccfg, gqa_combine_kernel<Pol::G, Pol::D>, a.p, segments);
 }
 
 }  // namespace gqa
