@@ -46,7 +46,7 @@ PROFILES = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [
     "decode_attention_gb300/csrc/kernels/decode_kernel.cuh",
     "decode_attention_gb300/csrc/kernels/policy_sliding_core.cuh",
-    "decode_attention_gb300/csrc/kernels/policy_global_mma.cuh",
+    "decode_attention_gb300/csrc/kernels/policy_mma.cuh",
     "decode_attention_gb300/csrc/kernels/ptx.cuh",
 ]
 

@@ -77,40 +77,27 @@ struct DeviceState {
 
 DeviceState g_dev[kMaxDevices];
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
+}  // namespace
 
-bool get_encode_fn() {
-    std::call_once(g_encode_once, [] {
+namespace gqa {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn_ptr = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            fn_ptr = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
-    return g_encode != nullptr;
+    return fn_ptr;
 }
 
-// 4-D view of a K or V cache for 16-row TMA boxes of one KV head, 128-byte
-// swizzled in shared memory as [D/64 chunks][16 rows][64 elements]:
-//   dim 0: 64 elements of the head dim (contiguous)
-//   dim 1: 16-row axis -- cache positions (contiguous) or page slots (paged)
-//   dim 2: 64-element chunk of the KVH*D row (stride 128 B)
-//   dim 3: sequence (contiguous) or page (paged)
-bool encode_kv_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t outer, int KVH,
-                   int D) {
-    const uint64_t row_bytes = static_cast<uint64_t>(KVH) * D * 2;
-    cuuint64_t dims[4] = {64, rows, static_cast<cuuint64_t>(KVH) * (D / 64), outer};
-    cuuint64_t strides[3] = {row_bytes, 128, row_bytes * rows};
-    cuuint32_t box[4] = {64, gqa::kBoxRows, static_cast<cuuint32_t>(D / 64), 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
+}  // namespace gqa
+
+namespace {
 
 struct CallShape {
     Geometry geo;
@@ -174,7 +161,7 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
                  uint64_t outer, int capacity, int num_pages, int max_pages, void* out,
                  gqa_out_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
                  cudaStream_t stream) {
-    if (!get_encode_fn()) return GQA_ERR_CUDA;
+    if (!gqa::tensor_map_encoder()) return GQA_ERR_CUDA;
     void* ws = nullptr;
     WorkspaceLayout lay;
     int grid = 0;
@@ -183,8 +170,10 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
 
     gqa::LaunchArgs a;
     std::memset(&a, 0, sizeof a);
-    if (!encode_kv_map(&a.tm_k, k, rows, outer, c.KVH, c.D)) return GQA_ERR_CUDA;
-    if (!encode_kv_map(&a.tm_v, v, rows, outer, c.KVH, c.D)) return GQA_ERR_CUDA;
+    a.k = k;
+    a.v = v;
+    a.rows = rows;
+    a.outer = outer;
     uint8_t* w = static_cast<uint8_t*>(ws);
     a.p.q = static_cast<const __nv_bfloat16*>(q);
     a.p.seq_lens = seq_lens;

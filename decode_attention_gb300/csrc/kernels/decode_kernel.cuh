@@ -32,8 +32,9 @@
 //
 // Data movement.  One producer thread walks the schedule and streams K and V
 // tiles of TP positions through a ring of shared-memory stages with TMA (4-D
-// boxes of 16 positions x D, 128-byte swizzled), completion counted on
-// mbarriers; with each stage it publishes a descriptor (segment, valid rows,
+// boxes of one KV head's rows: 16 positions = one page, or the policy's box
+// height on a contiguous cache; 128-byte swizzled where the policy reads the
+// tile with ldmatrix), completion counted on mbarriers; with each stage it publishes a descriptor (segment, valid rows,
 // first/last tile of a partial, workspace slot).  The consumer warps follow the
 // descriptors: policy arithmetic (CUDA cores or warp mma) per tile, epilogue
 // after the last tile of a partial.  Every wait is bounded (~2 s): a wait that
@@ -48,7 +49,7 @@
 
 namespace gqa {
 
-constexpr int kBoxRows = 16;          // positions per TMA box (= one 16-position page)
+constexpr int kPageRows = 16;         // positions per page = TMA box height on a paged cache
 constexpr int kChunkElems = 64;       // bf16 per 128-byte swizzle row
 constexpr int kChunkBytes = 2048;     // one chunk of a box: 16 rows x 128 B
 constexpr int kMaxBatch = 256;
@@ -316,6 +317,8 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
                       const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
     constexpr int G = Pol::G, D = Pol::D, TP = Pol::TP, STAGES = Pol::STAGES, NC = Pol::NC;
     constexpr int kConsumerThreads = NC * 32;
+    // TMA boxes: one page on a paged cache, Pol::kBoxRows positions on a contiguous one
+    constexpr int kBoxRows = kPaged ? kPageRows : Pol::kBoxRows;
     constexpr int kBoxBytes = kBoxRows * D * 2;
     constexpr int kBoxesPerTile = TP / kBoxRows;
     constexpr int kChunksPerRow = D / kChunkElems;
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
 
         // Streams the tiles of positions [p0, p1) of segment (b, kvh); returns false on abort.
         auto emit_piece = [&](int b, int kvh, int p0, int p1, int slot, bool unit_end) -> bool {
-            const int t_first = kPaged ? (p0 & ~(kBoxRows - 1)) : p0;
+            const int t_first = kPaged ? (p0 & ~(kPageRows - 1)) : p0;
             const int chunk0 = kvh * kChunksPerRow;
             const int32_t* bt_row =
                 kPaged ? p.block_table + static_cast<size_t>(b) * p.max_pages : nullptr;
@@ -435,16 +438,18 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
                     if (kPaged) {
                         int page = bt_row[(t >> 4) + j];
                         if (page < 0 || page >= p.num_pages) page = 0;   // flagged by the consumers
-                        ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, 0, chunk0, page,
-                                         policy);
-                        ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, 0, chunk0, page,
-                                         policy);
+                        // swizzled map: (elem, slot, chunk, page); plain map: (elem, kvh, slot, page)
+                        const int c1 = Pol::kSwizzle128 ? 0 : kvh;
+                        const int c2 = Pol::kSwizzle128 ? chunk0 : 0;
+                        ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, c1, c2, page, policy);
+                        ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, c1, c2, page, policy);
                     } else {
                         const int row = t + j * kBoxRows;
-                        ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, row, chunk0, b,
-                                         policy);
-                        ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, row, chunk0, b,
-                                         policy);
+                        // swizzled map: (elem, position, chunk, seq); plain map: (elem, kvh, position, seq)
+                        const int c1 = Pol::kSwizzle128 ? row : kvh;
+                        const int c2 = Pol::kSwizzle128 ? chunk0 : row;
+                        ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, c1, c2, b, policy);
+                        ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, c1, c2, b, policy);
                     }
                 }
                 ++t_idx;

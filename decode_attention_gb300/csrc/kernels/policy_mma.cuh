@@ -1,11 +1,14 @@
-// Tensor-core arithmetic for decodeGQA (g = 8 query heads per KV head, D = 512),
-// gemma-4-31B Model Spec, "Compute-graph nodes", attn.core row with Op Spec
-// decodeGQA.
+// Tensor-core arithmetic for the decode attention core: the two contractions
+// (scores Q K^T and the weighted sum P V) run as warp-level bf16 mma
+// (m16n8k16, fp32 accumulate) on tiles staged in shared memory.
 //
-// With 8 heads sharing each K/V row the work is 4 FMA per byte of K/V: at HBM
-// rate that would occupy most of the CUDA cores, so the two contractions run as
-// warp-level bf16 mma (m16n8k16, fp32 accumulate).  The 8 heads fill rows 0-7 of
-// the 16-row A operand.
+// Instantiated for decodeGQA (g = 8 query heads per KV head, D = 512) and for
+// slidingDecodeGQA (g = 2, D = 256), the two attn.core rows of the gemma-4-31B
+// Model Spec ("Compute-graph nodes").  The g heads of a KV head fill rows
+// 0..g-1 of the 16-row A operand; the remaining rows are zero.  Even with most
+// rows idle the tensor pipe does the arithmetic in a few instructions per
+// position, where the CUDA cores would spend ~25 per position per head pair on
+// unpacking and FMAs.
 //
 // Per tile of 32 positions and consumer warp w (of 8):
 //   scores  S[h, pos] = Q[h, :] . K[pos, :] for positions [8(w%4), 8(w%4)+8) and
@@ -14,7 +17,7 @@
 //           units;
 //   softmax every warp reads all 32 scores of its heads, so all warps hold the
 //           same running max/normaliser;
-//   P.V     O[h, d] += P[h, pos] V[pos, d] for the warp's 64-wide slice of d
+//   P.V     O[h, d] += P[h, pos] V[pos, d] for the warp's D/8-wide slice of d
 //           (B = V rows via ldmatrix.trans).  P is split into bf16 hi + lo parts
 //           placed in rows 0-7 and 8-15 of the A operand, so one mma applies
 //           P to ~16 significant bits at no extra cost; O = rows 0-7 + rows 8-15.
@@ -26,12 +29,17 @@
 
 namespace gqa {
 
-struct GlobalMma {
-    static constexpr int G = 8, D = 512, TP = 32, STAGES = 3, NC = 8;
-    static constexpr int kDSlice = D / NC;          // 64 output dims per warp
-    static constexpr int kNTiles = kDSlice / 8;     // 8 n-tiles of 8 dims
-    static constexpr int kKSteps = D / 16 / 2;      // 16 k-steps: half of the head dim
+template <int kG, int kD, int kStages>
+struct MmaPolicy {
+    static constexpr int G = kG, D = kD, TP = 32, STAGES = kStages, NC = 8;
+    static_assert(G >= 1 && G <= 8, "heads fill rows 0..G-1 of the A operand");
+    static constexpr int kDSlice = D / NC;          // output dims per warp
+    static constexpr int kNTiles = kDSlice / 8;     // n-tiles of 8 dims per warp
+    static_assert(kNTiles % 2 == 0, "n-tiles are loaded in pairs");
+    static constexpr int kKSteps = D / 16 / 2;      // k-steps over half of the head dim
     static constexpr int kSStride = 40;             // padded row of the score tile
+    static constexpr bool kSwizzle128 = true;       // ldmatrix needs the 128-byte swizzle
+    static constexpr int kBoxRows = 16;             // TMA box height on a contiguous cache
 
     struct Scratch {
         alignas(16) float S[2][2][G][kSStride];   // [tile parity][half of D][head][position]
@@ -47,12 +55,13 @@ struct GlobalMma {
     __device__ static __forceinline__ void begin(State& st, const __nv_bfloat16* q_heads, int warp,
                                                  int lane) {
         const int gid = lane >> 2, t4 = lane & 3;
+        const bool real = gid < G;   // rows G..7 of A are zero
         const uint32_t* qrow =
-            reinterpret_cast<const uint32_t*>(q_heads + gid * D + (warp >> 2) * (D / 2));
+            reinterpret_cast<const uint32_t*>(q_heads + (real ? gid : 0) * D + (warp >> 2) * (D / 2));
 #pragma unroll
         for (int kk = 0; kk < kKSteps; ++kk) {
-            st.qa[kk][0] = __ldg(qrow + (kk * 16 + 2 * t4) / 2);
-            st.qa[kk][1] = __ldg(qrow + (kk * 16 + 8 + 2 * t4) / 2);
+            st.qa[kk][0] = real ? __ldg(qrow + (kk * 16 + 2 * t4) / 2) : 0u;
+            st.qa[kk][1] = real ? __ldg(qrow + (kk * 16 + 8 + 2 * t4) / 2) : 0u;
         }
 #pragma unroll
         for (int n = 0; n < kNTiles; ++n)
@@ -66,8 +75,7 @@ struct GlobalMma {
     __device__ static __forceinline__ uint32_t unit_addr(uint32_t tile, int row, int grp) {
         const int box = row >> 4, r = row & 15;
         const int chunk = grp >> 3, unit = grp & 7;
-        return tile + box * (kBoxRows * D * 2) + chunk * kChunkBytes + r * 128 +
-               ((unit ^ (r & 7)) << 4);
+        return tile + box * (16 * D * 2) + chunk * kChunkBytes + r * 128 + ((unit ^ (r & 7)) << 4);
     }
 
     __device__ static __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -105,22 +113,24 @@ struct GlobalMma {
             float s1 = (c[0][1] + c[1][1]) * kLog2e;
             if (pos < vlo || pos >= vhi) s0 = -INFINITY;
             if (pos + 1 < vlo || pos + 1 >= vhi) s1 = -INFINITY;
-            *reinterpret_cast<float2*>(&S[warp >> 2][gid][pos]) = make_float2(s0, s1);
+            if (gid < G) *reinterpret_cast<float2*>(&S[warp >> 2][gid][pos]) = make_float2(s0, s1);
         }
         ptx::named_barrier_sync(1, NC * 32);
 
-        // ---- online softmax over the 32 positions of head gid ----
+        // ---- online softmax over the 32 positions of head gid (rows >= G stay empty) ----
         float sv[2][4];
+        const int hrow = gid < G ? gid : 0;
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
-            const float2 x0 = *reinterpret_cast<const float2*>(&S[0][gid][16 * ks + 2 * t4]);
-            const float2 x1 = *reinterpret_cast<const float2*>(&S[1][gid][16 * ks + 2 * t4]);
-            const float2 y0 = *reinterpret_cast<const float2*>(&S[0][gid][16 * ks + 8 + 2 * t4]);
-            const float2 y1 = *reinterpret_cast<const float2*>(&S[1][gid][16 * ks + 8 + 2 * t4]);
-            sv[ks][0] = x0.x + x1.x;
-            sv[ks][1] = x0.y + x1.y;
-            sv[ks][2] = y0.x + y1.x;
-            sv[ks][3] = y0.y + y1.y;
+            const float2 x0 = *reinterpret_cast<const float2*>(&S[0][hrow][16 * ks + 2 * t4]);
+            const float2 x1 = *reinterpret_cast<const float2*>(&S[1][hrow][16 * ks + 2 * t4]);
+            const float2 y0 = *reinterpret_cast<const float2*>(&S[0][hrow][16 * ks + 8 + 2 * t4]);
+            const float2 y1 = *reinterpret_cast<const float2*>(&S[1][hrow][16 * ks + 8 + 2 * t4]);
+            const bool real = gid < G;
+            sv[ks][0] = real ? x0.x + x1.x : -INFINITY;
+            sv[ks][1] = real ? x0.y + x1.y : -INFINITY;
+            sv[ks][2] = real ? y0.x + y1.x : -INFINITY;
+            sv[ks][3] = real ? y0.y + y1.y : -INFINITY;
         }
         float tmax = -INFINITY;
 #pragma unroll
@@ -194,18 +204,23 @@ struct GlobalMma {
         float l = st.l;
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
+        if (gid < G) {
 #pragma unroll
-        for (int n = 0; n < kNTiles; ++n) {
-            const int d = warp * kDSlice + n * 8 + 2 * t4;
-            *reinterpret_cast<float2*>(&acc_out[gid * D + d]) =
-                make_float2(st.acc[n][0] + st.acc[n][2], st.acc[n][1] + st.acc[n][3]);
+            for (int n = 0; n < kNTiles; ++n) {
+                const int d = warp * kDSlice + n * 8 + 2 * t4;
+                *reinterpret_cast<float2*>(&acc_out[gid * D + d]) =
+                    make_float2(st.acc[n][0] + st.acc[n][2], st.acc[n][1] + st.acc[n][3]);
+            }
         }
-        if (warp == 0 && t4 == 0) {
+        if (warp == 0 && t4 == 0 && gid < G) {
             m_out[gid] = st.m;
             l_out[gid] = l;
         }
         ptx::named_barrier_sync(1, NC * 32);
     }
 };
+
+using GlobalMma = MmaPolicy<8, 512, 3>;    // decodeGQA
+using SlidingMma = MmaPolicy<2, 256, 6>;   // slidingDecodeGQA
 
 }  // namespace gqa

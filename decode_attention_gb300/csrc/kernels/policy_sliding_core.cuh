@@ -5,14 +5,19 @@
 // At 2 heads per KV row the work is 1 FMA per byte of K/V (scores + P.V), far
 // below what the CUDA cores sustain at HBM rate, so no tensor core is used.
 //
-// Layout per consumer warp w (of 8) and tile of 32 positions: the warp owns the
-// 4 positions [4w, 4w+4); lane l owns head-dim elements [8l, 8l+8) of every
-// row, so each row is one conflict-free 512-byte read by the warp.  The 8 dot
-// products of a tile (4 positions x 2 heads) are reduced across lanes with a
-// reduce-scatter butterfly (9 shuffles), after which lane l holds the score of
-// position l/8, head (l/4)%2.  Each warp keeps its own online-softmax state
-// (m, l, acc); the 8 states are merged through shared memory when a piece ends.
-// Two warps per scheduler hide the shared-memory and shuffle latencies.
+// Shared-memory tiles are plain row-major [position][256] bf16 (no swizzle):
+// lane l reads bytes [16l, 16l+16) of a row, so a row is one conflict-free
+// 512-byte read, and the TMA moves whole 512-byte rows (one 32-position box per
+// tensor and tile on a contiguous cache).
+//
+// Layout per consumer warp w (of 8) and tile of 64 positions: the warp owns the
+// 8 positions [8w, 8w+8); lane l owns head-dim elements [8l, 8l+8) of every
+// row.  The 16 dot products of a tile (8 positions x 2 heads) are reduced
+// across lanes with a reduce-scatter butterfly (15 shuffles), after which lane
+// l holds the score of position l/4, head (l/2)%2.  Each warp keeps its own
+// online-softmax state (m, l, acc); the 8 states are merged through shared
+// memory when a piece ends.  Two warps per scheduler, and 8 positions per warp
+// per tile, keep the shuffle and shared-memory latency chains overlapped.
 // Scores are kept in log2 units (q is pre-multiplied by log2(e)), so every
 // exponential is exp2.
 #pragma once
@@ -22,9 +27,11 @@
 namespace gqa {
 
 struct SlidingCore {
-    static constexpr int G = 2, D = 256, TP = 32, STAGES = 6, NC = 8;
-    static constexpr int kPosPerWarp = TP / NC;   // 4
-    static_assert(kPosPerWarp == 4, "reduce-scatter below assumes 4 positions x 2 heads");
+    static constexpr int G = 2, D = 256, TP = 64, STAGES = 3, NC = 8;
+    static constexpr int kPosPerWarp = TP / NC;   // 8
+    static constexpr bool kSwizzle128 = false;    // plain [position][D] tiles
+    static constexpr int kBoxRows = 64;           // TMA box height on a contiguous cache
+    static_assert(kPosPerWarp == 8, "reduce-scatter below assumes 8 positions x 2 heads");
 
     struct Scratch {
         alignas(16) float wacc[NC][G][D];   // float4 stores
@@ -58,12 +65,9 @@ struct SlidingCore {
         }
     }
 
-    // Address of this lane's 16 bytes of row `row` (0..31) of a tile.
+    // Address of this lane's 16 bytes of row `row` of a tile.
     __device__ static __forceinline__ uint32_t row_addr(uint32_t tile, int row, int lane) {
-        const int box = row >> 4, r = row & 15;
-        const int chunk = lane >> 3, unit = lane & 7;
-        return tile + box * (kBoxRows * D * 2) + chunk * kChunkBytes + r * 128 +
-               ((unit ^ (r & 7)) << 4);
+        return tile + row * (D * 2) + lane * 16;
     }
 
     __device__ static __forceinline__ void tile(State& st, uint32_t k_tile, uint32_t v_tile, int vlo,
@@ -73,8 +77,8 @@ struct SlidingCore {
         (void)t_idx;
         const int row0 = warp * kPosPerWarp;
 
-        // ---- scores: 4 positions x 2 heads, partial sums over this lane's 8 dims ----
-        float v[8];
+        // ---- scores: 8 positions x 2 heads, partial sums over this lane's 8 dims ----
+        float v[16];
 #pragma unroll
         for (int j = 0; j < kPosPerWarp; ++j) {
             const uint4 raw = ptx::lds128(row_addr(k_tile, row0 + j, lane));
@@ -91,39 +95,46 @@ struct SlidingCore {
             v[2 * j] = s0;
             v[2 * j + 1] = s1;
         }
-        // ---- reduce-scatter: lane l ends with the full score of index (l >> 2) & 7 ----
+        // ---- reduce-scatter: lane l ends with the full score of index l >> 1 ----
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 8; ++i) {
             const bool up = lane & 16;
-            const float send = up ? v[i] : v[i + 4];
-            const float keep = up ? v[i + 4] : v[i];
+            const float send = up ? v[i] : v[i + 8];
+            const float keep = up ? v[i + 8] : v[i];
             v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
         }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             const bool up = lane & 8;
-            const float send = up ? v[i] : v[i + 2];
-            const float keep = up ? v[i + 2] : v[i];
+            const float send = up ? v[i] : v[i + 4];
+            const float keep = up ? v[i + 4] : v[i];
             v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
         }
-        {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
             const bool up = lane & 4;
+            const float send = up ? v[i] : v[i + 2];
+            const float keep = up ? v[i + 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        {
+            const bool up = lane & 2;
             const float send = up ? v[0] : v[1];
             const float keep = up ? v[1] : v[0];
-            v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+            v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
         }
-        float s = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 2);
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        // lane holds position row0 + (lane >> 3), head (lane >> 2) & 1
-        const int my_pos = row0 + (lane >> 3);
-        const int my_head = (lane >> 2) & 1;
+        float s = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+        // lane holds position row0 + (lane >> 2), head (lane >> 1) & 1
+        const int my_pos = row0 + (lane >> 2);
+        const int my_head = (lane >> 1) & 1;
         if (my_pos < vlo || my_pos >= vhi) s = -INFINITY;
 
-        // ---- online softmax (per head; lanes with equal bit 2 share a head) ----
+        // ---- online softmax (per head; lanes with equal bit 1 share a head) ----
         float tmax = s;
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-        const float tmax_other = __shfl_xor_sync(0xffffffffu, tmax, 4);
+        const float tmax_other = __shfl_xor_sync(0xffffffffu, tmax, 2);
         const float tm0 = my_head == 0 ? tmax : tmax_other;
         const float tm1 = my_head == 0 ? tmax_other : tmax;
         const float mn0 = fmaxf(st.m[0], tm0), mn1 = fmaxf(st.m[1], tm1);
@@ -132,9 +143,10 @@ struct SlidingCore {
         const float m_mine = my_head == 0 ? mn0 : mn1;
         const float pr = (s == -INFINITY) ? 0.0f : exp2f(s - m_mine);
         float psum = pr;
+        psum += __shfl_xor_sync(0xffffffffu, psum, 4);
         psum += __shfl_xor_sync(0xffffffffu, psum, 8);
         psum += __shfl_xor_sync(0xffffffffu, psum, 16);
-        const float psum_other = __shfl_xor_sync(0xffffffffu, psum, 4);
+        const float psum_other = __shfl_xor_sync(0xffffffffu, psum, 2);
         const float ps0 = my_head == 0 ? psum : psum_other;
         const float ps1 = my_head == 0 ? psum_other : psum;
         st.l[0] = st.l[0] * a0 + ps0;
@@ -150,8 +162,8 @@ struct SlidingCore {
         }
 #pragma unroll
         for (int j = 0; j < kPosPerWarp; ++j) {
-            const float p0 = __shfl_sync(0xffffffffu, pr, j * 8 + 0);
-            const float p1 = __shfl_sync(0xffffffffu, pr, j * 8 + 4);
+            const float p0 = __shfl_sync(0xffffffffu, pr, j * 4 + 0);
+            const float p1 = __shfl_sync(0xffffffffu, pr, j * 4 + 2);
             uint4 raw = ptx::lds128(row_addr(v_tile, row0 + j, lane));
             const bool valid = (row0 + j >= vlo) && (row0 + j < vhi);
             if (!valid) raw = make_uint4(0u, 0u, 0u, 0u);

@@ -1,5 +1,5 @@
 // decodeGQA kernels (H=32, KVH=4, D=512), contiguous and paged caches.
-#include "kernels/policy_global_mma.cuh"
+#include "kernels/policy_mma.cuh"
 #include "launch_common.cuh"
 
 namespace gqa {

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "kernels/decode_kernel.cuh"
@@ -13,12 +14,17 @@ constexpr int kMaxCtas = 1024;
 static_assert(kMaxCtas >= 1, "grid bound");
 
 struct LaunchArgs {
-    CUtensorMap tm_k;
-    CUtensorMap tm_v;
+    const void* k;          // K cache / page pool
+    const void* v;          // V cache / page pool
+    uint64_t rows;          // positions per sequence (contiguous) or slots per page (paged)
+    uint64_t outer;         // sequences (contiguous) or pages (paged)
     DecodeParams p;
     int grid;
     cudaStream_t stream;
 };
+
+// cuTensorMapEncodeTiled from the driver (resolved once); null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Kernel launchers, one translation unit per geometry.  Each sets its kernels'
 // shared-memory limit on first use on a device and launches one persistent grid.
