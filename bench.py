@@ -493,7 +493,8 @@ def run_ours(args, wl):
         items = oracle_sample(calls, budget_s=args.cpu_budget)
         nb, dt = run_oracle_items(items)
         reps = 1
-        while dt < 0.5 * args.cpu_budget and reps < 64:
+        # repeat the sample until about cpu_budget seconds of oracle work are timed
+        while dt < args.cpu_budget and reps < 100000:
             nb2, dt2 = run_oracle_items(items)
             nb, dt, reps = nb + nb2, dt + dt2, reps + 1
         import oracle

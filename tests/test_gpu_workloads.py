@@ -1,0 +1,56 @@
+"""Full-size parity: the five benchmark workloads at their stated sizes, built and
+launched exactly as bench.py builds and launches them, with sampled sequences
+checked against the fp64 oracle (the oracle computes each sampled sequence from
+its attended K/V rows copied to the host)."""
+import numpy as np
+import pytest
+import torch
+
+import bench
+from decode_attention_gb300 import inputs
+from tests.helpers import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import decode_attention_gb300 as gqa  # noqa: E402
+import oracle  # noqa: E402
+
+WORKLOADS = ["sliding_b1_s2048", "global_b8_s8192", "sliding_b64_s32768",
+             "global_b16_s131072", "paged_mixed_b256"]
+
+
+def sampled(lens, k=3, seed=0):
+    """First, last and a few random sequences with a non-empty range."""
+    idx = [i for i, L in enumerate(lens) if L > 0]
+    rng = np.random.default_rng(seed)
+    pick = {idx[0], idx[-1]} | set(rng.choice(idx, size=min(k, len(idx)), replace=False).tolist())
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_workload_sampled_parity(name):
+    wl = inputs.WORKLOADS[name]
+    calls, lens = bench.build_calls(wl, wl.seed)
+    for c in calls:
+        c.out = torch.empty_like(c.out, dtype=torch.float32)
+        c.launch(gqa)
+        out32 = c.out.clone()
+        c.out = torch.empty_like(out32, dtype=torch.bfloat16)
+        c.launch(gqa)
+        out16 = c.out.clone()
+        torch.cuda.synchronize()
+        assert gqa.gqa_device_status() == 0
+        assert torch.equal(out16, out32.to(torch.bfloat16))
+        for b in sampled(lens, seed=wl.seed):
+            qb, kb, vb, L, base = bench.host_slices(c, b)
+            ref = oracle.gqa_decode_f64(qb, kb, vb, [L], c.geo["window"], pos_base=base)[0]
+            assert_parity(out32[b], ref, f"{name}/{c.layer} b={b} L={L}")
+        # sequences with nothing to attend are exact zeros
+        for b, L in enumerate(lens):
+            if L == 0:
+                assert torch.all(out32[b] == 0)
+    del calls
+    torch.cuda.empty_cache()
