@@ -226,10 +226,9 @@ __device__ __forceinline__ void store_out4(const DecodeParams& p, size_t idx, fl
 // Plan computation (warp 0).  Lengths are clamped to [0, capacity]; the dynamic
 // share of each segment is floor(n_b * f / c_dyn) chunks with
 // f = min(1/5, kDynChunksPerCta * grid * c_dyn / N), so all segments together
-// hold about kDynChunksPerCta chunks per CTA (capped at kMaxDynUnits).  f is
-// evaluated in fp32: every CTA runs the same instructions on the same lengths,
-// so all of them derive the same split (its exact value only sets how much
-// work is dynamic).
+// hold at most kDynChunksPerCta chunks per CTA and at most kMaxDynUnits (exact
+// 32-bit integer arithmetic: n_b * target < 2^31 and N < 2^32, so the total can
+// never exceed the bound the workspace is sized for).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, int grid,
                                            int lane) {
@@ -252,10 +251,11 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
     const long long target = static_cast<long long>(kDynChunksPerCta) * grid < kMaxDynUnits
                                  ? static_cast<long long>(kDynChunksPerCta) * grid
                                  : kMaxDynUnits;
-    // chunks per attended position of a segment: f / c_dyn
-    const float chunk_rate = target * c * 5 < N
-                                 ? static_cast<float>(target) / static_cast<float>(N)
-                                 : 0.2f / static_cast<float>(c);
+    // d_b = floor(n_b * target / N) when that is below n_b / (5 c), else floor(n_b / (5 c))
+    const bool by_target = target * c * 5 < N;
+    const uint32_t tgt32 = static_cast<uint32_t>(target);
+    const uint32_t n32 = static_cast<uint32_t>(N);
+    const uint32_t five_c = static_cast<uint32_t>(5 * c);
     long long sloc[kPer], srun = 0;
     int dloc[kPer], drun = 0;
 #pragma unroll
@@ -263,8 +263,10 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
         const int b = lane * kPer + j;
         int d = 0, sn = 0;
         if (b < B) {
-            d = use_dyn ? static_cast<int>(static_cast<float>(pl.n[b]) * chunk_rate) : 0;
-            if (d * c > pl.n[b]) d = pl.n[b] / static_cast<int>(c);
+            const uint32_t nb = static_cast<uint32_t>(pl.n[b]);
+            d = !use_dyn ? 0
+                : by_target ? static_cast<int>((nb * tgt32) / n32)
+                            : static_cast<int>(nb / five_c);
             sn = pl.n[b] - d * static_cast<int>(c);
             pl.sn[b] = sn;
             pl.dn[b] = d;
