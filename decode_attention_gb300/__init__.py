@@ -23,6 +23,7 @@ from ._native import (  # noqa: F401
     PAGE_SIZE,
     GQAError,
     gqa_decode,
+    gqa_decode_noalloc,
     gqa_decode_paged,
     gqa_device_status,
     gqa_status_string,

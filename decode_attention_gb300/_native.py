@@ -32,7 +32,7 @@ GQA_DEVICE_BAD_LENGTH = 4
 PAGE_SIZE = 16
 
 EXPORTED_SYMBOLS = ("gqa_workspace_size", "gqa_workspace_init", "gqa_decode", "gqa_decode_paged",
-                    "gqa_device_status", "gqa_status_string")
+                    "gqa_device_status", "gqa_decode_noalloc", "gqa_status_string")
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +71,8 @@ def load_library(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.gqa_decode_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, vp,
                                          ci, vp, sz, vp]
         lib.gqa_decode_paged.restype = ci
+        lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, ci, vp]
+        lib.gqa_decode_noalloc.restype = ci
         lib.gqa_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gqa_device_status.restype = ci
         lib.gqa_status_string.argtypes = [ci]
@@ -189,6 +191,28 @@ def gqa_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tens
         block_table.shape[1], page_size, H, KVH, D, int(window), _ptr(out), _out_code(out),
         _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
     _check("gqa_decode_paged", st)
+    return out
+
+
+def gqa_decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
+                       window: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """gqa_decode for callers that cannot allocate: the library's fixed device scratch
+    replaces the workspace.  ``out`` must be supplied (bf16 or fp32 [B, H, D]), so the
+    call allocates nothing on the device."""
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("k", k, torch.bfloat16, 4)
+    _check_tensor("v", v, torch.bfloat16, 4)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    B, H, D = q.shape
+    _, S, KVH, _ = k.shape
+    _require(tuple(k.shape) == (B, S, KVH, D) and v.shape == k.shape, "k/v shape mismatch")
+    _require(seq_lens.shape[0] == B, "seq_lens must have B entries")
+    _check_tensor("out", out, out.dtype, 3)
+    _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
+    st = load_library().gqa_decode_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, S, H, KVH, D, int(window), _ptr(out),
+        _out_code(out), _stream_handle(stream, q.device))
+    _check("gqa_decode_noalloc", st)
     return out
 
 

@@ -1,0 +1,150 @@
+// gqa_decode_noalloc: the contiguous-cache decode attention call for callers
+// that cannot allocate device memory (see include/gqa_decode.h).
+//
+// Its scratch -- status word, claim counter, per-segment partial lists and the
+// split-softmax partials -- lives in one file-scope device array of fixed size
+// instead of a workspace the caller passes or the library allocates.  The
+// array's device address is looked up once per device with
+// cudaGetSymbolAddress (host code must never hand the symbol itself to a
+// kernel: on the host it is only a stand-in).  The kernels are the same ones
+// gqa_decode launches.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "gqa_decode.h"
+#include "launch.h"
+
+namespace {
+
+// The fixed scratch.  Every GPU that loads this library holds it until exit.
+__device__ __align__(256) uint8_t g_noalloc_scratch[GQA_NOALLOC_SCRATCH_BYTES];
+
+// Layout of the fixed scratch for one call (offsets in bytes):
+//   [0, 4)         status word        } cleared before every call
+//   [64, 68)       claim counter      }
+//   [256, ...)     B*KVH partial lists (int4)
+//   [ml, ...)      slots x G x 2 floats;  [acc, ...) slots x G x D floats
+// with slots = grid + B*KVH + min(4 grid, 1024): static unit j of the kernel
+// keeps its piece of segment u at slot j + u (j < grid), dynamic chunk k at
+// slot grid + B*KVH + k (k < min(4 grid, 1024)).
+constexpr size_t kClearBytes = 128;
+constexpr size_t kSegsOff = 256;
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct FixedLayout {
+    size_t ml_off, acc_off, total;
+    int dyn_slot_base;
+};
+
+FixedLayout fixed_layout(int grid, int B, int KVH, int G, int D) {
+    const int dyn = 4 * grid < gqa::kMaxDynUnits ? 4 * grid : gqa::kMaxDynUnits;
+    const size_t slots = static_cast<size_t>(grid) + static_cast<size_t>(B) * KVH + dyn;
+    FixedLayout f;
+    f.ml_off = round256(kSegsOff + static_cast<size_t>(B) * KVH * 16);
+    f.acc_off = round256(f.ml_off + slots * G * 2 * sizeof(float));
+    f.total = round256(f.acc_off + slots * G * D * sizeof(float));
+    f.dyn_slot_base = grid + B * KVH;
+    return f;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceScratch {
+    std::mutex mu;
+    bool ready = false;
+    uint8_t* ptr = nullptr;   // device address of g_noalloc_scratch on this device
+    int sm_count = 0;
+};
+
+DeviceScratch g_scratch[kMaxDevices];
+
+// Once per device, with that device current: the array's device address and
+// the SM count.
+gqa_status_t device_scratch(uint8_t** ptr, int* grid) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+    DeviceScratch& ds = g_scratch[dev];
+    std::lock_guard<std::mutex> lock(ds.mu);
+    if (!ds.ready) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return GQA_ERR_CUDA;
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return GQA_ERR_CUDA;
+        ds.ptr = static_cast<uint8_t*>(p);
+        ds.sm_count = n < gqa::kMaxCtas ? n : gqa::kMaxCtas;
+        ds.ready = true;
+    }
+    *ptr = ds.ptr;
+    *grid = ds.sm_count;
+    return GQA_OK;
+}
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" gqa_status_t gqa_decode_noalloc(const void* q, const void* k, const void* v,
+                                           const int32_t* seq_lens, int B, int S, int H, int KVH,
+                                           int D, int window, void* out, gqa_out_dtype_t out_dtype,
+                                           gqa_stream_t stream) {
+    // argument checks: the same rules as gqa_decode
+    const bool sliding = (H == 32 && KVH == 16 && D == 256);
+    const bool global = (H == 32 && KVH == 4 && D == 512);
+    if (S < 1 || S > GQA_MAX_SEQ || B < 0 || B > GQA_MAX_BATCH || window < 0)
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (out_dtype != GQA_OUT_BF16 && out_dtype != GQA_OUT_F32) return GQA_ERR_INVALID_ARGUMENT;
+    if (!sliding && !global) return GQA_ERR_UNSUPPORTED;
+    if (B == 0) return GQA_OK;
+    if (!q || !k || !v || !seq_lens || !out) return GQA_ERR_INVALID_ARGUMENT;
+    if (!aligned_to(q, 16) || !aligned_to(k, 16) || !aligned_to(v, 16) || !aligned_to(out, 16) ||
+        !aligned_to(seq_lens, 4))
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (!gqa::tensor_map_encoder()) return GQA_ERR_CUDA;
+
+    uint8_t* ws = nullptr;
+    int grid = 0;
+    gqa_status_t st = device_scratch(&ws, &grid);
+    if (st != GQA_OK) return st;
+    const int G = H / KVH;
+    const FixedLayout lay = fixed_layout(grid, B, KVH, G, D);
+    if (lay.total > GQA_NOALLOC_SCRATCH_BYTES) return GQA_ERR_WORKSPACE;   // call too large
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the status word and the claim counter must start at zero
+    if (cudaMemsetAsync(ws, 0, kClearBytes, s) != cudaSuccess) return GQA_ERR_CUDA;
+
+    gqa::LaunchArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.k = k;
+    a.v = v;
+    a.rows = static_cast<uint64_t>(S);
+    a.outer = static_cast<uint64_t>(B);
+    a.p.q = static_cast<const __nv_bfloat16*>(q);
+    a.p.seq_lens = seq_lens;
+    a.p.block_table = nullptr;
+    a.p.out = out;
+    a.p.ws_acc = reinterpret_cast<float*>(ws + lay.acc_off);
+    a.p.ws_ml = reinterpret_cast<float*>(ws + lay.ml_off);
+    a.p.ws_segs = reinterpret_cast<int4*>(ws + kSegsOff);
+    a.p.ws_flags = reinterpret_cast<uint32_t*>(ws);
+    a.p.ws_claim = reinterpret_cast<uint32_t*>(ws + 64);
+    a.p.dyn_slot_base = lay.dyn_slot_base;
+    a.p.B = B;
+    a.p.H = H;
+    a.p.KVH = KVH;
+    a.p.capacity = S;
+    a.p.window = window;
+    a.p.num_pages = 0;
+    a.p.max_pages = 0;
+    a.p.out_f32 = out_dtype == GQA_OUT_F32 ? 1 : 0;
+    a.grid = grid;
+    a.stream = s;
+    const cudaError_t e = sliding ? gqa::launch_sliding(a, false) : gqa::launch_global(a, false);
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}

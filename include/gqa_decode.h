@@ -153,6 +153,45 @@ gqa_status_t gqa_decode_paged(const void *q, const void *k_pages, const void *v_
  */
 gqa_status_t gqa_device_status(void *workspace, uint32_t *flags, gqa_stream_t stream);
 
+/*
+ * gqa_decode without any allocation, for callers that cannot allocate device
+ * memory during a call: for example a plugin layer that is handed only the
+ * tensors of one operator, or a runtime whose device memory all belongs to a
+ * fixed pool.  gqa_decode needs a workspace the caller supplies or the library
+ * allocates (cudaMalloc); this call instead uses one fixed device array of
+ * GQA_NOALLOC_SCRATCH_BYTES bytes, built into the library.  Every GPU that
+ * loads the library holds that array until the process exits.
+ *
+ * No counterpart on the reference pages: it is an interface convenience of
+ * this library, computing exactly what gqa_decode computes.
+ *
+ * Arguments, layouts and errors are those of gqa_decode, without the workspace.
+ * In addition it returns GQA_ERR_WORKSPACE, enqueueing nothing, when the call
+ * needs more scratch than the array holds.  The need is
+ *   (grid + B*KVH + min(4*grid, 1024)) * g * (D + 2) * 4 bytes plus about
+ *   16*B*KVH + 1 KB, where grid = the device's SM count.
+ * On a 152-SM GB300 that covers every slidingDecodeGQA call (B <= 256) and
+ * decodeGQA calls with B <= 64.
+ *
+ * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.  It does the following:
+ *   - Its first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and the SM count.  Make
+ *     that first call before any stream capture.
+ *   - Every call clears the array's status word and claim counter with a
+ *     128-byte cudaMemsetAsync on `stream`.
+ * All calls on a device share the one array, and it keeps the last call's
+ * contents.  Calls whose kernels overlap on the GPU (different streams) race on
+ * it; serialise them.  The device status bits of this call are not reported
+ * (gqa_device_status reads workspaces only).
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+gqa_status_t gqa_decode_noalloc(const void *q, const void *k, const void *v,
+                                const int32_t *seq_lens, int B, int S, int H, int KVH, int D,
+                                int window, void *out, gqa_out_dtype_t out_dtype,
+                                gqa_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *gqa_status_string(gqa_status_t status);
 
