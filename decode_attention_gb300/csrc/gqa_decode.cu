@@ -185,6 +185,7 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
     a.p.ws_flags = reinterpret_cast<uint32_t*>(w + kFlagsOff);
     a.p.ws_claim = reinterpret_cast<uint32_t*>(w + kClaimOff);
     a.p.dyn_slot_base = kMaxCtas + c.B * c.KVH;
+    a.p.max_dyn = gqa::kMaxDynUnits;
     a.p.B = c.B;
     a.p.H = c.H;
     a.p.KVH = c.KVH;

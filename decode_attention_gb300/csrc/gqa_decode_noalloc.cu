@@ -27,9 +27,11 @@ __device__ __align__(256) uint8_t g_noalloc_scratch[GQA_NOALLOC_SCRATCH_BYTES];
 //   [64, 68)       claim counter      }
 //   [256, ...)     B*KVH partial lists (int4)
 //   [ml, ...)      slots x G x 2 floats;  [acc, ...) slots x G x D floats
-// with slots = grid + B*KVH + min(4 grid, 1024): static unit j of the kernel
-// keeps its piece of segment u at slot j + u (j < grid), dynamic chunk k at
-// slot grid + B*KVH + k (k < min(4 grid, 1024)).
+// with slots = grid + B*KVH + dyn: static unit j of the kernel keeps its piece
+// of segment u at slot j + u (j < grid), dynamic chunk k at slot grid + B*KVH + k
+// (k < dyn).  dyn is min(kDynChunksPerCta grid, kMaxDynUnits) when that fits the
+// array, else what does fit (down to 0: the kernel then splits the work into
+// static units only); the kernel is told the bound and never exceeds it.
 constexpr size_t kClearBytes = 128;
 constexpr size_t kSegsOff = 256;
 
@@ -37,18 +39,34 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct FixedLayout {
     size_t ml_off, acc_off, total;
-    int dyn_slot_base;
+    int dyn_slot_base, max_dyn;
 };
 
-FixedLayout fixed_layout(int grid, int B, int KVH, int G, int D) {
-    const int dyn = 4 * grid < gqa::kMaxDynUnits ? 4 * grid : gqa::kMaxDynUnits;
+FixedLayout layout_with(int grid, int B, int KVH, int G, int D, int dyn) {
     const size_t slots = static_cast<size_t>(grid) + static_cast<size_t>(B) * KVH + dyn;
     FixedLayout f;
     f.ml_off = round256(kSegsOff + static_cast<size_t>(B) * KVH * 16);
     f.acc_off = round256(f.ml_off + slots * G * 2 * sizeof(float));
     f.total = round256(f.acc_off + slots * G * D * sizeof(float));
     f.dyn_slot_base = grid + B * KVH;
+    f.max_dyn = dyn;
     return f;
+}
+
+// The layout with as many dynamic slots (up to the kernel's own bound) as the
+// array holds; total > GQA_NOALLOC_SCRATCH_BYTES when not even dyn = 0 fits.
+FixedLayout fixed_layout(int grid, int B, int KVH, int G, int D) {
+    const int want = gqa::kDynChunksPerCta * grid < gqa::kMaxDynUnits
+                         ? gqa::kDynChunksPerCta * grid
+                         : gqa::kMaxDynUnits;
+    const FixedLayout none = layout_with(grid, B, KVH, G, D, 0);
+    if (none.total > GQA_NOALLOC_SCRATCH_BYTES) return none;
+    // each slot takes G (D + 2) floats; 512 bytes cover the two 256-byte roundings
+    const size_t per_slot = static_cast<size_t>(G) * (D + 2) * sizeof(float);
+    const size_t spare = GQA_NOALLOC_SCRATCH_BYTES - none.total;
+    const size_t fit = spare >= 512 ? (spare - 512) / per_slot : 0;
+    const int dyn = fit < static_cast<size_t>(want) ? static_cast<int>(fit) : want;
+    return layout_with(grid, B, KVH, G, D, dyn);
 }
 
 constexpr int kMaxDevices = 64;
@@ -135,6 +153,7 @@ extern "C" gqa_status_t gqa_decode_noalloc(const void* q, const void* k, const v
     a.p.ws_flags = reinterpret_cast<uint32_t*>(ws);
     a.p.ws_claim = reinterpret_cast<uint32_t*>(ws + 64);
     a.p.dyn_slot_base = lay.dyn_slot_base;
+    a.p.max_dyn = lay.max_dyn;
     a.p.B = B;
     a.p.H = H;
     a.p.KVH = KVH;

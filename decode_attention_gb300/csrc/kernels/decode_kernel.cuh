@@ -54,7 +54,13 @@ constexpr int kChunkElems = 64;       // bf16 per 128-byte swizzle row
 constexpr int kChunkBytes = 2048;     // one chunk of a box: 16 rows x 128 B
 constexpr int kMaxBatch = 256;
 constexpr int kMaxDynUnits = 1024;    // bound on dynamic chunks (sizes the workspace)
-constexpr int kDynChunksPerCta = 4;   // dynamic work aimed for, in chunks per CTA
+constexpr int kDynChunksPerCta = 6;   // bound on dynamic chunks per CTA
+constexpr int kDynSmallPerCta = 4;    // chunks per CTA when the work is small
+constexpr int kDynMinSpan = 5;        // segment positions per chunk, in chunk lengths, at least
+constexpr int kDynFraction = 7;       // about 1/7 of the work is dynamic: covers the spread
+                                      // of per-SM memory throughput (~13% between SMs)
+constexpr int kDynMinChunk = 128;     // positions: keeps the per-piece epilogue small
+constexpr int kDynMinShare = 256;     // positions per CTA below which all work is static
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // a wait gives up after 2 s
 constexpr uint32_t kWaitMaxRounds = 1u << 24;        // ... or after this many polling rounds
@@ -75,6 +81,7 @@ struct DecodeParams {
     uint32_t* ws_flags;           // device status word
     uint32_t* ws_claim;           // dynamic-chunk claim counter (reset by the combine kernel)
     int dyn_slot_base;            // first workspace slot of the dynamic chunks (> grid + B*KVH - 2)
+    int max_dyn;                  // dynamic-chunk slots the workspace holds (<= kMaxDynUnits)
     int B, H, KVH;
     int capacity;                 // S, or 16 * max_pages
     int window;                   // 0 = full history
@@ -223,77 +230,136 @@ __device__ __forceinline__ void store_out4(const DecodeParams& p, size_t idx, fl
 }
 
 // ---------------------------------------------------------------------------
-// Plan computation (warp 0).  Lengths are clamped to [0, capacity]; the dynamic
-// share of each segment is floor(n_b * f / c_dyn) chunks with
-// f = min(1/5, kDynChunksPerCta * grid * c_dyn / N), so all segments together
-// hold at most kDynChunksPerCta chunks per CTA and at most kMaxDynUnits (exact
-// 32-bit integer arithmetic: n_b * target < 2^31 and N < 2^32, so the total can
-// never exceed the bound the workspace is sized for).
+// Plan computation (warp 0; lane l owns sequences 8l .. 8l + 7).  Lengths are
+// clamped to [0, capacity].  The tail of each segment becomes dynamic chunks of
+// c_dyn positions, about one chunk per F positions of the segment.  With much
+// work per CTA, c_dyn is chosen so that about 1/kDynFraction of the work is
+// dynamic in at most cap = min(kDynChunksPerCta * grid, max_dyn) chunks (the
+// slots the workspace holds), F = kDynFraction c_dyn; with little, chunks keep
+// their minimum length and number about kDynSmallPerCta per CTA (F = N /
+// (kDynSmallPerCta grid)), at most 1/kDynMinSpan of the work (F >= kDynMinSpan
+// c_dyn).  The T chunks per kv head are spread over the sequences in proportion
+// to their lengths, and none takes more than half of a segment.
+//
+// Only T <= cap / KVH bounds the chunk count, so c_dyn, F and T may be rounded
+// freely: they are taken in float (all CTAs compute the same values), which keeps
+// this warp's serial latency low.  The counts themselves are integers: n_b <=
+// 2^18, B <= 256, KVH <= 16, so every sum fits 32 bits.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, int grid,
-                                           int lane) {
+                                           int lane, int cta) {
     constexpr int kPer = kMaxBatch / 32;
     const int B = p.B, KVH = p.KVH;
-    long long tot = 0;
+    int n[kPer];
+    {
+        int L[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int b = lane * kPer + j;
+            L[j] = b < B ? __ldg(p.seq_lens + b) : 0;
+        }
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int b = lane * kPer + j;
+            int x = L[j];
+            if (x < 0 || x > p.capacity) {
+                bad = b < B;
+                x = x < 0 ? 0 : p.capacity;
+            }
+            const int lo = (p.window > 0 && x > p.window) ? x - p.window : 0;
+            n[j] = b < B ? x - lo : 0;
+            if (b < B) {
+                pl.lo[b] = lo;
+                pl.n[b] = n[j];
+            }
+        }
+        if (bad && cta == 0) atomicOr(p.ws_flags, kFlagBadLength);
+    }
+    // exclusive prefix of n over the sequences (lane-local run, then a warp scan)
+    int nloc[kPer], nrun = 0;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-        const int b = lane * kPer + j;
-        if (b < B) tot += pl.n[b];
+        nloc[j] = nrun;
+        nrun += n[j];
     }
+    int nincl = nrun;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-    const long long N = tot * KVH;
-    const long long g = N < grid ? N : grid;
-    const long long share = g > 0 ? N / g : 0;
-    long long c = (share / 4) / 32 * 32;
-    c = c < 32 ? 32 : (c > 128 ? 128 : c);
-    const bool use_dyn = share >= 128;
-    const long long target = static_cast<long long>(kDynChunksPerCta) * grid < kMaxDynUnits
-                                 ? static_cast<long long>(kDynChunksPerCta) * grid
-                                 : kMaxDynUnits;
-    // d_b = floor(n_b * target / N) when that is below n_b / (5 c), else floor(n_b / (5 c))
-    const bool by_target = target * c * 5 < N;
-    const uint32_t tgt32 = static_cast<uint32_t>(target);
-    const uint32_t n32 = static_cast<uint32_t>(N);
-    const uint32_t five_c = static_cast<uint32_t>(5 * c);
-    long long sloc[kPer], srun = 0;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int tn = __shfl_up_sync(0xffffffffu, nincl, off);
+        if (lane >= off) nincl += tn;
+    }
+    const int nexcl = nincl - nrun;
+    const uint32_t tot = static_cast<uint32_t>(__shfl_sync(0xffffffffu, nincl, 31));
+    const uint32_t N = tot * static_cast<uint32_t>(KVH);
+    const uint32_t ugrid = static_cast<uint32_t>(grid);
+    const uint32_t g = N < ugrid ? N : ugrid;
+    const uint32_t cdyn = static_cast<uint32_t>(kDynChunksPerCta) * ugrid;
+    const uint32_t cap = cdyn < static_cast<uint32_t>(p.max_dyn) ? cdyn : static_cast<uint32_t>(p.max_dyn);
+    // floor(N / g) >= kDynMinShare
+    const bool use_dyn = g > 0 && N >= static_cast<uint32_t>(kDynMinShare) * g && cap > 0;
+    int c = kDynMinChunk, T = 0;
+    if (use_dyn) {
+        const float Nf = static_cast<float>(N);
+        // chunk length: at least kDynMinChunk, about N / (kDynFraction cap), whole tiles
+        const int cf = static_cast<int>(ceilf(Nf / static_cast<float>(kDynFraction * cap)));
+        c = ((cf + 31) / 32) * 32;
+        c = c < kDynMinChunk ? kDynMinChunk : c;
+        const uint32_t csmall = static_cast<uint32_t>(kDynSmallPerCta) * ugrid;
+        const float small = static_cast<float>(csmall < cap ? csmall : cap);
+        const float cff = static_cast<float>(c);
+        const float F = fmaxf(fminf(ceilf(Nf / small), kDynFraction * cff), kDynMinSpan * cff);
+        const int t = static_cast<int>(static_cast<float>(tot) / F + 0.5f);
+        const int tmax = static_cast<int>(cap) / KVH;
+        T = t < tmax ? t : tmax;
+    }
+    // sequence b gets d_b = f(P_b + n_b) - f(P_b) chunks per kv head, P_b the sum of
+    // n over the sequences before b and f(x) = floor(x * (T / sum n)): f is monotone
+    // and f(sum n) <= T, so the d_b are >= 0 and add up to at most T
+    const float r = T > 0 ? static_cast<float>(T) / static_cast<float>(tot) : 0.0f;
+    const float inv2c = 1.0f / static_cast<float>(2 * c);
+    uint32_t sloc[kPer], srun = 0;
     int dloc[kPer], drun = 0;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const int b = lane * kPer + j;
-        int d = 0, sn = 0;
+        int d = 0;
+        if (T > 0 && n[j] > 0) {
+            const int x0 = nexcl + nloc[j];
+            d = __float2int_rd(__fmul_rn(static_cast<float>(x0 + n[j]), r)) -
+                __float2int_rd(__fmul_rn(static_cast<float>(x0), r));
+            int h = __float2int_rd(static_cast<float>(n[j]) * inv2c);   // floor(n / 2c)
+            h -= (h * 2 * c > n[j]) ? 1 : 0;
+            d = d < h ? d : h;
+        }
+        const int sn = n[j] - d * c;
         if (b < B) {
-            const uint32_t nb = static_cast<uint32_t>(pl.n[b]);
-            d = !use_dyn ? 0
-                : by_target ? static_cast<int>((nb * tgt32) / n32)
-                            : static_cast<int>(nb / five_c);
-            sn = pl.n[b] - d * static_cast<int>(c);
             pl.sn[b] = sn;
             pl.dn[b] = d;
         }
         sloc[j] = srun;
         dloc[j] = drun;
-        srun += static_cast<long long>(sn) * KVH;
+        srun += static_cast<uint32_t>(sn) * static_cast<uint32_t>(KVH);
         drun += d * KVH;
     }
-    long long sincl = srun;
+    uint32_t sincl = srun;
     int dincl = drun;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const long long ts = __shfl_up_sync(0xffffffffu, sincl, off);
+        const uint32_t ts = __shfl_up_sync(0xffffffffu, sincl, off);
         const int td = __shfl_up_sync(0xffffffffu, dincl, off);
         if (lane >= off) {
             sincl += ts;
             dincl += td;
         }
     }
-    const long long sexcl = sincl - srun;
+    const uint32_t sexcl = sincl - srun;
     const int dexcl = dincl - drun;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const int b = lane * kPer + j;
         if (b <= B) {
-            pl.spref[b] = sexcl + sloc[j];
+            pl.spref[b] = static_cast<long long>(sexcl + sloc[j]);
             pl.dpref[b] = dexcl + dloc[j];
         }
     }
@@ -302,10 +368,10 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
             pl.spref[kMaxBatch] = sincl;
             pl.dpref[kMaxBatch] = dincl;
         }
-        pl.n_static = sincl;
+        pl.n_static = static_cast<long long>(sincl);
         pl.n_dyn = dincl;
-        pl.c_dyn = static_cast<int>(c);
-        pl.g_eff = static_cast<int>(sincl < grid ? sincl : grid);
+        pl.c_dyn = c;
+        pl.g_eff = static_cast<int>(sincl < ugrid ? sincl : ugrid);
     }
 }
 
@@ -354,18 +420,7 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
     ptx::allow_dependent_launch();
 
     // ---- plan: clamped lengths, attended ranges, static/dynamic split ----
-    for (int b = tid; b < B; b += blockDim.x) {
-        int L = p.seq_lens[b];
-        if (L < 0 || L > p.capacity) {
-            if (cta == 0) atomicOr(p.ws_flags, kFlagBadLength);
-            L = L < 0 ? 0 : p.capacity;
-        }
-        const int lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
-        pl.lo[b] = lo;
-        pl.n[b] = L - lo;
-    }
-    __syncthreads();
-    if (warp == 0) build_plan(pl, p, gridDim.x, lane);
+    if (warp == 0) build_plan(pl, p, gridDim.x, lane, cta);
     __syncthreads();
 
     // sequences with nothing to attend produce zeros (the empty sum)

@@ -167,11 +167,14 @@ gqa_status_t gqa_device_status(void *workspace, uint32_t *flags, gqa_stream_t st
  *
  * Arguments, layouts and errors are those of gqa_decode, without the workspace.
  * In addition it returns GQA_ERR_WORKSPACE, enqueueing nothing, when the call
- * needs more scratch than the array holds.  The need is
- *   (grid + B*KVH + min(4*grid, 1024)) * g * (D + 2) * 4 bytes plus about
- *   16*B*KVH + 1 KB, where grid = the device's SM count.
- * On a 152-SM GB300 that covers every slidingDecodeGQA call (B <= 256) and
- * decodeGQA calls with B <= 64.
+ * needs more scratch than the array holds.  The need is at least
+ *   (grid + B*KVH) * g * (D + 2) * 4 bytes plus about 16*B*KVH + 1 KB,
+ * where grid = the device's SM count; what is left holds partials of up to
+ * min(6*grid, 1024) dynamically scheduled chunks, the slots gqa_decode always
+ * has.  Fewer slots leave the result unchanged up to rounding but balance the
+ * load across SMs less well.  On a 152-SM GB300 the array covers every
+ * slidingDecodeGQA call (B <= 256, all slots) and decodeGQA calls with
+ * B <= 216 (all slots for B <= 1, about 740 of 912 at B = 32).
  *
  * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
  * routine.  It does the following:

@@ -81,3 +81,21 @@ def test_rejects_calls_larger_than_the_scratch():
     with pytest.raises(gqa.GQAError) as e:
         gqa.gqa_decode_noalloc(q, k, k, lens, 0, out)
     assert e.value.status == gqa.GQA_ERR_WORKSPACE
+
+
+@pytest.mark.gpu
+@needs_gpu
+def test_decode_global_with_fewer_dynamic_slots():
+    # decodeGQA with B = 64 fits the scratch with only part of the dynamic-chunk
+    # slots gqa_decode has (about 610 of 912 on 152 SMs): the kernel sizes its
+    # chunks to that bound, and the result must not change beyond rounding
+    geo = inputs.geometry("global")
+    B, S = 64, 8192
+    lens = np.random.default_rng(5).integers(6000, S + 1, B).tolist()
+    case = inputs.contiguous_case(B, S, geo["H"], geo["KVH"], geo["D"], lens, seed=78, device="cuda")
+    ref = gqa.gqa_decode(case["q"], case["k"], case["v"], case["seq_lens"], 0, out_dtype=torch.float32)
+    for _ in range(2):
+        out = torch.full_like(ref, float("nan"))
+        gqa.gqa_decode_noalloc(case["q"], case["k"], case["v"], case["seq_lens"], 0, out)
+        torch.cuda.synchronize()
+        close(out, ref)
