@@ -21,7 +21,7 @@
 namespace gqa {
 
 constexpr int kCombineThreads = 128;    // float4 outputs per work item
-constexpr int kCombineBatch = 8;        // pieces whose loads are in flight together
+constexpr int kCombineBatch = 16;       // pieces whose loads are in flight together
 
 template <int G, int D>
 __global__ void __launch_bounds__(kCombineThreads)

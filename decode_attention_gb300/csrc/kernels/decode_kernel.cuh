@@ -53,10 +53,12 @@ constexpr int kPageRows = 16;         // positions per page = TMA box height on 
 constexpr int kChunkElems = 64;       // bf16 per 128-byte swizzle row
 constexpr int kChunkBytes = 2048;     // one chunk of a box: 16 rows x 128 B
 constexpr int kMaxBatch = 256;
-constexpr int kMaxDynUnits = 1024;    // bound on dynamic chunks (sizes the workspace)
-constexpr int kDynChunksPerCta = 6;   // bound on dynamic chunks per CTA
+constexpr int kMaxDynUnits = 2048;    // bound on dynamic chunks (sizes the workspace)
+constexpr int kDynChunksPerCta = 8;   // bound on dynamic chunks per CTA
 constexpr int kDynSmallPerCta = 4;    // chunks per CTA when the work is small
 constexpr int kDynMinSpan = 5;        // segment positions per chunk, in chunk lengths, at least
+constexpr int kDynTailPerCta = 2;     // short chunks (claimed last) per CTA
+constexpr int kDynTailRatio = 4;      // long / short chunk length
 constexpr int kDynFraction = 7;       // about 1/7 of the work is dynamic: covers the spread
                                       // of per-SM memory throughput (~13% between SMs)
 constexpr int kDynMinChunk = 128;     // positions: keeps the per-piece epilogue small
@@ -102,12 +104,16 @@ struct PlanSmem {
     int lo[kMaxBatch];               // first attended position
     int n[kMaxBatch];                // attended positions
     int sn[kMaxBatch];               // static head length of each segment of sequence b
-    int dn[kMaxBatch];               // dynamic chunks of each segment of sequence b
+    int dn[kMaxBatch];               // long dynamic chunks of each segment of sequence b
+    int dn1[kMaxBatch];              // short dynamic chunks of each segment of sequence b
     long long spref[kMaxBatch + 1];  // KVH * sum_{b' < b} sn_b'
     int dpref[kMaxBatch + 1];        // KVH * sum_{b' < b} dn_b'
+    int dpref1[kMaxBatch + 1];       // KVH * sum_{b' < b} dn1_b'
     long long n_static;              // Ns
-    int n_dyn;                       // dynamic chunks in total
-    int c_dyn;                       // positions per dynamic chunk
+    int n_dyn;                       // dynamic chunks in total (long, then short)
+    int n_dyn0;                      // long dynamic chunks
+    int c_dyn;                       // positions per long dynamic chunk
+    int c_dyn1;                      // positions per short dynamic chunk
     int g_eff;                       // static units (= CTAs with work)
 };
 
@@ -142,8 +148,10 @@ struct SegmentParts {
         const long long ss = pl.spref[b] + static_cast<long long>(kvh) * pl.sn[b];
         first_s = static_unit_of(pl, ss);
         ns_parts = static_unit_of(pl, ss + pl.sn[b] - 1) - first_s + 1;
-        dk0 = pl.dpref[b] + kvh * pl.dn[b];
-        nd_parts = pl.dn[b];
+        // the dynamic slots of a segment are contiguous: its long chunks, then its
+        // short ones (whatever order they are claimed in)
+        nd_parts = pl.dn[b] + pl.dn1[b];
+        dk0 = pl.dpref[b] + pl.dpref1[b] + kvh * nd_parts;
     }
     __device__ __forceinline__ int count() const { return ns_parts + nd_parts; }
     __device__ __forceinline__ size_t slot(int j, int u) const {
@@ -231,23 +239,29 @@ __device__ __forceinline__ void store_out4(const DecodeParams& p, size_t idx, fl
 
 // ---------------------------------------------------------------------------
 // Plan computation (warp 0; lane l owns sequences 8l .. 8l + 7).  Lengths are
-// clamped to [0, capacity].  The tail of each segment becomes dynamic chunks of
-// c_dyn positions, about one chunk per F positions of the segment.  With much
-// work per CTA, c_dyn is chosen so that about 1/kDynFraction of the work is
-// dynamic in at most cap = min(kDynChunksPerCta * grid, max_dyn) chunks (the
-// slots the workspace holds), F = kDynFraction c_dyn; with little, chunks keep
-// their minimum length and number about kDynSmallPerCta per CTA (F = N /
-// (kDynSmallPerCta grid)), at most 1/kDynMinSpan of the work (F >= kDynMinSpan
-// c_dyn).  The T chunks per kv head are spread over the sequences in proportion
-// to their lengths, and none takes more than half of a segment.
+// clamped to [0, capacity].  The tail of each segment becomes dynamic chunks:
+// long ones of c_dyn positions, then short ones of c_dyn1 ~ c_dyn / 4, all whole
+// tiles of `unit` positions.  At most cap = min(kDynChunksPerCta * grid,
+// max_dyn) chunks exist (the slots the workspace holds); kDynTailPerCta * grid
+// of them (at most half) are kept for the short ones, the rest bound the long.
+//  - Long: with much work per CTA, c_dyn is chosen so that about 1/kDynFraction
+//    of the work is dynamic, about one chunk per F = kDynFraction c_dyn positions
+//    of a segment; with little, chunks keep their minimum length and number about
+//    kDynSmallPerCta per CTA (F = N / (kDynSmallPerCta grid)), at most
+//    1/kDynMinSpan of the work.
+//  - Short: claimed after every long one.  When the long chunks run out, CTAs
+//    still differ by up to one long chunk of work; the short ones even that out,
+//    so the last CTA ends about one short chunk after the others.
+// The T (T1) chunks per kv head are spread over the sequences in proportion to
+// their lengths; together they never take more than half of a segment.
 //
-// Only T <= cap / KVH bounds the chunk count, so c_dyn, F and T may be rounded
-// freely: they are taken in float (all CTAs compute the same values), which keeps
-// this warp's serial latency low.  The counts themselves are integers: n_b <=
-// 2^18, B <= 256, KVH <= 16, so every sum fits 32 bits.
+// Only the chunk counts are bounded, so c_dyn, F and T may be rounded freely:
+// they are taken in float (all CTAs compute the same values), which keeps this
+// warp's serial latency low.  The counts themselves are integers: n_b <= 2^18,
+// B <= 256, KVH <= 16, so every sum fits 32 bits.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, int grid,
-                                           int lane, int cta) {
+                                           int lane, int cta, int unit) {
     constexpr int kPer = kMaxBatch / 32;
     const int B = p.B, KVH = p.KVH;
     int n[kPer];
@@ -296,81 +310,120 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
     const uint32_t g = N < ugrid ? N : ugrid;
     const uint32_t cdyn = static_cast<uint32_t>(kDynChunksPerCta) * ugrid;
     const uint32_t cap = cdyn < static_cast<uint32_t>(p.max_dyn) ? cdyn : static_cast<uint32_t>(p.max_dyn);
+    // the short chunks' slots are set aside first (at most half of them)
+    const uint32_t tail_want = static_cast<uint32_t>(kDynTailPerCta) * ugrid;
+    const uint32_t tail_cap = tail_want < cap / 2 ? tail_want : cap / 2;
+    const uint32_t long_cap = cap - tail_cap;
     // floor(N / g) >= kDynMinShare
-    const bool use_dyn = g > 0 && N >= static_cast<uint32_t>(kDynMinShare) * g && cap > 0;
+    const bool use_dyn = g > 0 && N >= static_cast<uint32_t>(kDynMinShare) * g && long_cap > 0;
     int c = kDynMinChunk, T = 0;
     if (use_dyn) {
         const float Nf = static_cast<float>(N);
         // chunk length: at least kDynMinChunk, about N / (kDynFraction cap), whole tiles
-        const int cf = static_cast<int>(ceilf(Nf / static_cast<float>(kDynFraction * cap)));
-        c = ((cf + 31) / 32) * 32;
+        const int cf = static_cast<int>(ceilf(Nf / static_cast<float>(kDynFraction * long_cap)));
+        c = ((cf + unit - 1) / unit) * unit;
         c = c < kDynMinChunk ? kDynMinChunk : c;
         const uint32_t csmall = static_cast<uint32_t>(kDynSmallPerCta) * ugrid;
-        const float small = static_cast<float>(csmall < cap ? csmall : cap);
+        const float small = static_cast<float>(csmall < long_cap ? csmall : long_cap);
         const float cff = static_cast<float>(c);
         const float F = fmaxf(fminf(ceilf(Nf / small), kDynFraction * cff), kDynMinSpan * cff);
         const int t = static_cast<int>(static_cast<float>(tot) / F + 0.5f);
-        const int tmax = static_cast<int>(cap) / KVH;
+        const int tmax = static_cast<int>(long_cap) / KVH;
         T = t < tmax ? t : tmax;
     }
-    // sequence b gets d_b = f(P_b + n_b) - f(P_b) chunks per kv head, P_b the sum of
-    // n over the sequences before b and f(x) = floor(x * (T / sum n)): f is monotone
-    // and f(sum n) <= T, so the d_b are >= 0 and add up to at most T
+    // short chunks of c1 ~ c / kDynTailRatio positions, about kDynTailPerCta per CTA,
+    // claimed after the long ones: when the long chunks run out, CTAs still differ
+    // by up to one long chunk of work, and the short ones even that out
+    int c1 = c, T1 = 0;
+    if (T > 0) {
+        // (never below kDynMinChunk: shorter pieces cost more in their epilogue
+        // and claim than they gain in balance)
+        c1 = (c / kDynTailRatio) / unit * unit;
+        if (c1 >= kDynMinChunk) {
+            const int want = (static_cast<int>(tail_cap) + KVH / 2) / KVH;
+            const int room = static_cast<int>(cap) / KVH - T;
+            T1 = want < room ? want : room;
+        } else {
+            c1 = c;
+        }
+    }
+    // sequence b gets d_b = f(P_b + n_b) - f(P_b) long chunks per kv head, P_b the sum
+    // of n over the sequences before b and f(x) = floor(x * (T / sum n)): f is
+    // monotone and f(sum n) <= T, so the d_b are >= 0 and add up to at most T; the
+    // same with T1 for the short ones.  Together they take at most half a segment.
     const float r = T > 0 ? static_cast<float>(T) / static_cast<float>(tot) : 0.0f;
+    const float r1 = T1 > 0 ? static_cast<float>(T1) / static_cast<float>(tot) : 0.0f;
     const float inv2c = 1.0f / static_cast<float>(2 * c);
+    const float inv2c1 = 1.0f / static_cast<float>(2 * c1);
     uint32_t sloc[kPer], srun = 0;
-    int dloc[kPer], drun = 0;
+    int dloc[kPer], drun = 0, d1loc[kPer], d1run = 0;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const int b = lane * kPer + j;
-        int d = 0;
+        int d = 0, d1 = 0;
         if (T > 0 && n[j] > 0) {
-            const int x0 = nexcl + nloc[j];
-            d = __float2int_rd(__fmul_rn(static_cast<float>(x0 + n[j]), r)) -
-                __float2int_rd(__fmul_rn(static_cast<float>(x0), r));
+            const float x0 = static_cast<float>(nexcl + nloc[j]);
+            const float x1 = static_cast<float>(nexcl + nloc[j] + n[j]);
+            d = __float2int_rd(__fmul_rn(x1, r)) - __float2int_rd(__fmul_rn(x0, r));
             int h = __float2int_rd(static_cast<float>(n[j]) * inv2c);   // floor(n / 2c)
             h -= (h * 2 * c > n[j]) ? 1 : 0;
             d = d < h ? d : h;
+            if (T1 > 0) {
+                d1 = __float2int_rd(__fmul_rn(x1, r1)) - __float2int_rd(__fmul_rn(x0, r1));
+                const int left = n[j] - 2 * d * c;                       // >= 0
+                int h1 = __float2int_rd(static_cast<float>(left) * inv2c1);
+                h1 -= (h1 * 2 * c1 > left) ? 1 : 0;
+                d1 = d1 < h1 ? d1 : h1;
+            }
         }
-        const int sn = n[j] - d * c;
+        const int sn = n[j] - d * c - d1 * c1;
         if (b < B) {
             pl.sn[b] = sn;
             pl.dn[b] = d;
+            pl.dn1[b] = d1;
         }
         sloc[j] = srun;
         dloc[j] = drun;
+        d1loc[j] = d1run;
         srun += static_cast<uint32_t>(sn) * static_cast<uint32_t>(KVH);
         drun += d * KVH;
+        d1run += d1 * KVH;
     }
     uint32_t sincl = srun;
-    int dincl = drun;
+    int dincl = drun, d1incl = d1run;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const uint32_t ts = __shfl_up_sync(0xffffffffu, sincl, off);
         const int td = __shfl_up_sync(0xffffffffu, dincl, off);
+        const int td1 = __shfl_up_sync(0xffffffffu, d1incl, off);
         if (lane >= off) {
             sincl += ts;
             dincl += td;
+            d1incl += td1;
         }
     }
     const uint32_t sexcl = sincl - srun;
-    const int dexcl = dincl - drun;
+    const int dexcl = dincl - drun, d1excl = d1incl - d1run;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const int b = lane * kPer + j;
         if (b <= B) {
             pl.spref[b] = static_cast<long long>(sexcl + sloc[j]);
             pl.dpref[b] = dexcl + dloc[j];
+            pl.dpref1[b] = d1excl + d1loc[j];
         }
     }
     if (lane == 31) {
         if (B == kMaxBatch) {
             pl.spref[kMaxBatch] = sincl;
             pl.dpref[kMaxBatch] = dincl;
+            pl.dpref1[kMaxBatch] = d1incl;
         }
         pl.n_static = static_cast<long long>(sincl);
-        pl.n_dyn = dincl;
+        pl.n_dyn0 = dincl;
+        pl.n_dyn = dincl + d1incl;
         pl.c_dyn = c;
+        pl.c_dyn1 = c1;
         pl.g_eff = static_cast<int>(sincl < ugrid ? sincl : ugrid);
     }
 }
@@ -420,7 +473,7 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
     ptx::allow_dependent_launch();
 
     // ---- plan: clamped lengths, attended ranges, static/dynamic split ----
-    if (warp == 0) build_plan(pl, p, gridDim.x, lane, cta);
+    if (warp == 0) build_plan(pl, p, gridDim.x, lane, cta, TP);
     __syncthreads();
 
     // sequences with nothing to attend produce zeros (the empty sum)
@@ -534,12 +587,22 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
             const int k = claimed;
             claimed = -1;
             if (k >= pl.n_dyn) break;
-            const int b = upper_seq(pl.dpref, B, k);
-            const int rel = k - pl.dpref[b];
-            const int kvh = rel / pl.dn[b];
-            const int c = rel - kvh * pl.dn[b];
-            const int p0 = pl.lo[b] + pl.sn[b] + c * pl.c_dyn;
-            ok = emit_piece(b, kvh, p0, p0 + pl.c_dyn, p.dyn_slot_base + k, true);
+            // chunk k: long chunks first, then the short ones; a segment's tail is its
+            // long chunks followed by its short ones
+            const bool is_long = k < pl.n_dyn0;
+            const int kk = is_long ? k : k - pl.n_dyn0;
+            const int* pref = is_long ? pl.dpref : pl.dpref1;
+            const int b = upper_seq(pref, B, kk);
+            const int per = is_long ? pl.dn[b] : pl.dn1[b];
+            const int rel = kk - pref[b];
+            const int kvh = rel / per;
+            const int idx = rel - kvh * per;
+            const int len = is_long ? pl.c_dyn : pl.c_dyn1;
+            const int local = is_long ? idx : pl.dn[b] + idx;
+            const int p0 = pl.lo[b] + pl.sn[b] + (is_long ? 0 : pl.dn[b] * pl.c_dyn) + idx * len;
+            const int slot = p.dyn_slot_base + pl.dpref[b] + pl.dpref1[b] +
+                             kvh * (pl.dn[b] + pl.dn1[b]) + local;
+            ok = emit_piece(b, kvh, p0, p0 + len, slot, true);
         }
         if (ok) {
             // end-of-work descriptor (a plain arrival, no bytes)

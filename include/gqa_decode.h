@@ -170,11 +170,11 @@ gqa_status_t gqa_device_status(void *workspace, uint32_t *flags, gqa_stream_t st
  * needs more scratch than the array holds.  The need is at least
  *   (grid + B*KVH) * g * (D + 2) * 4 bytes plus about 16*B*KVH + 1 KB,
  * where grid = the device's SM count; what is left holds partials of up to
- * min(6*grid, 1024) dynamically scheduled chunks, the slots gqa_decode always
+ * min(8*grid, 2048) dynamically scheduled chunks, the slots gqa_decode always
  * has.  Fewer slots leave the result unchanged up to rounding but balance the
  * load across SMs less well.  On a 152-SM GB300 the array covers every
- * slidingDecodeGQA call (B <= 256, all slots) and decodeGQA calls with
- * B <= 216 (all slots for B <= 1, about 740 of 912 at B = 32).
+ * slidingDecodeGQA call (B <= 256, all 1216 slots) and decodeGQA calls with
+ * B <= 216 (about 860 of the 1216 slots at B = 1, 740 at B = 32).
  *
  * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
  * routine.  It does the following:
