@@ -183,8 +183,14 @@ struct alignas(1024) KernelSmem {
     alignas(8) uint64_t full[Pol::STAGES];
     alignas(8) uint64_t empty[Pol::STAGES];
     TileDesc desc[Pol::STAGES];
+    alignas(8) uint64_t q_empty[2];           // q buffer free (consumer warps arrive)
     PlanSmem plan;
-    alignas(16) float acc[Pol::G][Pol::D];    // merged partial of the current piece
+    // q of the next pieces (bf16, [G][D]), copied in by the producer with the
+    // first tile of each piece; double-buffered over pieces
+    alignas(128) __nv_bfloat16 q[2][Pol::G * Pol::D];
+    // merged partial of the current piece (policies that merge their warps' results
+    // through shared memory; the others store straight from registers)
+    alignas(16) float acc[Pol::kDirectEpilogue ? 1 : Pol::G][Pol::kDirectEpilogue ? 4 : Pol::D];
     float m[Pol::G];
     float l[Pol::G];
     alignas(16) typename Pol::Scratch scratch;
@@ -223,6 +229,15 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, flo
         static_cast<float*>(p.out)[idx] = x;
     else
         static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(x);
+}
+
+// Two consecutive outputs starting at idx (a multiple of 2).
+__device__ __forceinline__ void store_out2(const DecodeParams& p, size_t idx, float x, float y) {
+    if (p.out_f32)
+        *reinterpret_cast<float2*>(static_cast<float*>(p.out) + idx) = make_float2(x, y);
+    else
+        *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + idx) =
+            __floats2bfloat162_rn(x, y);
 }
 
 // Four consecutive outputs starting at idx (a multiple of 4).
@@ -460,6 +475,8 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
             ptx::mbar_init(ptx::smem_addr(&sm.full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&sm.empty[s]), NC);
         }
+        ptx::mbar_init(ptx::smem_addr(&sm.q_empty[0]), NC);
+        ptx::mbar_init(ptx::smem_addr(&sm.q_empty[1]), NC);
         ptx::fence_mbar_init();
         sm.abort_flag = 0;
     }
@@ -514,6 +531,8 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
         // overlaps the wait for a free stage.
         const bool dynamic = pl.n_dyn > 0;
         int claimed = -1;   // result of the claim in flight, -1 when none
+        uint32_t q_n = 0;   // pieces started (q buffer q_n & 1)
+        constexpr uint32_t kQBytes = G * D * 2;
 
         // Streams the tiles of positions [p0, p1) of segment (b, kvh); returns false on abort.
         auto emit_piece = [&](int b, int kvh, int p0, int p1, int slot, bool unit_end) -> bool {
@@ -521,6 +540,13 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
             const int chunk0 = kvh * kChunksPerRow;
             const int32_t* bt_row =
                 kPaged ? p.block_table + static_cast<size_t>(b) * p.max_pages : nullptr;
+            // the piece's q goes to buffer q_n & 1 once the consumers are done with
+            // the q the buffer held two pieces ago
+            const uint32_t qb = q_n & 1u;
+            if (!wait_bounded(ptx::smem_addr(&sm.q_empty[qb]), ((q_n >> 1) & 1u) ^ 1u,
+                              &sm.abort_flag, p.ws_flags))
+                return false;
+            ++q_n;
             for (int t = t_first; t < p1; t += TP) {
                 if (dynamic && unit_end && t + TP >= p1)
                     claimed = static_cast<int>(atomicAdd(p.ws_claim, 1u));
@@ -529,6 +555,7 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
                 if (!wait_bounded(ptx::smem_addr(&sm.empty[s]), ph ^ 1u, &sm.abort_flag,
                                   p.ws_flags))
                     return false;
+                const bool first = (t == t_first);
                 TileDesc& d = sm.desc[s];
                 d.b = b;
                 d.kvh = kvh;
@@ -536,12 +563,17 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
                 d.vlo = (p0 > t ? p0 : t) - t;
                 d.vhi = (p1 < t + TP ? p1 : t + TP) - t;
                 d.slot = slot;
-                d.flags = (t == t_first ? kDescFirst : 0) | (t + TP >= p1 ? kDescLast : 0);
+                d.flags = (first ? kDescFirst : 0) | (t + TP >= p1 ? kDescLast : 0);
                 int nbox = 0;
 #pragma unroll
                 for (int j = 0; j < kBoxesPerTile; ++j) nbox += (t + j * kBoxRows < p1) ? 1 : 0;
                 const uint32_t full_bar = ptx::smem_addr(&sm.full[s]);
-                ptx::mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(nbox) * 2u * kBoxBytes);
+                ptx::mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(nbox) * 2u * kBoxBytes +
+                                                         (first ? kQBytes : 0u));
+                if (first)
+                    ptx::bulk_copy_g2s(ptx::smem_addr(&sm.q[qb][0]),
+                                       p.q + (static_cast<size_t>(b) * H + kvh * G) * D, kQBytes,
+                                       full_bar);
                 const uint32_t k_dst = kv_base + s * kStageBytes;
                 const uint32_t v_dst = k_dst + KernelSmem<Pol>::kTileBytes;
                 for (int j = 0; j < nbox; ++j) {
@@ -624,6 +656,7 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
     // ===================== consumers: follow the descriptors =====================
     typename Pol::State st;
     uint32_t t_idx = 0;
+    uint32_t q_n = 0;   // pieces started (q buffer q_n & 1)
     bool bad = false;
     const float nan = __uint_as_float(0x7fc00000u);
     while (true) {
@@ -635,7 +668,12 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
         const TileDesc d = sm.desc[s];
         if (d.flags & kDescDone) break;
         if (d.flags & kDescFirst) {
-            Pol::begin(st, p.q + (static_cast<size_t>(d.b) * H + d.kvh * G) * D, warp, lane);
+            // q arrived with this tile; release the buffer once every lane has read it
+            const uint32_t qb = q_n & 1u;
+            Pol::begin(st, &sm.q[qb][0], warp, lane);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.q_empty[qb]));
+            ++q_n;
             bad = false;
         }
         if (kPaged) {
@@ -654,34 +692,42 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
         if (!(d.flags & kDescLast)) continue;
 
         // ---------------- epilogue of a partial ----------------
-        // merged (m, l, acc) of this piece -> sm.m, sm.l, sm.acc (ends with a consumer barrier)
-        Pol::end(st, &sm.acc[0][0], sm.m, sm.l, sm.scratch, warp, lane);
         if (bad && tid == 0) atomicOr(p.ws_flags, kFlagBadPage);
         const SegmentParts sp(pl, d.b, d.kvh, p.dyn_slot_base);
         const int nparts = sp.count();
         const size_t out_base = (static_cast<size_t>(d.b) * H + d.kvh * G) * D;
-        const float4* acc4 = reinterpret_cast<const float4*>(&sm.acc[0][0]);
-        const float4 nan4 = make_float4(nan, nan, nan, nan);
-        if (nparts == 1) {
-            for (int i4 = tid; i4 < G * D / 4; i4 += kConsumerThreads) {
-                const float inv = 1.0f / sm.l[(i4 * 4) / D];
-                const float4 a = acc4[i4];
-                store_out4(p, out_base + static_cast<size_t>(i4) * 4,
-                           bad ? nan4 : make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
-            }
+        if constexpr (Pol::kDirectEpilogue) {
+            // each warp stores its own share of the result from registers: the
+            // output when the piece is the whole segment, else the partial (the
+            // combine kernel merges the partials after this grid completes)
+            Pol::store(st, p, out_base, nparts == 1 ? -1 : d.slot, bad, warp, lane);
         } else {
-            // the combine kernel merges the partials after this grid completes
-            const size_t slot = static_cast<size_t>(d.slot);
-            float4* wacc4 = reinterpret_cast<float4*>(p.ws_acc + slot * G * D);
-            for (int i4 = tid; i4 < G * D / 4; i4 += kConsumerThreads)
-                wacc4[i4] = bad ? nan4 : acc4[i4];
-            if (tid < G) {
-                p.ws_ml[(slot * G + tid) * 2 + 0] = bad ? 0.0f : sm.m[tid];
-                p.ws_ml[(slot * G + tid) * 2 + 1] = bad ? nan : sm.l[tid];
+            // merged (m, l, acc) of this piece -> sm.m, sm.l, sm.acc (ends with a
+            // consumer barrier)
+            Pol::end(st, &sm.acc[0][0], sm.m, sm.l, sm.scratch, warp, lane);
+            const float4* acc4 = reinterpret_cast<const float4*>(&sm.acc[0][0]);
+            const float4 nan4 = make_float4(nan, nan, nan, nan);
+            if (nparts == 1) {
+                for (int i4 = tid; i4 < G * D / 4; i4 += kConsumerThreads) {
+                    const float inv = 1.0f / sm.l[(i4 * 4) / D];
+                    const float4 a = acc4[i4];
+                    store_out4(p, out_base + static_cast<size_t>(i4) * 4,
+                               bad ? nan4 : make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
+                }
+            } else {
+                // the combine kernel merges the partials after this grid completes
+                const size_t slot = static_cast<size_t>(d.slot);
+                float4* wacc4 = reinterpret_cast<float4*>(p.ws_acc + slot * G * D);
+                for (int i4 = tid; i4 < G * D / 4; i4 += kConsumerThreads)
+                    wacc4[i4] = bad ? nan4 : acc4[i4];
+                if (tid < G) {
+                    p.ws_ml[(slot * G + tid) * 2 + 0] = bad ? 0.0f : sm.m[tid];
+                    p.ws_ml[(slot * G + tid) * 2 + 1] = bad ? nan : sm.l[tid];
+                }
             }
+            // sm.acc is reused by the next piece
+            ptx::named_barrier_sync(1, kConsumerThreads);
         }
-        // sm.acc is reused by the next piece
-        ptx::named_barrier_sync(1, kConsumerThreads);
     }
 }
 

@@ -40,6 +40,9 @@ struct MmaPolicy {
     static constexpr int kSStride = 40;             // padded row of the score tile
     static constexpr bool kSwizzle128 = true;       // ldmatrix needs the 128-byte swizzle
     static constexpr int kBoxRows = 16;             // TMA box height on a contiguous cache
+    // every warp holds the full running max/normaliser and its own slice of the
+    // output, so results are stored straight from registers
+    static constexpr bool kDirectEpilogue = true;
 
     struct Scratch {
         alignas(16) float S[2][2][G][kSStride];   // [tile parity][half of D][head][position]
@@ -56,12 +59,13 @@ struct MmaPolicy {
                                                  int lane) {
         const int gid = lane >> 2, t4 = lane & 3;
         const bool real = gid < G;   // rows G..7 of A are zero
+        // q_heads: the g query heads of the KV head, [G][D] bf16 in shared memory
         const uint32_t* qrow =
             reinterpret_cast<const uint32_t*>(q_heads + (real ? gid : 0) * D + (warp >> 2) * (D / 2));
 #pragma unroll
         for (int kk = 0; kk < kKSteps; ++kk) {
-            st.qa[kk][0] = real ? __ldg(qrow + (kk * 16 + 2 * t4) / 2) : 0u;
-            st.qa[kk][1] = real ? __ldg(qrow + (kk * 16 + 8 + 2 * t4) / 2) : 0u;
+            st.qa[kk][0] = real ? qrow[(kk * 16 + 2 * t4) / 2] : 0u;
+            st.qa[kk][1] = real ? qrow[(kk * 16 + 8 + 2 * t4) / 2] : 0u;
         }
 #pragma unroll
         for (int n = 0; n < kNTiles; ++n)
@@ -193,6 +197,44 @@ struct MmaPolicy {
                 ptx::mma_bf16_16816(st.acc[2 * jj], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b0, b1);
                 ptx::mma_bf16_16816(st.acc[2 * jj + 1], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b2,
                                     b3);
+            }
+        }
+    }
+
+    // The piece's result for head gid, dims [warp D/8, +D/8) of this warp: the
+    // normalised output (slot < 0; the piece is the whole segment) or the partial
+    // (acc, m, l) at workspace slot `slot`.  A bad page turns it into NaN.
+    __device__ static __forceinline__ void store(const State& st, const DecodeParams& p,
+                                                 size_t out_base, int slot, bool bad, int warp,
+                                                 int lane) {
+        const int gid = lane >> 2, t4 = lane & 3;
+        float l = st.l;
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        if (gid >= G) return;
+        const float nan = __uint_as_float(0x7fc00000u);
+        if (slot < 0) {
+            const float inv = 1.0f / l;
+#pragma unroll
+            for (int n = 0; n < kNTiles; ++n) {
+                const int d = warp * kDSlice + n * 8 + 2 * t4;
+                const float x = (st.acc[n][0] + st.acc[n][2]) * inv;
+                const float y = (st.acc[n][1] + st.acc[n][3]) * inv;
+                store_out2(p, out_base + gid * D + d, bad ? nan : x, bad ? nan : y);
+            }
+        } else {
+            float* wacc = p.ws_acc + static_cast<size_t>(slot) * G * D + gid * D;
+#pragma unroll
+            for (int n = 0; n < kNTiles; ++n) {
+                const int d = warp * kDSlice + n * 8 + 2 * t4;
+                *reinterpret_cast<float2*>(wacc + d) =
+                    bad ? make_float2(nan, nan)
+                        : make_float2(st.acc[n][0] + st.acc[n][2], st.acc[n][1] + st.acc[n][3]);
+            }
+            if (warp == 0 && t4 == 0) {
+                float* ml = p.ws_ml + (static_cast<size_t>(slot) * G + gid) * 2;
+                ml[0] = bad ? 0.0f : st.m;
+                ml[1] = bad ? nan : l;
             }
         }
     }

@@ -93,6 +93,17 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Contiguous bulk copy global -> shared (both 16-byte aligned, bytes a multiple
+// of 16), completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // ---- barriers among a subset of warps -----------------------------------------
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
