@@ -25,6 +25,7 @@ from ._native import (  # noqa: F401
     gqa_decode,
     gqa_decode_noalloc,
     gqa_decode_paged,
+    gqa_check_inputs_host,
     gqa_device_status,
     gqa_status_string,
     gqa_workspace_init,

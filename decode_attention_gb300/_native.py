@@ -32,7 +32,8 @@ GQA_DEVICE_BAD_LENGTH = 4
 PAGE_SIZE = 16
 
 EXPORTED_SYMBOLS = ("gqa_workspace_size", "gqa_workspace_init", "gqa_decode", "gqa_decode_paged",
-                    "gqa_device_status", "gqa_decode_noalloc", "gqa_status_string")
+                    "gqa_device_status", "gqa_decode_noalloc", "gqa_check_inputs_host",
+                    "gqa_status_string")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +76,8 @@ def load_library(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.gqa_decode_noalloc.restype = ci
         lib.gqa_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gqa_device_status.restype = ci
+        lib.gqa_check_inputs_host.argtypes = [vp, ci, ci, ci, vp, ci, ci, ctypes.POINTER(ci)]
+        lib.gqa_check_inputs_host.restype = ci
         lib.gqa_status_string.argtypes = [ci]
         lib.gqa_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -214,6 +217,24 @@ def gqa_decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_le
         _out_code(out), _stream_handle(stream, q.device))
     _check("gqa_decode_noalloc", st)
     return out
+
+
+def gqa_check_inputs_host(seq_lens, capacity: int, window: int, block_table=None,
+                          num_pages: int = 0) -> int:
+    """Check host copies of seq_lens (and the block table): returns -1 when every
+    sequence is valid, else the index of the first bad one (length outside
+    [0, capacity], or an attended page outside [0, num_pages))."""
+    import numpy as np
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    bt = None if block_table is None else np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    max_pages = 0 if bt is None else int(bt.shape[1])
+    first = ctypes.c_int(-1)
+    st = load_library().gqa_check_inputs_host(
+        lens.ctypes.data if lens.size else None, int(lens.shape[0]), int(capacity), int(window),
+        None if bt is None else bt.ctypes.data, max_pages, int(num_pages), ctypes.byref(first))
+    if st not in (GQA_OK, GQA_ERR_INVALID_ARGUMENT) or (st != GQA_OK and first.value < 0):
+        raise GQAError("gqa_check_inputs_host", st)
+    return first.value
 
 
 def gqa_device_status(workspace: torch.Tensor | None = None, stream=None) -> int:

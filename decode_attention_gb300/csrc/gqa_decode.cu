@@ -280,6 +280,30 @@ gqa_status_t gqa_device_status(void* workspace, uint32_t* flags, gqa_stream_t st
     return GQA_OK;
 }
 
+gqa_status_t gqa_check_inputs_host(const int32_t* seq_lens, int B, int capacity, int window,
+                                   const int32_t* block_table, int max_pages, int P,
+                                   int* first_bad) {
+    if (first_bad) *first_bad = -1;
+    if (B < 0 || B > GQA_MAX_BATCH || capacity < 1 || window < 0 || (B > 0 && !seq_lens))
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (block_table && (max_pages < 1 || P < 1)) return GQA_ERR_INVALID_ARGUMENT;
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b];
+        bool bad = L < 0 || L > capacity;
+        if (!bad && block_table && L > 0) {
+            const int lo = (window > 0 && L > window) ? L - window : 0;
+            const int32_t* row = block_table + static_cast<size_t>(b) * max_pages;
+            for (int pg = lo / GQA_PAGE_SIZE; pg <= (L - 1) / GQA_PAGE_SIZE && !bad; ++pg)
+                bad = pg >= max_pages || row[pg] < 0 || row[pg] >= P;
+        }
+        if (bad) {
+            if (first_bad) *first_bad = b;
+            return GQA_ERR_INVALID_ARGUMENT;
+        }
+    }
+    return GQA_OK;
+}
+
 const char* gqa_status_string(gqa_status_t status) {
     switch (status) {
         case GQA_OK: return "GQA_OK";

@@ -195,6 +195,32 @@ gqa_status_t gqa_decode_noalloc(const void *q, const void *k, const void *v,
                                 int window, void *out, gqa_out_dtype_t out_dtype,
                                 gqa_stream_t stream);
 
+/*
+ * Host-side check of the device-resident inputs, for tests and debugging: the
+ * caller copies seq_lens (and the block table) to host memory and passes them
+ * here.  The decode calls never read these arrays on the host (they stay on the
+ * device and the kernel clamps a bad length and turns a bad page into NaN
+ * output, raising a GQA_DEVICE_* bit); this reports the same conditions
+ * synchronously.
+ *
+ *   seq_lens     host int32 [B]
+ *   capacity     S for a contiguous cache, 16 * max_pages for a paged one
+ *   window       0 = full history, > 0 = last `window` positions
+ *   block_table  host int32 [B, max_pages], or NULL for a contiguous cache
+ *   P            pages in the pool (paged only)
+ *   first_bad    optional: index b of the first bad sequence, or -1
+ *
+ * A sequence is bad when its length lies outside [0, capacity], or (paged)
+ * when a page covering one of its attended positions [lo, L) lies outside
+ * [0, P).  Entries past the last attended page are not looked at.  Returns
+ * GQA_OK when no sequence is bad, GQA_ERR_INVALID_ARGUMENT otherwise or for bad
+ * sizes (B outside [0, GQA_MAX_BATCH], capacity < 1, window < 0, NULL seq_lens
+ * with B > 0, max_pages or P < 1 on a paged check).
+ */
+gqa_status_t gqa_check_inputs_host(const int32_t *seq_lens, int B, int capacity, int window,
+                                   const int32_t *block_table, int max_pages, int P,
+                                   int *first_bad);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *gqa_status_string(gqa_status_t status);
 

@@ -130,3 +130,57 @@ def test_python_binding_validates_before_calling():
     lens = torch.zeros(2, dtype=torch.int32)
     with pytest.raises(ValueError):     # CPU tensors are refused, no fallback
         gqa.gqa_decode(q, k, k, lens, 1024)
+
+
+def test_check_inputs_host_lengths():
+    # contiguous cache: lengths must lie in [0, capacity]
+    assert gqa.gqa_check_inputs_host([0, 1, 64], capacity=64, window=0) == -1
+    assert gqa.gqa_check_inputs_host([3, 65, 1], capacity=64, window=0) == 1
+    assert gqa.gqa_check_inputs_host([-1], capacity=64, window=16) == 0
+    assert gqa.gqa_check_inputs_host([], capacity=64, window=0) == -1
+
+
+def test_check_inputs_host_pages_only_attended():
+    # paged: only the pages covering [lo, L) must be valid; later entries (-1 in
+    # inputs.page_table) and pages before a sliding window are not looked at
+    P = 10
+    bt = [[0, 1, 2, -1, -1],
+          [-7, 9, 3, 4, -1]]          # page 0 of sequence 1 is bad but lies before its window
+    assert gqa.gqa_check_inputs_host([40, 64], capacity=80, window=40, block_table=bt,
+                                     num_pages=P) == -1
+    # the same table with full history: sequence 1 attends page 0 -> bad
+    assert gqa.gqa_check_inputs_host([40, 64], capacity=80, window=0, block_table=bt,
+                                     num_pages=P) == 1
+    # a page id equal to P is out of range
+    assert gqa.gqa_check_inputs_host([17], capacity=80, window=0, block_table=[[0, P, 0, 0, 0]],
+                                     num_pages=P) == 0
+    # L = 48 covers pages 0..2 exactly; entry 3 = -1 is not attended
+    assert gqa.gqa_check_inputs_host([48], capacity=80, window=0, block_table=[[5, 6, 7, -1, -1]],
+                                     num_pages=P) == -1
+
+
+def test_check_inputs_host_matches_generated_tables():
+    import numpy as np
+    from decode_attention_gb300 import inputs
+    wl = inputs.WORKLOADS["paged_mixed_b256"]
+    lens = wl.lengths(np.random.default_rng(wl.seed))
+    table, P = inputs.page_table(lens, wl.seed, max_pages=(wl.S + 15) // 16)
+    for window in (0, 1024):
+        assert gqa.gqa_check_inputs_host(lens, wl.S, window, table, P) == -1
+    # one attended page out of range is found
+    bad = table.copy()
+    b = int(np.argmax(lens))
+    bad[b, (int(lens[b]) - 1) // 16] = P
+    assert gqa.gqa_check_inputs_host(lens, wl.S, 0, bad, P) == b
+
+
+def test_check_inputs_host_rejects_bad_sizes(lib):
+    first = ctypes.c_int(5)
+    assert lib.gqa_check_inputs_host(None, 2, 64, 0, None, 0, 0, ctypes.byref(first)) == \
+        gqa.GQA_ERR_INVALID_ARGUMENT
+    assert first.value == -1
+    lens = (ctypes.c_int32 * 1)(4)
+    assert lib.gqa_check_inputs_host(lens, 1, 0, 0, None, 0, 0, None) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert lib.gqa_check_inputs_host(lens, 1, 64, -1, None, 0, 0, None) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert lib.gqa_check_inputs_host(lens, 1, 64, 0, lens, 0, 3, None) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert lib.gqa_check_inputs_host(lens, 1, 64, 0, None, 0, 0, None) == gqa.GQA_OK
