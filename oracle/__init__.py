@@ -52,6 +52,9 @@ def _bind(path: str):
     lib.oracle_gqa_decode_paged_f64.argtypes = [u16p, u16p, u16p, i32p, i32p, ci, ci, ci,
                                                 ci, ci, ci, ci, ci, ci, f64p]
     lib.oracle_gqa_decode_paged_f64.restype = ci
+    lib.oracle_gqa_decode_ring_f64.argtypes = [u16p, u16p, u16p, i32p, ci, ci, ci, ci, ci, ci,
+                                               ci, f64p]
+    lib.oracle_gqa_decode_ring_f64.restype = ci
     lib.oracle_default_threads.argtypes = []
     lib.oracle_default_threads.restype = ci
     return lib
@@ -138,6 +141,33 @@ def gqa_decode_paged_f64(q: np.ndarray, k_pages: np.ndarray, v_pages: np.ndarray
     return out
 
 
+def gqa_decode_ring_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, seq_lens, window: int,
+                        nthreads: int = 0, _lib_override=None) -> np.ndarray:
+    """Decode attention over a window-capped ring-buffer cache, exact up to fp64 rounding.
+
+    k, v: uint16 [B, C, KVH, D]; position s of sequence b is row s % C.  The
+    attended positions are [max(0, L - window), L) with 1 <= window <= C, so all of
+    them are still in the ring; L may exceed C.
+    """
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, H, D = q.shape
+    Bk, C, KVH, Dk = k.shape
+    if k.shape != v.shape or Bk != B or Dk != D:
+        raise ValueError("shape mismatch between q, k and v")
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError("seq_lens must have shape [B]")
+    out = np.zeros((B, H, D), dtype=np.float64)
+    lib = _lib_override if _lib_override is not None else _load()
+    rc = lib.oracle_gqa_decode_ring_f64(
+        _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
+        _ptr(lens, ctypes.c_int32), B, C, H, KVH, D, int(window), int(nthreads),
+        _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out
+
+
 class OracleLibrary:
     """The oracle API bound to a specific compiled copy of the C source.
 
@@ -153,6 +183,9 @@ class OracleLibrary:
 
     def gqa_decode_paged_f64(self, *args, **kw):
         return gqa_decode_paged_f64(*args, _lib_override=self._lib, **kw)
+
+    def gqa_decode_ring_f64(self, *args, **kw):
+        return gqa_decode_ring_f64(*args, _lib_override=self._lib, **kw)
 
 
 def compile_variant(source_text: str, out_path: str) -> str:

@@ -315,3 +315,91 @@ int oracle_default_threads(void)
     return 1;
 #endif
 }
+
+/* ---- window-capped (ring-buffer) cache: k, v are [B, C, KVH, D]; position s of
+ *      sequence b lives at row s mod C ("Retrofit Plan: Gemma 4 31B IT ->
+ *      Progressive Multi-Scale SWA with Block Attention Residuals", §3.3 and
+ *      §7.3: each sliding layer keeps its own cache, capped at its window) ---- */
+typedef struct {
+    const uint16_t *k, *v;
+    int64_t b, kvh, lo, C;
+    int KVH, D;
+} ring_ctx;
+
+static const uint16_t *ring_row(const uint16_t *t, const ring_ctx *x, int64_t j)
+{
+    const int64_t s = x->lo + j;    /* absolute position */
+    const int64_t row = s % x->C;   /* its slot in the ring */
+    return t + ((x->b * x->C + row) * x->KVH + x->kvh) * x->D;
+}
+static const uint16_t *ring_k(const void *c, int64_t j)
+{
+    return ring_row(((const ring_ctx *)c)->k, (const ring_ctx *)c, j);
+}
+static const uint16_t *ring_v(const void *c, int64_t j)
+{
+    return ring_row(((const ring_ctx *)c)->v, (const ring_ctx *)c, j);
+}
+
+/*
+ * Ring-buffer variant.  The attended range is the same as above, positions
+ * [max(0, L_b - window), L_b); all of them are still held when 1 <= window <= C
+ * (each of the last C positions has its own slot), which this function
+ * requires.  L_b itself may exceed C.
+ * k, v: [B, C, KVH, D] bf16 bits.
+ */
+int oracle_gqa_decode_ring_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                               const int32_t *seq_lens, int B, int C, int H, int KVH, int D,
+                               int window, int nthreads, double *out)
+{
+    int b;
+    if (B < 0 || C <= 0 || H <= 0 || KVH <= 0 || D <= 0 || window < 1 || window > C)
+        return ORACLE_EINVAL;
+    if (H % KVH != 0) return ORACLE_EINVAL;
+    int64_t max_n = 1;
+    for (b = 0; b < B; ++b) {
+        int64_t lo, hi;
+        if (seq_lens[b] < 0) return ORACLE_EINVAL;
+        attended_range(seq_lens[b], window, &lo, &hi);
+        if (hi - lo > max_n) max_n = hi - lo;
+    }
+    const int g = H / KVH;
+    const int64_t pairs = (int64_t)B * H;
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#endif
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)max_n);
+        double *q_row = (double *)malloc(sizeof(double) * (size_t)D);
+        const int have_scratch = scores != NULL && q_row != NULL;
+        int64_t p;
+        /* every thread reaches the work-sharing loop (it ends in a barrier) */
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (p = 0; p < pairs; ++p) {
+            if (!have_scratch) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+                err = ORACLE_ENOMEM;
+                continue;
+            }
+            {
+                const int64_t bb = p / H, h = p % H;
+                int64_t lo, hi;
+                int d;
+                attended_range(seq_lens[bb], window, &lo, &hi);
+                for (d = 0; d < D; ++d) q_row[d] = bf16_bits_to_double(q[(bb * H + h) * D + d]);
+                ring_ctx c = {k, v, bb, h / g, lo, C, KVH, D};
+                attend(q_row, D, hi - lo, ring_k, ring_v, &c, scores, out + (bb * H + h) * D);
+            }
+        }
+        free(scores);
+        free(q_row);
+    }
+    (void)nthreads;
+    return err;
+}

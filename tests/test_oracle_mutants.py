@@ -59,6 +59,15 @@ MUTANTS = {
     "query_transposed": (
         "q_row[d] = bf16_bits_to_double(q[(bb * H + h) * D + d]);\n                contig_ctx",
         "q_row[d] = bf16_bits_to_double(q[(d % H) * D + (bb * H + h) % D]);\n                contig_ctx"),
+    "ring_row_shifted": (
+        "const int64_t row = s % x->C;",
+        "const int64_t row = (s + 1) % x->C;"),
+    "ring_head_map_modulo": (
+        "ring_ctx c = {k, v, bb, h / g,",
+        "ring_ctx c = {k, v, bb, h % KVH,"),
+    "ring_window_start_late": (
+        "attend(q_row, D, hi - lo, ring_k",
+        "attend(q_row, D, hi - lo - (hi - lo > 1), ring_k"),
     "empty_range_not_zero": (
         "if (n <= 0) return; /* empty sum */",
         "if (n <= 0) { for (d = 0; d < D; ++d) out[d] = 1.0; return; }"),

@@ -369,6 +369,63 @@ def test_paged_bad_page_id_gives_nan_for_that_sequence(oracle_lib):
     assert np.all(np.isfinite(out2))
 
 
+# ---------------------------------------------------------------------------
+# window-capped ring-buffer cache ("Retrofit Plan: Gemma 4 31B IT -> Progressive
+# Multi-Scale SWA with Block Attention Residuals", §3.3 and §7.3): position s at
+# row s mod C
+# ---------------------------------------------------------------------------
+
+def ring_copy(t, lens, C, keep):
+    """Ring of C rows per sequence holding positions [L - keep, L) of the
+    contiguous tensor t at rows s mod C; every other row is bf16 NaN."""
+    B, S, KVH, D = t.shape
+    r = np.full((B, C, KVH, D), 0x7FC0, np.uint16)
+    for b, L in enumerate(lens):
+        for s in range(max(0, L - keep), L):
+            r[b, s % C] = t[b, s]
+    return r
+
+
+@pytest.mark.parametrize("C,W", [(16, 16), (24, 16), (16, 5), (7, 7)])
+def test_ring_equals_contiguous_on_a_wrapped_copy(oracle_lib, C, W):
+    """A ring holding the same rows at s mod C gives the identical result, with NaN in
+    every row outside the window: lengths below, at and across multiples of C."""
+    lens = [1, W - 1 if W > 1 else 1, W, C, C + 1, 2 * C + 3, 3 * C, 5 * C - 1]
+    S = max(lens)
+    H, KVH, D = 8, 2, 16
+    q, k, v = random_case(len(lens), S, H, KVH, D, seed=17 + C + W)
+    rk, rv = ring_copy(k, lens, C, W), ring_copy(v, lens, C, W)
+    ring = oracle_lib.gqa_decode_ring_f64(q, rk, rv, lens, W)
+    contig = oracle_lib.gqa_decode_f64(q, k, v, lens, W)
+    assert np.array_equal(ring, contig)
+
+
+@pytest.mark.parametrize("H,KVH", [(32, 16), (32, 4)])
+def test_ring_torch_sdpa_float64(oracle_lib, H, KVH):
+    """SDPA in float64 on the rows a ring holds for the window, gathered by
+    position (row s mod C), against random ring contents."""
+    B, C, D, W = 3, 12, 16, 9
+    q, rk, rv = random_case(B, C, H, KVH, D, seed=18)
+    lens = [5, 12, 31]
+    out = oracle_lib.gqa_decode_ring_f64(q, rk, rv, lens, W)
+    g = H // KVH
+    for b, L in enumerate(lens):
+        lo, hi = window_range(L, W)
+        rows = [s % C for s in range(lo, hi)]
+        qt = torch.from_numpy(to_vals(q[b]))[:, None, :]                             # [H, 1, D]
+        kt = torch.from_numpy(to_vals(rk[b, rows])).permute(1, 0, 2).repeat_interleave(g, dim=0)
+        vt = torch.from_numpy(to_vals(rv[b, rows])).permute(1, 0, 2).repeat_interleave(g, dim=0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=1.0)
+        np.testing.assert_allclose(out[b], ref[:, 0, :].numpy(), rtol=1e-11, atol=1e-13)
+
+
+def test_ring_rejects_windows_it_cannot_hold(oracle_lib):
+    q, k, v = random_case(1, 8, 4, 2, 8, seed=19)
+    for W in (0, 9):
+        with pytest.raises(ValueError):
+            oracle_lib.gqa_decode_ring_f64(q, k, v, [20], W)
+
+
 def test_oracle_rejects_ranges_outside_the_cache(oracle_lib):
     q, k, v = random_case(1, 8, 4, 2, 8, seed=16)
     with pytest.raises(ValueError):
