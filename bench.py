@@ -113,8 +113,10 @@ class Call:
     """One library call of a step, with its inputs resident on the device."""
 
     def __init__(self, layer: str, geo: dict, case: dict, paged: bool, seq_lens: np.ndarray,
-                 device="cuda"):
+                 device="cuda", ring: int = 0):
         self.layer, self.geo, self.case, self.paged = layer, geo, case, paged
+        self.ring = ring   # > 0: window-capped ring cache of `ring` rows
+        self.name = f"{layer}_ring{ring}" if ring else layer
         self.seq_lens = seq_lens
         self.bytes = kv_bytes(seq_lens, geo)
         self.times_ms = []
@@ -131,6 +133,8 @@ class Call:
         if self.paged:
             gqa.gqa_decode_paged(q, c["k_pages"], c["v_pages"], c["block_table"], lens,
                                  self.geo["window"], out=self.out)
+        elif self.ring:
+            gqa.gqa_decode_ring(q, c["k"], c["v"], lens, self.geo["window"], out=self.out)
         else:
             gqa.gqa_decode(q, c["k"], c["v"], lens, self.geo["window"], out=self.out)
 
@@ -145,6 +149,12 @@ def build_calls(wl: inputs.Workload, seed: int, device="cuda"):
             case = inputs.paged_case(wl.B, geo["H"], geo["KVH"], geo["D"], lens, seed + 100 * i,
                                      device=device, table=table)
             calls.append(Call(layer, geo, case, True, lens, device))
+    elif wl.rings:
+        for i, window in enumerate(wl.rings):
+            geo = dict(inputs.geometry(wl.layers[0]), window=window)
+            case = inputs.contiguous_case(wl.B, window, geo["H"], geo["KVH"], geo["D"], lens,
+                                          seed + 100 * i, device=device)
+            calls.append(Call(wl.layers[0], geo, case, False, lens, device, ring=window))
     else:
         layer = wl.layers[0]
         geo = inputs.geometry(layer)
@@ -263,11 +273,14 @@ def recorded_traffic(workload: str, layer: str):
 # ---------------------------------------------------------------------------
 
 def host_slices(call: Call, b: int):
-    """uint16 host copies of the attended rows of sequence b (and pos_base)."""
+    """uint16 host copies of the attended rows of sequence b (and pos_base); for a
+    ring cache, the sequence's whole ring (it holds exactly its window's rows)."""
     c, geo = call.case, call.geo
     L = int(call.seq_lens[b])
     lo = max(0, L - geo["window"]) if geo["window"] > 0 else 0
     qb = inputs.bf16_bits(c["q"][b:b + 1])
+    if call.ring:
+        return qb, inputs.bf16_bits(c["k"][b:b + 1]), inputs.bf16_bits(c["v"][b:b + 1]), L, 0
     if call.paged:
         pages = c["block_table"][b, lo // 16:(L + 15) // 16].long()
         k = c["k_pages"][pages].reshape(1, -1, geo["KVH"], geo["D"])
@@ -304,12 +317,20 @@ def oracle_sample(calls, budget_s: float, max_seqs: int | None = None):
     return items
 
 
-def run_oracle_items(items):
+def oracle_for(call: Call, slices):
+    """The fp64 oracle's output [H, D] for one sequence, from host_slices()."""
     import oracle
+    qb, kb, vb, L, base = slices
+    if call.ring:
+        return oracle.gqa_decode_ring_f64(qb, kb, vb, [L], call.geo["window"])[0]
+    return oracle.gqa_decode_f64(qb, kb, vb, [L], call.geo["window"], pos_base=base)[0]
+
+
+def run_oracle_items(items):
     t0 = time.perf_counter()
     nbytes = 0
-    for call, b, (qb, kb, vb, L, base), nb in items:
-        oracle.gqa_decode_f64(qb, kb, vb, [L], call.geo["window"], pos_base=base)
+    for call, b, slices, nb in items:
+        oracle_for(call, slices)
         nbytes += nb
     return nbytes, time.perf_counter() - t0
 
@@ -359,7 +380,11 @@ def run_reference(args, wl):
 
 
 def workload_config(wl, l2_note=None):
-    geo = [dict(layer=l, **{k: v for k, v in inputs.geometry(l).items()}) for l in wl.layers]
+    if wl.rings:
+        geo = [dict(layer=wl.layers[0], **dict(inputs.geometry(wl.layers[0]), window=w), ring=w)
+               for w in wl.rings]
+    else:
+        geo = [dict(layer=l, **{k: v for k, v in inputs.geometry(l).items()}) for l in wl.layers]
     cfg = {"workload": wl.name, "description": wl.description, "B": wl.B, "S": wl.S,
            "seed": wl.seed, "paged": wl.paged, "page_size": 16 if wl.paged else None,
            "geometry": geo}
@@ -414,7 +439,7 @@ def run_ours(args, wl):
     t_wall1 = time.time()
     for c in calls:
         c.times_ms = [a.elapsed_time(b) for a, b in events[id(c)]]
-        print(f"[bench] {c.layer} us per step: " + " ".join(f"{t * 1e3:.1f}" for t in c.times_ms),
+        print(f"[bench] {c.name} us per step: " + " ".join(f"{t * 1e3:.1f}" for t in c.times_ms),
               file=sys.stderr)
     barrier(world)
     time.sleep(0.1)
@@ -461,17 +486,19 @@ def run_ours(args, wl):
     dom_ms = statistics.mean(dom.times_ms)
     achieved = dom.bytes / (dom_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
-    roofline = {"bound": "hbm", "kernel": f"gqa_decode_kernel<{dom.layer}>",
+    roofline = {"bound": "hbm", "kernel": f"gqa_decode_kernel<{dom.name}>",
                 "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": recorded_traffic(wl.name, dom.layer),
                 "algorithmic_bytes_per_launch": dom.bytes}
 
-    us_per_layer = {c.layer: round(statistics.median(c.times_ms) * 1e3, 2) for c in calls}
-    if len(calls) == 2:
+    us_per_layer = {c.name: round(statistics.median(c.times_ms) * 1e3, 2) for c in calls}
+    if wl.rings:
+        us_per_layer["block_of_ring_calls"] = round(sum(us_per_layer[c.name] for c in calls), 2)
+    if len(calls) == 2 and {c.layer for c in calls} == {"sliding", "global"}:
         us_per_layer["weighted_50_sliding_10_global"] = round(
             (50 * us_per_layer["sliding"] + 10 * us_per_layer["global"]) / 60, 2)
-    pct = {c.layer: [round(float(np.percentile(c.times_ms, p)) * 1e3, 2) for p in (10, 50, 90)]
+    pct = {c.name: [round(float(np.percentile(c.times_ms, p)) * 1e3, 2) for p in (10, 50, 90)]
            for c in calls}
 
     if rank != 0:

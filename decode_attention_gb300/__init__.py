@@ -24,6 +24,7 @@ from ._native import (  # noqa: F401
     GQAError,
     gqa_decode,
     gqa_decode_noalloc,
+    gqa_decode_ring,
     gqa_decode_paged,
     gqa_check_inputs_host,
     gqa_device_status,

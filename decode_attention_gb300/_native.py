@@ -32,7 +32,8 @@ GQA_DEVICE_BAD_LENGTH = 4
 PAGE_SIZE = 16
 
 EXPORTED_SYMBOLS = ("gqa_workspace_size", "gqa_workspace_init", "gqa_decode", "gqa_decode_paged",
-                    "gqa_device_status", "gqa_decode_noalloc", "gqa_check_inputs_host",
+                    "gqa_device_status", "gqa_decode_noalloc", "gqa_decode_ring",
+                    "gqa_check_inputs_host",
                     "gqa_status_string")
 
 _lock = threading.Lock()
@@ -74,6 +75,8 @@ def load_library(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.gqa_decode_paged.restype = ci
         lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, ci, vp]
         lib.gqa_decode_noalloc.restype = ci
+        lib.gqa_decode_ring.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, ci, vp, sz, vp]
+        lib.gqa_decode_ring.restype = ci
         lib.gqa_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gqa_device_status.restype = ci
         lib.gqa_check_inputs_host.argtypes = [vp, ci, ci, ci, vp, ci, ci, ctypes.POINTER(ci)]
@@ -194,6 +197,31 @@ def gqa_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tens
         block_table.shape[1], page_size, H, KVH, D, int(window), _ptr(out), _out_code(out),
         _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
     _check("gqa_decode_paged", st)
+    return out
+
+
+def gqa_decode_ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
+                    window: int, out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+                    workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """attn.core over a window-capped ring cache: k/v [B,C,KVH,D] (bf16) hold position s
+    at row s % C; attends [max(0, L - window), L) with 1 <= window <= C."""
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("k", k, torch.bfloat16, 4)
+    _check_tensor("v", v, torch.bfloat16, 4)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    B, H, D = q.shape
+    _, C, KVH, _ = k.shape
+    _require(tuple(k.shape) == (B, C, KVH, D) and v.shape == k.shape, "k/v shape mismatch")
+    _require(seq_lens.shape[0] == B, "seq_lens must have B entries")
+    if out is None:
+        out = torch.empty((B, H, D), dtype=out_dtype, device=q.device)
+    _check_tensor("out", out, out.dtype, 3)
+    _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().gqa_decode_ring(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, C, H, KVH, D, int(window), _ptr(out),
+        _out_code(out), _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
+    _check("gqa_decode_ring", st)
     return out
 
 

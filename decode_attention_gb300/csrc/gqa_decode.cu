@@ -158,7 +158,7 @@ gqa_status_t prepare(const CallShape& c, void* workspace, size_t workspace_bytes
 
 gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, const void* v,
                  const int32_t* block_table, const int32_t* seq_lens, uint64_t rows,
-                 uint64_t outer, int capacity, int num_pages, int max_pages, void* out,
+                 uint64_t outer, int capacity, int ring, int num_pages, int max_pages, void* out,
                  gqa_out_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
                  cudaStream_t stream) {
     if (!gqa::tensor_map_encoder()) return GQA_ERR_CUDA;
@@ -190,6 +190,7 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
     a.p.H = c.H;
     a.p.KVH = c.KVH;
     a.p.capacity = capacity;
+    a.p.ring = ring;
     a.p.window = c.window;
     a.p.num_pages = num_pages;
     a.p.max_pages = max_pages;
@@ -231,7 +232,7 @@ gqa_status_t gqa_decode(const void* q, const void* k, const void* v, const int32
     if (st != GQA_OK || B == 0) return st;
     if (!k || !v || !aligned(k, 16) || !aligned(v, 16)) return GQA_ERR_INVALID_ARGUMENT;
     return run(c, false, q, k, v, nullptr, seq_lens, static_cast<uint64_t>(S),
-               static_cast<uint64_t>(B), S, 0, 0, out, out_dtype, workspace, workspace_bytes,
+               static_cast<uint64_t>(B), S, 0, 0, 0, out, out_dtype, workspace, workspace_bytes,
                reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -250,8 +251,23 @@ gqa_status_t gqa_decode_paged(const void* q, const void* k_pages, const void* v_
         !aligned(block_table, 4))
         return GQA_ERR_INVALID_ARGUMENT;
     return run(c, true, q, k_pages, v_pages, block_table, seq_lens, GQA_PAGE_SIZE,
-               static_cast<uint64_t>(P), max_pages * GQA_PAGE_SIZE, P, max_pages, out, out_dtype,
-               workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+               static_cast<uint64_t>(P), max_pages * GQA_PAGE_SIZE, 0, P, max_pages, out,
+               out_dtype, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t gqa_decode_ring(const void* q, const void* k, const void* v, const int32_t* seq_lens,
+                             int B, int C, int H, int KVH, int D, int window, void* out,
+                             gqa_out_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
+                             gqa_stream_t stream) {
+    const CallShape c{geometry_of(H, KVH, D), B, H, KVH, D, window};
+    if (C < 1 || C > GQA_MAX_SEQ || window < 1 || window > C) return GQA_ERR_INVALID_ARGUMENT;
+    gqa_status_t st = check_common(c, q, out, seq_lens, out_dtype);
+    if (st != GQA_OK || B == 0) return st;
+    if (!k || !v || !aligned(k, 16) || !aligned(v, 16)) return GQA_ERR_INVALID_ARGUMENT;
+    // lengths are clamped to the longest context, not to the ring
+    return run(c, false, q, k, v, nullptr, seq_lens, static_cast<uint64_t>(C),
+               static_cast<uint64_t>(B), GQA_MAX_SEQ, C, 0, 0, out, out_dtype, workspace,
+               workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gqa_status_t gqa_device_status(void* workspace, uint32_t* flags, gqa_stream_t stream) {

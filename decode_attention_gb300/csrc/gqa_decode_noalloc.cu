@@ -158,6 +158,7 @@ extern "C" gqa_status_t gqa_decode_noalloc(const void* q, const void* k, const v
     a.p.H = H;
     a.p.KVH = KVH;
     a.p.capacity = S;
+    a.p.ring = 0;
     a.p.window = window;
     a.p.num_pages = 0;
     a.p.max_pages = 0;

@@ -85,7 +85,8 @@ struct DecodeParams {
     int dyn_slot_base;            // first workspace slot of the dynamic chunks (> grid + B*KVH - 2)
     int max_dyn;                  // dynamic-chunk slots the workspace holds (<= kMaxDynUnits)
     int B, H, KVH;
-    int capacity;                 // S, or 16 * max_pages
+    int capacity;                 // S, or 16 * max_pages (GQA_MAX_SEQ for a ring)
+    int ring;                     // > 0: contiguous ring of `ring` rows, position s at row s mod ring
     int window;                   // 0 = full history
     int num_pages;                // P (paged)
     int max_pages;                // block-table row length (paged)
@@ -536,10 +537,6 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
 
         // Streams the tiles of positions [p0, p1) of segment (b, kvh); returns false on abort.
         auto emit_piece = [&](int b, int kvh, int p0, int p1, int slot, bool unit_end) -> bool {
-            const int t_first = kPaged ? (p0 & ~(kPageRows - 1)) : p0;
-            const int chunk0 = kvh * kChunksPerRow;
-            const int32_t* bt_row =
-                kPaged ? p.block_table + static_cast<size_t>(b) * p.max_pages : nullptr;
             // the piece's q goes to buffer q_n & 1 once the consumers are done with
             // the q the buffer held two pieces ago
             const uint32_t qb = q_n & 1u;
@@ -547,54 +544,70 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
                               &sm.abort_flag, p.ws_flags))
                 return false;
             ++q_n;
-            for (int t = t_first; t < p1; t += TP) {
-                if (dynamic && unit_end && t + TP >= p1)
-                    claimed = static_cast<int>(atomicAdd(p.ws_claim, 1u));
-                const int s = t_idx % STAGES;
-                const uint32_t ph = (t_idx / STAGES) & 1u;
-                if (!wait_bounded(ptx::smem_addr(&sm.empty[s]), ph ^ 1u, &sm.abort_flag,
-                                  p.ws_flags))
-                    return false;
-                const bool first = (t == t_first);
-                TileDesc& d = sm.desc[s];
-                d.b = b;
-                d.kvh = kvh;
-                d.t = t;
-                d.vlo = (p0 > t ? p0 : t) - t;
-                d.vhi = (p1 < t + TP ? p1 : t + TP) - t;
-                d.slot = slot;
-                d.flags = (first ? kDescFirst : 0) | (t + TP >= p1 ? kDescLast : 0);
-                int nbox = 0;
+            const int chunk0 = kvh * kChunksPerRow;
+            const int32_t* bt_row =
+                kPaged ? p.block_table + static_cast<size_t>(b) * p.max_pages : nullptr;
+            bool first = true;
+            // runs [a, e) of positions held in consecutive rows: the whole piece,
+            // or on a ring the parts between multiples of the ring length
+            for (int a = p0; a < p1;) {
+                const int base = p.ring > 0 ? (a / p.ring) * p.ring : 0;   // row = position - base
+                const int e = p.ring > 0 && base + p.ring < p1 ? base + p.ring : p1;
+                const int t_first = kPaged ? (a & ~(kPageRows - 1)) : a;
+                for (int t = t_first; t < e; t += TP) {
+                    const bool last = (t + TP >= e) && (e == p1);
+                    if (dynamic && unit_end && last)
+                        claimed = static_cast<int>(atomicAdd(p.ws_claim, 1u));
+                    const int s = t_idx % STAGES;
+                    const uint32_t ph = (t_idx / STAGES) & 1u;
+                    if (!wait_bounded(ptx::smem_addr(&sm.empty[s]), ph ^ 1u, &sm.abort_flag,
+                                      p.ws_flags))
+                        return false;
+                    const int row0 = t - base;
+                    TileDesc& d = sm.desc[s];
+                    d.b = b;
+                    d.kvh = kvh;
+                    d.t = row0;
+                    d.vlo = (a > t ? a : t) - t;
+                    d.vhi = (e < t + TP ? e : t + TP) - t;
+                    d.slot = slot;
+                    d.flags = (first ? kDescFirst : 0) | (last ? kDescLast : 0);
+                    int nbox = 0;
 #pragma unroll
-                for (int j = 0; j < kBoxesPerTile; ++j) nbox += (t + j * kBoxRows < p1) ? 1 : 0;
-                const uint32_t full_bar = ptx::smem_addr(&sm.full[s]);
-                ptx::mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(nbox) * 2u * kBoxBytes +
-                                                         (first ? kQBytes : 0u));
-                if (first)
-                    ptx::bulk_copy_g2s(ptx::smem_addr(&sm.q[qb][0]),
-                                       p.q + (static_cast<size_t>(b) * H + kvh * G) * D, kQBytes,
-                                       full_bar);
-                const uint32_t k_dst = kv_base + s * kStageBytes;
-                const uint32_t v_dst = k_dst + KernelSmem<Pol>::kTileBytes;
-                for (int j = 0; j < nbox; ++j) {
-                    if (kPaged) {
-                        int page = bt_row[(t >> 4) + j];
-                        if (page < 0 || page >= p.num_pages) page = 0;   // flagged by the consumers
-                        // swizzled map: (elem, slot, chunk, page); plain map: (elem, kvh, slot, page)
-                        const int c1 = Pol::kSwizzle128 ? 0 : kvh;
-                        const int c2 = Pol::kSwizzle128 ? chunk0 : 0;
-                        ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, c1, c2, page, policy);
-                        ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, c1, c2, page, policy);
-                    } else {
-                        const int row = t + j * kBoxRows;
-                        // swizzled map: (elem, position, chunk, seq); plain map: (elem, kvh, position, seq)
-                        const int c1 = Pol::kSwizzle128 ? row : kvh;
-                        const int c2 = Pol::kSwizzle128 ? chunk0 : row;
-                        ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, c1, c2, b, policy);
-                        ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, c1, c2, b, policy);
+                    for (int j = 0; j < kBoxesPerTile; ++j) nbox += (t + j * kBoxRows < e) ? 1 : 0;
+                    const uint32_t full_bar = ptx::smem_addr(&sm.full[s]);
+                    ptx::mbar_arrive_expect_tx(full_bar,
+                                               static_cast<uint32_t>(nbox) * 2u * kBoxBytes +
+                                                   (first ? kQBytes : 0u));
+                    if (first)
+                        ptx::bulk_copy_g2s(ptx::smem_addr(&sm.q[qb][0]),
+                                           p.q + (static_cast<size_t>(b) * H + kvh * G) * D,
+                                           kQBytes, full_bar);
+                    const uint32_t k_dst = kv_base + s * kStageBytes;
+                    const uint32_t v_dst = k_dst + KernelSmem<Pol>::kTileBytes;
+                    for (int j = 0; j < nbox; ++j) {
+                        if (kPaged) {
+                            int page = bt_row[(row0 >> 4) + j];
+                            if (page < 0 || page >= p.num_pages) page = 0;   // flagged by the consumers
+                            // swizzled map: (elem, slot, chunk, page); plain map: (elem, kvh, slot, page)
+                            const int c1 = Pol::kSwizzle128 ? 0 : kvh;
+                            const int c2 = Pol::kSwizzle128 ? chunk0 : 0;
+                            ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, c1, c2, page, policy);
+                            ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, c1, c2, page, policy);
+                        } else {
+                            // rows past the end of the cache (a run's last tile) read as zeros
+                            const int row = row0 + j * kBoxRows;
+                            // swizzled map: (elem, position, chunk, seq); plain map: (elem, kvh, position, seq)
+                            const int c1 = Pol::kSwizzle128 ? row : kvh;
+                            const int c2 = Pol::kSwizzle128 ? chunk0 : row;
+                            ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, c1, c2, b, policy);
+                            ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, c1, c2, b, policy);
+                        }
                     }
+                    first = false;
+                    ++t_idx;
                 }
-                ++t_idx;
+                a = e;
             }
             return true;
         };

@@ -102,6 +102,7 @@ class Workload:
     lengths: object = field(repr=False)
     layers: tuple = ()       # ("sliding",) / ("global",) / ("sliding", "global")
     paged: bool = False
+    rings: tuple = ()        # windows of ring-cache sliding calls (ring length = window)
 
     def seq_lens(self) -> np.ndarray:
         return self.lengths(np.random.default_rng(self.seed))
@@ -122,6 +123,14 @@ WORKLOADS = {
                  "sigma 1) clipped to [1, 65536]; one sliding and one global call",
                  B=256, S=65536, seed=4, lengths=lengths_lognormal(4096, 1.0, 1, 65536, 256),
                  layers=("sliding", "global"), paged=True),
+        # One block of the progressive-window retrofit ("Retrofit Plan: Gemma 4 31B IT ->
+        # Progressive Multi-Scale SWA with Block Attention Residuals", §3.3): four
+        # sliding layers with windows 1024, 2048, 4096, 8192, each over its own
+        # window-capped ring cache, at the batched sliding shape's lengths.
+        Workload("retrofit_block_b64", "progressive-window sliding block, B=64, seq_lens uniform "
+                 "on [1, 32768]; four ring-cache calls, windows 1024/2048/4096/8192",
+                 B=64, S=32768, seed=6, lengths=lengths_uniform(1, 32768, 64),
+                 layers=("sliding",), rings=(1024, 2048, 4096, 8192)),
         # Smaller instance of the batched sliding shape for profiler captures: the same
         # bytes per call as sliding_b64_s32768 (every sequence reads its full 1024-position
         # window) with a 2 GB cache instead of 34 GB.

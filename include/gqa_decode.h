@@ -196,6 +196,29 @@ gqa_status_t gqa_decode_noalloc(const void *q, const void *k, const void *v,
                                 gqa_stream_t stream);
 
 /*
+ * Decode over a window-capped ring-buffer cache.  Each sliding layer of the
+ * retrofit on the "Retrofit Plan: Gemma 4 31B IT -> Progressive Multi-Scale SWA
+ * with Block Attention Residuals" page keeps its own KV cache, capped at its
+ * window (§3.3 "Progressive Window Assignment", windows 1024/2048/4096/8192;
+ * §7.3: the cache grows with the window, not with the sequence).
+ *
+ *   k, v   bf16 [B, C, KVH, D] contiguous; position s of sequence b is held in
+ *          row s mod C (the caller writes the new token there before the call)
+ *   C      ring length, 1 <= C <= GQA_MAX_SEQ
+ *   window attended positions [max(0, L - window), L), 1 <= window <= C, so
+ *          every one of them is still in the ring
+ * seq_lens[b] = L is the sequence's length, which may exceed C; it is clamped
+ * to [0, GQA_MAX_SEQ] (GQA_DEVICE_BAD_LENGTH when clamped).  Everything else --
+ * q, out, workspace, stream, geometries, errors -- is as for gqa_decode; a C or
+ * window outside the ranges above returns GQA_ERR_INVALID_ARGUMENT.  The same
+ * workspace size serves (it does not depend on C).
+ */
+gqa_status_t gqa_decode_ring(const void *q, const void *k, const void *v,
+                             const int32_t *seq_lens, int B, int C, int H, int KVH, int D,
+                             int window, void *out, gqa_out_dtype_t out_dtype, void *workspace,
+                             size_t workspace_bytes, gqa_stream_t stream);
+
+/*
  * Host-side check of the device-resident inputs, for tests and debugging: the
  * caller copies seq_lens (and the block table) to host memory and passes them
  * here.  The decode calls never read these arrays on the host (they stay on the

@@ -184,3 +184,19 @@ def test_check_inputs_host_rejects_bad_sizes(lib):
     assert lib.gqa_check_inputs_host(lens, 1, 64, -1, None, 0, 0, None) == gqa.GQA_ERR_INVALID_ARGUMENT
     assert lib.gqa_check_inputs_host(lens, 1, 64, 0, lens, 0, 3, None) == gqa.GQA_ERR_INVALID_ARGUMENT
     assert lib.gqa_check_inputs_host(lens, 1, 64, 0, None, 0, 0, None) == gqa.GQA_OK
+
+
+def test_ring_argument_checks(lib):
+    F = FAKE
+    H, KVH, D = SLIDING
+    st = gqa.GQA_ERR_INVALID_ARGUMENT
+    # window must lie in [1, C]; C in [1, GQA_MAX_SEQ]
+    assert lib.gqa_decode_ring(F, F, F, F, 2, 1024, H, KVH, D, 0, F, 1, None, 0, None) == st
+    assert lib.gqa_decode_ring(F, F, F, F, 2, 1024, H, KVH, D, 1025, F, 1, None, 0, None) == st
+    assert lib.gqa_decode_ring(F, F, F, F, 2, 0, H, KVH, D, 1, F, 1, None, 0, None) == st
+    assert lib.gqa_decode_ring(F, F, F, F, 2, 262145, H, KVH, D, 1024, F, 1, None, 0, None) == st
+    assert lib.gqa_decode_ring(F, None, F, F, 2, 1024, H, KVH, D, 1024, F, 1, None, 0, None) == st
+    assert lib.gqa_decode_ring(F, F, F, F, 2, 1024, 32, 8, 256, 1024, F, 1, None, 0, None) == \
+        gqa.GQA_ERR_UNSUPPORTED
+    assert lib.gqa_decode_ring(None, None, None, None, 0, 1024, H, KVH, D, 1024, None, 1, None, 0,
+                               None) == gqa.GQA_OK

@@ -16,10 +16,9 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import decode_attention_gb300 as gqa  # noqa: E402
-import oracle  # noqa: E402
 
 WORKLOADS = ["sliding_b1_s2048", "global_b8_s8192", "sliding_b64_s32768",
-             "global_b16_s131072", "paged_mixed_b256"]
+             "global_b16_s131072", "paged_mixed_b256", "retrofit_block_b64"]
 
 
 def sampled(lens, k=3, seed=0):
@@ -45,9 +44,9 @@ def test_workload_sampled_parity(name):
         assert gqa.gqa_device_status() == 0
         assert torch.equal(out16, out32.to(torch.bfloat16))
         for b in sampled(lens, seed=wl.seed):
-            qb, kb, vb, L, base = bench.host_slices(c, b)
-            ref = oracle.gqa_decode_f64(qb, kb, vb, [L], c.geo["window"], pos_base=base)[0]
-            assert_parity(out32[b], ref, f"{name}/{c.layer} b={b} L={L}")
+            slices = bench.host_slices(c, b)
+            ref = bench.oracle_for(c, slices)
+            assert_parity(out32[b], ref, f"{name}/{c.name} b={b} L={slices[3]}")
         # sequences with nothing to attend are exact zeros
         for b, L in enumerate(lens):
             if L == 0:
