@@ -55,6 +55,9 @@ def _bind(path: str):
     lib.oracle_gqa_decode_ring_f64.argtypes = [u16p, u16p, u16p, i32p, ci, ci, ci, ci, ci, ci,
                                                ci, f64p]
     lib.oracle_gqa_decode_ring_f64.restype = ci
+    lib.oracle_gqa_decode_keqv_f64.argtypes = [u16p, u16p, u16p, i32p, ci, ci, ci, ci, ci, ci,
+                                               ci, ctypes.c_double, ci, f64p]
+    lib.oracle_gqa_decode_keqv_f64.restype = ci
     lib.oracle_default_threads.argtypes = []
     lib.oracle_default_threads.restype = ci
     return lib
@@ -168,6 +171,39 @@ def gqa_decode_ring_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, seq_lens, w
     return out
 
 
+# RoPE of the global layers (Model Spec, `attn.rope` row for layers 5, 11, ..., 59)
+GLOBAL_ROPE_PAIRS = 64
+GLOBAL_ROPE_THETA = 1.0e6
+
+
+def gqa_decode_keqv_f64(q: np.ndarray, v: np.ndarray, w_k: np.ndarray, seq_lens, window: int,
+                        n_rot: int = GLOBAL_ROPE_PAIRS, theta: float = GLOBAL_ROPE_THETA,
+                        nthreads: int = 0, _lib_override=None) -> np.ndarray:
+    """Decode attention over a single K=V cache, exact up to fp64 rounding.
+
+    v: uint16 [B, S, KVH, D], the cached values (row s is position s); w_k: uint16
+    [D], the k_norm weight.  The key of row s is rope(w_k * v[s], s): pairs
+    (i, i + D/2), i < n_rot, rotated by s * theta^(-2i/D).
+    """
+    q, v, w_k = _u16(q), _u16(v), _u16(w_k)
+    B, H, D = q.shape
+    Bv, S, KVH, Dv = v.shape
+    if Bv != B or Dv != D or w_k.shape != (D,):
+        raise ValueError("shape mismatch between q, v and w_k")
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError("seq_lens must have shape [B]")
+    out = np.zeros((B, H, D), dtype=np.float64)
+    lib = _lib_override if _lib_override is not None else _load()
+    rc = lib.oracle_gqa_decode_keqv_f64(
+        _ptr(q, ctypes.c_uint16), _ptr(v, ctypes.c_uint16), _ptr(w_k, ctypes.c_uint16),
+        _ptr(lens, ctypes.c_int32), B, S, H, KVH, D, int(window), int(n_rot), float(theta),
+        int(nthreads), _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out
+
+
 class OracleLibrary:
     """The oracle API bound to a specific compiled copy of the C source.
 
@@ -186,6 +222,9 @@ class OracleLibrary:
 
     def gqa_decode_ring_f64(self, *args, **kw):
         return gqa_decode_ring_f64(*args, _lib_override=self._lib, **kw)
+
+    def gqa_decode_keqv_f64(self, *args, **kw):
+        return gqa_decode_keqv_f64(*args, _lib_override=self._lib, **kw)
 
 
 def compile_variant(source_text: str, out_path: str) -> str:

@@ -403,3 +403,128 @@ int oracle_gqa_decode_ring_f64(const uint16_t *q, const uint16_t *k, const uint1
     (void)nthreads;
     return err;
 }
+
+/* ---- single K=V global cache (gemma-4-31B Model Spec, "What to watch for": the
+ *      global layers have values = keys; "Gemma 4 31B-it Text Architecture",
+ *      decoder listing: V_raw = K_raw on full layers, K = rope(k_norm(K_raw)),
+ *      V = v_norm(K_raw)).  k_norm and v_norm divide the same vector by the same
+ *      root mean square, so k_norm(K_raw) = w_k * v elementwise and the key of a
+ *      cached value row v at position s is
+ *          k = rope(w_k * v, s)
+ *      with the Model Spec's `attn.rope` row for global layers: pairs (i, i + D/2),
+ *      i < n_rot, rotated by s * theta^(-2i/D):
+ *          k[i]       = x[i] cos(a) - x[i + D/2] sin(a)
+ *          k[i + D/2] = x[i + D/2] cos(a) + x[i] sin(a),   a = s * theta^(-2i/D)
+ *      and every other coordinate unchanged (zero inverse frequency). ---- */
+
+/* key of cached row `vr` (D bf16) at position s, in double precision */
+static void derived_key(const uint16_t *vr, const double *w, int D, int n_rot, double theta,
+                        int64_t s, double *k)
+{
+    int d, i;
+    const int half = D / 2;
+    for (d = 0; d < D; ++d) k[d] = w[d] * bf16_bits_to_double(vr[d]);
+    for (i = 0; i < n_rot; ++i) {
+        const double a = (double)s * pow(theta, -2.0 * (double)i / (double)D);
+        const double c = cos(a), sn = sin(a);
+        const double x0 = k[i], x1 = k[i + half];
+        k[i] = x0 * c - x1 * sn;
+        k[i + half] = x1 * c + x0 * sn;
+    }
+}
+
+/*
+ * q:        [B, H, D] bf16 bits (already normed and rotated at its own position)
+ * v:        [B, S, KVH, D] bf16 bits, the cached values; row s is position s
+ * w_k:      [D] bf16 bits, the layer's k_norm weight
+ * n_rot, theta: rotated pairs and RoPE base (64 and 1e6 for the global layers)
+ * Steps 1-5 of the definition at the top, with k derived from v as above.
+ */
+int oracle_gqa_decode_keqv_f64(const uint16_t *q, const uint16_t *v, const uint16_t *w_k,
+                               const int32_t *seq_lens, int B, int S, int H, int KVH, int D,
+                               int window, int n_rot, double theta, int nthreads, double *out)
+{
+    int b;
+    if (B < 0 || S < 0 || H <= 0 || KVH <= 0 || D <= 0 || D % 2 != 0 || window < 0 ||
+        n_rot < 0 || n_rot > D / 2 || !(theta > 0.0))
+        return ORACLE_EINVAL;
+    if (H % KVH != 0) return ORACLE_EINVAL;
+    int64_t max_n = 1;
+    for (b = 0; b < B; ++b) {
+        int64_t lo, hi;
+        if (seq_lens[b] < 0 || seq_lens[b] > S) return ORACLE_EINVAL;
+        attended_range(seq_lens[b], window, &lo, &hi);
+        if (hi - lo > max_n) max_n = hi - lo;
+    }
+    const int g = H / KVH;
+    const int64_t pairs = (int64_t)B * H;
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#endif
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)max_n);
+        double *q_row = (double *)malloc(sizeof(double) * (size_t)D);
+        double *w = (double *)malloc(sizeof(double) * (size_t)D);
+        double *k = (double *)malloc(sizeof(double) * (size_t)D);
+        const int have_scratch = scores && q_row && w && k;
+        int64_t p;
+        /* every thread reaches the work-sharing loop (it ends in a barrier) */
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (p = 0; p < pairs; ++p) {
+            if (!have_scratch) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+                err = ORACLE_ENOMEM;
+                continue;
+            }
+            {
+                const int64_t bb = p / H, h = p % H, kvh = h / g;
+                double *o = out + (bb * H + h) * D;
+                int64_t lo, hi, j;
+                int d;
+                attended_range(seq_lens[bb], window, &lo, &hi);
+                for (d = 0; d < D; ++d) {
+                    q_row[d] = bf16_bits_to_double(q[(bb * H + h) * D + d]);
+                    w[d] = bf16_bits_to_double(w_k[d]);
+                    o[d] = 0.0;
+                }
+                const int64_t n = hi - lo;
+                if (n <= 0) continue; /* empty sum */
+                /* 1. scores with the derived keys, scale 1 */
+                for (j = 0; j < n; ++j) {
+                    const int64_t s = lo + j;
+                    derived_key(v + ((bb * S + s) * KVH + kvh) * D, w, D, n_rot, theta, s, k);
+                    double acc = 0.0;
+                    for (d = 0; d < D; ++d) acc += q_row[d] * k[d];
+                    scores[j] = acc;
+                }
+                /* 2. max, 3. exponentials, 4. normaliser */
+                double m = scores[0];
+                for (j = 1; j < n; ++j)
+                    if (scores[j] > m) m = scores[j];
+                double l = 0.0;
+                for (j = 0; j < n; ++j) {
+                    scores[j] = exp(scores[j] - m);
+                    l += scores[j];
+                }
+                /* 5. weighted sum of the cached values over the normaliser */
+                for (j = 0; j < n; ++j) {
+                    const uint16_t *vr = v + ((bb * S + lo + j) * KVH + kvh) * D;
+                    for (d = 0; d < D; ++d) o[d] += scores[j] * bf16_bits_to_double(vr[d]);
+                }
+                for (d = 0; d < D; ++d) o[d] /= l;
+            }
+        }
+        free(scores);
+        free(q_row);
+        free(w);
+        free(k);
+    }
+    (void)nthreads;
+    return err;
+}

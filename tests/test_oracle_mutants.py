@@ -33,8 +33,8 @@ MUTANTS = {
         "paged_ctx c = {k_pages, v_pages, bt_row, h / g,",
         "paged_ctx c = {k_pages, v_pages, bt_row, h % KVH,"),
     "no_max_subtraction": (
-        "scores[j] = exp(scores[j] - m);",
-        "scores[j] = exp(scores[j]);"),
+        "\n        scores[j] = exp(scores[j] - m);",
+        "\n        scores[j] = exp(scores[j]);"),
     "keys_and_values_swapped": (
         "const uint16_t *kr = k_row(ctx, j);",
         "const uint16_t *kr = v_row(ctx, j);"),
@@ -45,8 +45,8 @@ MUTANTS = {
         "for (d = 0; d < D; ++d) out[d] /= l;",
         "(void)l;"),
     "first_term_of_normaliser_dropped": (
-        "        l += scores[j];\n",
-        "        l += (j > 0) ? scores[j] : 0.0;\n"),
+        "\n        l += scores[j];\n",
+        "\n        l += (j > 0) ? scores[j] : 0.0;\n"),
     "last_key_dropped": (
         "attend(q_row, D, hi - lo, contig_k",
         "attend(q_row, D, hi - lo - (hi - lo > 1), contig_k"),
@@ -68,6 +68,21 @@ MUTANTS = {
     "ring_window_start_late": (
         "attend(q_row, D, hi - lo, ring_k",
         "attend(q_row, D, hi - lo - (hi - lo > 1), ring_k"),
+    "keqv_frequency_exponent": (
+        "pow(theta, -2.0 * (double)i / (double)D)",
+        "pow(theta, -2.0 * (double)i / (double)(D / 2))"),
+    "keqv_sine_sign": (
+        "k[i] = x0 * c - x1 * sn;",
+        "k[i] = x0 * c + x1 * sn;"),
+    "keqv_pair_offset": (
+        "const int half = D / 2;\n    for (d = 0; d < D; ++d) k[d] = w[d]",
+        "const int half = D / 2 - 1;\n    for (d = 0; d < D; ++d) k[d] = w[d]"),
+    "keqv_position_shift": (
+        "w, D, n_rot, theta, s, k);",
+        "w, D, n_rot, theta, s + 1, k);"),
+    "keqv_weight_ignored": (
+        "for (d = 0; d < D; ++d) k[d] = w[d] * bf16_bits_to_double(vr[d]);",
+        "for (d = 0; d < D; ++d) k[d] = bf16_bits_to_double(vr[d]);"),
     "empty_range_not_zero": (
         "if (n <= 0) return; /* empty sum */",
         "if (n <= 0) { for (d = 0; d < D; ++d) out[d] = 1.0; return; }"),

@@ -426,6 +426,86 @@ def test_ring_rejects_windows_it_cannot_hold(oracle_lib):
             oracle_lib.gqa_decode_ring_f64(q, k, v, [20], W)
 
 
+# ---------------------------------------------------------------------------
+# single K=V global cache: the key of cached value row v at position s is
+# rope(w_k * v, s) (Model Spec "What to watch for" and `attn.rope` row; decoder
+# listing of the "Gemma 4 31B-it Text Architecture" page)
+# ---------------------------------------------------------------------------
+
+def complex_rope_keys(v_vals, w_vals, positions, n_rot, theta):
+    """Keys through a different route: each rotated pair (i, i + D/2) as the complex
+    number x_i + j x_{i+D/2}, multiplied by exp(j * s * theta^(-2i/D))."""
+    x = v_vals * w_vals                                   # [S, ..., D]
+    D = x.shape[-1]
+    half = D // 2
+    z = x[..., :n_rot] + 1j * x[..., half:half + n_rot]
+    freq = theta ** (-2.0 * np.arange(n_rot) / D)
+    pos = np.asarray(positions, dtype=np.float64).reshape(-1, 1, 1)   # the [S, KVH, pair] axes
+    z = z * np.exp(1j * pos * freq)
+    k = x.copy()
+    k[..., :n_rot] = z.real
+    k[..., half:half + n_rot] = z.imag
+    return k
+
+
+@pytest.mark.parametrize("H,KVH,D,n_rot,theta,W", [(8, 2, 16, 3, 100.0, 0), (8, 2, 16, 8, 10.0, 5),
+                                                   (32, 4, 64, 8, 1.0e6, 0)])
+def test_keqv_complex_rope_and_sdpa(oracle_lib, H, KVH, D, n_rot, theta, W):
+    B, S = 3, 37
+    q, _, v = random_case(B, S, H, KVH, D, seed=20 + D + n_rot)
+    w = to_bits(1.0 + 0.25 * np.random.default_rng(21).standard_normal(D))
+    lens = [37, 20, 1]
+    out = oracle_lib.gqa_decode_keqv_f64(q, v, w, lens, W, n_rot=n_rot, theta=theta)
+    g = H // KVH
+    k64 = complex_rope_keys(to_vals(v), to_vals(w), np.arange(S), n_rot, theta)   # [B, S, KVH, D]
+    qt = torch.from_numpy(to_vals(q))[:, :, None, :]
+    kt = torch.from_numpy(k64).permute(0, 2, 1, 3).repeat_interleave(g, dim=1)
+    vt = torch.from_numpy(to_vals(v)).permute(0, 2, 1, 3).repeat_interleave(g, dim=1)
+    pos = torch.arange(S)
+    mask = torch.zeros(B, 1, 1, S, dtype=torch.bool)
+    for b, L in enumerate(lens):
+        lo, hi = window_range(L, W)
+        mask[b, 0, 0] = (pos >= lo) & (pos < hi)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=1.0)
+    np.testing.assert_allclose(out, ref[:, :, 0, :].numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_keqv_global_geometry_long_positions(oracle_lib):
+    """D = 512, 64 rotated pairs, theta = 1e6, keys at positions just below 131075
+    (a 40-position window): the complex route again, on the rows of one sequence."""
+    H, KVH, D, S = 32, 4, 512, 131080
+    L, n = 131075, 40
+    rng = np.random.default_rng(22)
+    q = to_bits(rng.standard_normal((1, H, D)))
+    v = np.zeros((1, S, KVH, D), np.uint16)
+    v[0, L - n:L] = to_bits(rng.standard_normal((n, KVH, D)) * 0.3)
+    w = to_bits(1.0 + 0.25 * rng.standard_normal(D))
+    out = oracle_lib.gqa_decode_keqv_f64(q, v, w, [L], n)
+    k_tail = complex_rope_keys(to_vals(v[0, L - n:L]), to_vals(w), np.arange(L - n, L), 64, 1.0e6)
+    g = H // KVH
+    qt = torch.from_numpy(to_vals(q[0]))[:, None, :]                                   # [H, 1, D]
+    kt = torch.from_numpy(k_tail).permute(1, 0, 2).repeat_interleave(g, dim=0)          # [H, n, D]
+    vt = torch.from_numpy(to_vals(v[0, L - n:L])).permute(1, 0, 2).repeat_interleave(g, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=1.0)
+    np.testing.assert_allclose(out[0], ref[:, 0, :].numpy(), rtol=1e-9, atol=1e-12)
+
+
+def test_keqv_unrotated_dims_equal_plain_keys(oracle_lib):
+    """Values that live on unrotated coordinates only, with power-of-two weights
+    (so w * v is exact in bf16): identical to the plain oracle with k = w * v."""
+    B, S, H, KVH, D, n_rot = 2, 30, 8, 2, 16, 3
+    q, _, v = random_case(B, S, H, KVH, D, seed=23)
+    rot = list(range(n_rot)) + list(range(D // 2, D // 2 + n_rot))
+    v[..., rot] = 0
+    w_vals = np.array([2.0 ** ((i % 5) - 2) for i in range(D)])
+    w = exact_bits(w_vals)
+    k = exact_bits(to_vals(v) * w_vals)
+    lens = [30, 11]
+    keqv = oracle_lib.gqa_decode_keqv_f64(q, v, w, lens, 0, n_rot=n_rot, theta=1e4)
+    plain = oracle_lib.gqa_decode_f64(q, k, v, lens, 0)
+    assert np.array_equal(keqv, plain)
+
+
 def test_oracle_rejects_ranges_outside_the_cache(oracle_lib):
     q, k, v = random_case(1, 8, 4, 2, 8, seed=16)
     with pytest.raises(ValueError):
