@@ -113,12 +113,13 @@ class Call:
     """One library call of a step, with its inputs resident on the device."""
 
     def __init__(self, layer: str, geo: dict, case: dict, paged: bool, seq_lens: np.ndarray,
-                 device="cuda", ring: int = 0):
+                 device="cuda", ring: int = 0, keqv: bool = False):
         self.layer, self.geo, self.case, self.paged = layer, geo, case, paged
         self.ring = ring   # > 0: window-capped ring cache of `ring` rows
-        self.name = f"{layer}_ring{ring}" if ring else layer
+        self.keqv = keqv   # single K=V cache: only values are read
+        self.name = f"{layer}_ring{ring}" if ring else (f"{layer}_keqv" if keqv else layer)
         self.seq_lens = seq_lens
-        self.bytes = kv_bytes(seq_lens, geo)
+        self.bytes = kv_bytes(seq_lens, geo) // (2 if keqv else 1)
         self.times_ms = []
         if str(device).startswith("cuda"):
             B = len(seq_lens)
@@ -135,6 +136,8 @@ class Call:
                                  self.geo["window"], out=self.out)
         elif self.ring:
             gqa.gqa_decode_ring(q, c["k"], c["v"], lens, self.geo["window"], out=self.out)
+        elif self.keqv:
+            gqa.gqa_decode_keqv(q, c["v"], c["w_k"], lens, out=self.out)
         else:
             gqa.gqa_decode(q, c["k"], c["v"], lens, self.geo["window"], out=self.out)
 
@@ -149,6 +152,11 @@ def build_calls(wl: inputs.Workload, seed: int, device="cuda"):
             case = inputs.paged_case(wl.B, geo["H"], geo["KVH"], geo["D"], lens, seed + 100 * i,
                                      device=device, table=table)
             calls.append(Call(layer, geo, case, True, lens, device))
+    elif wl.keqv:
+        geo = inputs.geometry(wl.layers[0])
+        case = inputs.keqv_case(wl.B, wl.S, geo["H"], geo["KVH"], geo["D"], lens, seed,
+                                device=device)
+        calls.append(Call(wl.layers[0], geo, case, False, lens, device, keqv=True))
     elif wl.rings:
         for i, window in enumerate(wl.rings):
             geo = dict(inputs.geometry(wl.layers[0]), window=window)
@@ -281,6 +289,9 @@ def host_slices(call: Call, b: int):
     qb = inputs.bf16_bits(c["q"][b:b + 1])
     if call.ring:
         return qb, inputs.bf16_bits(c["k"][b:b + 1]), inputs.bf16_bits(c["v"][b:b + 1]), L, 0
+    if call.keqv:
+        # the oracle reads rows [0, L) of the value cache and the weight
+        return qb, inputs.bf16_bits(c["w_k"]), inputs.bf16_bits(c["v"][b:b + 1, :L]), L, 0
     if call.paged:
         pages = c["block_table"][b, lo // 16:(L + 15) // 16].long()
         k = c["k_pages"][pages].reshape(1, -1, geo["KVH"], geo["D"])
@@ -307,10 +318,12 @@ def oracle_sample(calls, budget_s: float, max_seqs: int | None = None):
         if n == 0:
             continue
         flops = 4.0 * n * call.geo["H"] * call.geo["D"]
+        if call.keqv:
+            flops *= 5.0   # plus a pow, cos and sin per rotated pair of every derived key
         if items and est + flops / rate > budget_s:
             break
         items.append((call, b, host_slices(call, b),
-                      n * call.geo["KVH"] * call.geo["D"] * 4))
+                      n * call.geo["KVH"] * call.geo["D"] * (2 if call.keqv else 4)))
         est += flops / rate
         if max_seqs and len(items) >= max_seqs:
             break
@@ -323,6 +336,8 @@ def oracle_for(call: Call, slices):
     qb, kb, vb, L, base = slices
     if call.ring:
         return oracle.gqa_decode_ring_f64(qb, kb, vb, [L], call.geo["window"])[0]
+    if call.keqv:
+        return oracle.gqa_decode_keqv_f64(qb, vb, kb, [L], 0)[0]   # kb holds w_k
     return oracle.gqa_decode_f64(qb, kb, vb, [L], call.geo["window"], pos_base=base)[0]
 
 

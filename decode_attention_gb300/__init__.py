@@ -23,6 +23,8 @@ from ._native import (  # noqa: F401
     PAGE_SIZE,
     GQAError,
     gqa_decode,
+    gqa_decode_keqv,
+    gqa_decode_keqv_paged,
     gqa_decode_noalloc,
     gqa_decode_ring,
     gqa_decode_paged,

@@ -33,6 +33,7 @@ PAGE_SIZE = 16
 
 EXPORTED_SYMBOLS = ("gqa_workspace_size", "gqa_workspace_init", "gqa_decode", "gqa_decode_paged",
                     "gqa_device_status", "gqa_decode_noalloc", "gqa_decode_ring",
+                    "gqa_decode_keqv", "gqa_decode_keqv_paged",
                     "gqa_check_inputs_host",
                     "gqa_status_string")
 
@@ -77,6 +78,11 @@ def load_library(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.gqa_decode_noalloc.restype = ci
         lib.gqa_decode_ring.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, ci, vp, sz, vp]
         lib.gqa_decode_ring.restype = ci
+        lib.gqa_decode_keqv.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ci, vp, sz, vp]
+        lib.gqa_decode_keqv.restype = ci
+        lib.gqa_decode_keqv_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp,
+                                              ci, vp, sz, vp]
+        lib.gqa_decode_keqv_paged.restype = ci
         lib.gqa_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gqa_device_status.restype = ci
         lib.gqa_check_inputs_host.argtypes = [vp, ci, ci, ci, vp, ci, ci, ctypes.POINTER(ci)]
@@ -222,6 +228,58 @@ def gqa_decode_ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens:
         _ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, C, H, KVH, D, int(window), _ptr(out),
         _out_code(out), _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
     _check("gqa_decode_ring", st)
+    return out
+
+
+def gqa_decode_keqv(q: torch.Tensor, v: torch.Tensor, w_k: torch.Tensor, seq_lens: torch.Tensor,
+                    out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+                    workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """decodeGQA over a single K=V cache: v [B,S,4,512] (bf16), w_k [512] (bf16) the
+    k_norm weight; each key is rope(w_k * v, position), derived in the kernel."""
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("v", v, torch.bfloat16, 4)
+    _check_tensor("w_k", w_k, torch.bfloat16, 1)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    B, H, D = q.shape
+    _, S, KVH, _ = v.shape
+    _require(tuple(v.shape) == (B, S, KVH, D) and w_k.shape[0] == D, "v / w_k shape mismatch")
+    _require(seq_lens.shape[0] == B, "seq_lens must have B entries")
+    if out is None:
+        out = torch.empty((B, H, D), dtype=out_dtype, device=q.device)
+    _check_tensor("out", out, out.dtype, 3)
+    _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().gqa_decode_keqv(
+        _ptr(q), _ptr(v), _ptr(w_k), _ptr(seq_lens), B, S, H, KVH, D, _ptr(out), _out_code(out),
+        _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
+    _check("gqa_decode_keqv", st)
+    return out
+
+
+def gqa_decode_keqv_paged(q: torch.Tensor, v_pages: torch.Tensor, w_k: torch.Tensor,
+                          block_table: torch.Tensor, seq_lens: torch.Tensor,
+                          out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+                          workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gqa_decode_keqv over a paged value cache: pool [P,16,4,512], block_table [B,max_pages]."""
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("v_pages", v_pages, torch.bfloat16, 4)
+    _check_tensor("w_k", w_k, torch.bfloat16, 1)
+    _check_tensor("block_table", block_table, torch.int32, 2)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    B, H, D = q.shape
+    P, page_size, KVH, _ = v_pages.shape
+    _require(v_pages.shape[3] == D and w_k.shape[0] == D, "page pool / w_k shape mismatch")
+    _require(block_table.shape[0] == B and seq_lens.shape[0] == B, "batch size mismatch")
+    if out is None:
+        out = torch.empty((B, H, D), dtype=out_dtype, device=q.device)
+    _check_tensor("out", out, out.dtype, 3)
+    _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().gqa_decode_keqv_paged(
+        _ptr(q), _ptr(v_pages), _ptr(w_k), _ptr(block_table), _ptr(seq_lens), B, P,
+        block_table.shape[1], page_size, H, KVH, D, _ptr(out), _out_code(out), _ptr(workspace),
+        ws_bytes, _stream_handle(stream, q.device))
+    _check("gqa_decode_keqv_paged", st)
     return out
 
 

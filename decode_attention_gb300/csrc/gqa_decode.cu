@@ -6,6 +6,7 @@
 // shapes from "Tensors of the main nodes"; 16-position pages from "At a glance",
 // Shape domain row).
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -29,6 +30,9 @@ Geometry geometry_of(int H, int KVH, int D) {
 }
 
 int heads_per_kv(Geometry g) { return g == Geometry::kSliding ? 2 : 8; }
+
+// RoPE base of the global layers (Model Spec, `attn.rope` row for layers 5, 11, ..., 59).
+constexpr double kGlobalRopeTheta = 1.0e6;
 
 // ---- workspace layout --------------------------------------------------------
 // [0, 4)              status word (uint32)
@@ -160,7 +164,7 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
                  const int32_t* block_table, const int32_t* seq_lens, uint64_t rows,
                  uint64_t outer, int capacity, int ring, int num_pages, int max_pages, void* out,
                  gqa_out_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, const void* w_k = nullptr) {
     if (!gqa::tensor_map_encoder()) return GQA_ERR_CUDA;
     void* ws = nullptr;
     WorkspaceLayout lay;
@@ -197,6 +201,14 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
     a.p.out_f32 = out_dtype == GQA_OUT_F32 ? 1 : 0;
     a.grid = grid;
     a.stream = stream;
+    if (w_k) {
+        // single K=V cache: keys derived in the kernel with the global layers' rotary
+        // frequencies theta^(-2i/D), i < 64, theta = 1e6
+        a.p.w_k = static_cast<const __nv_bfloat16*>(w_k);
+        for (int i = 0; i < 64; ++i)
+            a.p.rope_freq[i] = std::pow(kGlobalRopeTheta, -2.0 * i / static_cast<double>(c.D));
+        return gqa::launch_global_keqv(a, paged) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    }
     const cudaError_t e = c.geo == Geometry::kSliding ? gqa::launch_sliding(a, paged)
                                                       : gqa::launch_global(a, paged);
     return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
@@ -294,6 +306,41 @@ gqa_status_t gqa_device_status(void* workspace, uint32_t* flags, gqa_stream_t st
     }
     *flags = word;
     return GQA_OK;
+}
+
+gqa_status_t gqa_decode_keqv(const void* q, const void* v, const void* w_k,
+                             const int32_t* seq_lens, int B, int S, int H, int KVH, int D,
+                             void* out, gqa_out_dtype_t out_dtype, void* workspace,
+                             size_t workspace_bytes, gqa_stream_t stream) {
+    const CallShape c{geometry_of(H, KVH, D), B, H, KVH, D, 0};
+    if (S < 1 || S > GQA_MAX_SEQ) return GQA_ERR_INVALID_ARGUMENT;
+    if (c.geo == Geometry::kSliding) return GQA_ERR_UNSUPPORTED;   // values = keys on global layers only
+    gqa_status_t st = check_common(c, q, out, seq_lens, out_dtype);
+    if (st != GQA_OK || B == 0) return st;
+    if (!v || !w_k || !aligned(v, 16) || !aligned(w_k, 2)) return GQA_ERR_INVALID_ARGUMENT;
+    return run(c, false, q, v, v, nullptr, seq_lens, static_cast<uint64_t>(S),
+               static_cast<uint64_t>(B), S, 0, 0, 0, out, out_dtype, workspace, workspace_bytes,
+               reinterpret_cast<cudaStream_t>(stream), w_k);
+}
+
+gqa_status_t gqa_decode_keqv_paged(const void* q, const void* v_pages, const void* w_k,
+                                   const int32_t* block_table, const int32_t* seq_lens, int B,
+                                   int P, int max_pages, int page_size, int H, int KVH, int D,
+                                   void* out, gqa_out_dtype_t out_dtype, void* workspace,
+                                   size_t workspace_bytes, gqa_stream_t stream) {
+    const CallShape c{geometry_of(H, KVH, D), B, H, KVH, D, 0};
+    if (page_size != GQA_PAGE_SIZE || P < 1 || max_pages < 1 ||
+        static_cast<int64_t>(max_pages) * GQA_PAGE_SIZE > GQA_MAX_SEQ)
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (c.geo == Geometry::kSliding) return GQA_ERR_UNSUPPORTED;
+    gqa_status_t st = check_common(c, q, out, seq_lens, out_dtype);
+    if (st != GQA_OK || B == 0) return st;
+    if (!v_pages || !w_k || !block_table || !aligned(v_pages, 16) || !aligned(w_k, 2) ||
+        !aligned(block_table, 4))
+        return GQA_ERR_INVALID_ARGUMENT;
+    return run(c, true, q, v_pages, v_pages, block_table, seq_lens, GQA_PAGE_SIZE,
+               static_cast<uint64_t>(P), max_pages * GQA_PAGE_SIZE, 0, P, max_pages, out,
+               out_dtype, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), w_k);
 }
 
 gqa_status_t gqa_check_inputs_host(const int32_t* seq_lens, int B, int capacity, int window,

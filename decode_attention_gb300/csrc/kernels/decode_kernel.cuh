@@ -91,11 +91,23 @@ struct DecodeParams {
     int num_pages;                // P (paged)
     int max_pages;                // block-table row length (paged)
     int out_f32;                  // 1: fp32 output, 0: bf16
+    // single K=V cache (policies with kKeqV): the k_norm weight [D] and the rotary
+    // frequencies theta^(-2i/D) of the rotated pairs, in fp64
+    const __nv_bfloat16* w_k;
+    double rope_freq[64];
 };
 
 // Unpack 2 x bf16 (low half first) to fp32.
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// ---------------------------------------------------------------------------
+// Threads per CTA: NC consumer warps, the producer warp, and for the single K=V
+// cache a helper warp that prepares per-tile rotation angles.
+template <class Pol>
+constexpr int block_threads() {
+    return (Pol::NC + 1 + (Pol::kKeqV ? 1 : 0)) * 32;
+}
 
 // ---------------------------------------------------------------------------
 // Plan (shared memory): per-sequence ranges, static/dynamic split, prefix sums
@@ -164,7 +176,8 @@ struct SegmentParts {
 // What the producer publishes with every stage.
 struct TileDesc {
     int b, kvh;
-    int t;          // first cache position of the tile
+    int t;          // first cache row of the tile
+    int pos0;       // position held by that row
     int vlo, vhi;   // rows [vlo, vhi) of the tile are attended positions of this partial
     int slot;       // workspace slot of the partial
     int flags;
@@ -180,11 +193,13 @@ constexpr int kDescDone = 4;    // no more tiles: consumers leave
 template <class Pol>
 struct alignas(1024) KernelSmem {
     static constexpr int kTileBytes = Pol::TP * Pol::D * 2;
-    uint8_t kv[Pol::STAGES][2][kTileBytes];   // [stage][K, V][box][chunk][16 rows][128 B]
+    static constexpr int kTensors = Pol::kKeqV ? 1 : 2;   // K and V tiles, or the value tile only
+    uint8_t kv[Pol::STAGES][kTensors][kTileBytes];   // [stage][K, V][box][chunk][16 rows][128 B]
     alignas(8) uint64_t full[Pol::STAGES];
     alignas(8) uint64_t empty[Pol::STAGES];
     TileDesc desc[Pol::STAGES];
     alignas(8) uint64_t q_empty[2];           // q buffer free (consumer warps arrive)
+    alignas(8) uint64_t ready[Pol::STAGES];   // K=V: the stage's rotation angles are ready
     PlanSmem plan;
     // q of the next pieces (bf16, [G][D]), copied in by the producer with the
     // first tile of each piece; double-buffered over pieces
@@ -194,7 +209,7 @@ struct alignas(1024) KernelSmem {
     alignas(16) float acc[Pol::kDirectEpilogue ? 1 : Pol::G][Pol::kDirectEpilogue ? 4 : Pol::D];
     float m[Pol::G];
     float l[Pol::G];
-    alignas(16) typename Pol::Scratch scratch;
+    typename Pol::Scratch scratch;   // each policy aligns its own members (16 B or more)
     int abort_flag;
 };
 
@@ -449,7 +464,7 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
 // ---------------------------------------------------------------------------
 
 template <class Pol, bool kPaged>
-__global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
+__global__ void __launch_bounds__(block_threads<Pol>(), 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
     constexpr int G = Pol::G, D = Pol::D, TP = Pol::TP, STAGES = Pol::STAGES, NC = Pol::NC;
@@ -478,6 +493,8 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
         }
         ptx::mbar_init(ptx::smem_addr(&sm.q_empty[0]), NC);
         ptx::mbar_init(ptx::smem_addr(&sm.q_empty[1]), NC);
+        if (Pol::kKeqV)
+            for (int s = 0; s < STAGES; ++s) ptx::mbar_init(ptx::smem_addr(&sm.ready[s]), 1);
         ptx::fence_mbar_init();
         sm.abort_flag = 0;
     }
@@ -518,7 +535,8 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
     if (cta >= pl.g_eff) return;   // also covers an all-empty batch
 
     const uint32_t kv_base = ptx::smem_addr(&sm.kv[0][0][0]);
-    constexpr uint32_t kStageBytes = 2u * KernelSmem<Pol>::kTileBytes;
+    constexpr int kTensors = KernelSmem<Pol>::kTensors;
+    constexpr uint32_t kStageBytes = kTensors * KernelSmem<Pol>::kTileBytes;
 
     if (warp == NC) {
         // ================= producer: one thread walks the schedule =================
@@ -568,6 +586,7 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
                     d.b = b;
                     d.kvh = kvh;
                     d.t = row0;
+                    d.pos0 = t;
                     d.vlo = (a > t ? a : t) - t;
                     d.vhi = (e < t + TP ? e : t + TP) - t;
                     d.slot = slot;
@@ -577,14 +596,15 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
                     for (int j = 0; j < kBoxesPerTile; ++j) nbox += (t + j * kBoxRows < e) ? 1 : 0;
                     const uint32_t full_bar = ptx::smem_addr(&sm.full[s]);
                     ptx::mbar_arrive_expect_tx(full_bar,
-                                               static_cast<uint32_t>(nbox) * 2u * kBoxBytes +
+                                               static_cast<uint32_t>(nbox * kTensors) * kBoxBytes +
                                                    (first ? kQBytes : 0u));
                     if (first)
                         ptx::bulk_copy_g2s(ptx::smem_addr(&sm.q[qb][0]),
                                            p.q + (static_cast<size_t>(b) * H + kvh * G) * D,
                                            kQBytes, full_bar);
+                    // the value tile is the stage's last tensor
                     const uint32_t k_dst = kv_base + s * kStageBytes;
-                    const uint32_t v_dst = k_dst + KernelSmem<Pol>::kTileBytes;
+                    const uint32_t v_dst = k_dst + (kTensors - 1) * KernelSmem<Pol>::kTileBytes;
                     for (int j = 0; j < nbox; ++j) {
                         if (kPaged) {
                             int page = bt_row[(row0 >> 4) + j];
@@ -592,7 +612,8 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
                             // swizzled map: (elem, slot, chunk, page); plain map: (elem, kvh, slot, page)
                             const int c1 = Pol::kSwizzle128 ? 0 : kvh;
                             const int c2 = Pol::kSwizzle128 ? chunk0 : 0;
-                            ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, c1, c2, page, policy);
+                            if (!Pol::kKeqV)
+                                ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, c1, c2, page, policy);
                             ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, c1, c2, page, policy);
                         } else {
                             // rows past the end of the cache (a run's last tile) read as zeros
@@ -600,7 +621,8 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
                             // swizzled map: (elem, position, chunk, seq); plain map: (elem, kvh, position, seq)
                             const int c1 = Pol::kSwizzle128 ? row : kvh;
                             const int c2 = Pol::kSwizzle128 ? chunk0 : row;
-                            ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, c1, c2, b, policy);
+                            if (!Pol::kKeqV)
+                                ptx::tma_load_4d(k_dst + j * kBoxBytes, &tm_k, full_bar, 0, c1, c2, b, policy);
                             ptx::tma_load_4d(v_dst + j * kBoxBytes, &tm_v, full_bar, 0, c1, c2, b, policy);
                         }
                     }
@@ -666,8 +688,27 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
         return;
     }
 
+    if constexpr (Pol::kKeqV) {
+        if (warp == NC + 1) {
+            // ====== helper: the rotation angles of every tile, a few stages ahead ======
+            for (uint32_t t_idx = 0;; ++t_idx) {
+                const int s = t_idx % STAGES;
+                const uint32_t ph = (t_idx / STAGES) & 1u;
+                const bool ok = __all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&sm.full[s]), ph,
+                                                                    &sm.abort_flag, p.ws_flags));
+                if (!ok) return;
+                const TileDesc d = sm.desc[s];
+                if (!(d.flags & kDescDone)) Pol::tile_angles(sm.scratch, s, d.pos0, lane);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.ready[s]));
+                if (d.flags & kDescDone) return;
+            }
+        }
+    }
+
     // ===================== consumers: follow the descriptors =====================
     typename Pol::State st;
+    if constexpr (Pol::kKeqV) Pol::init(sm.scratch, p, tid);   // ends in a consumer barrier
     uint32_t t_idx = 0;
     uint32_t q_n = 0;   // pieces started (q buffer q_n & 1)
     bool bad = false;
@@ -675,7 +716,9 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
     while (true) {
         const int s = t_idx % STAGES;
         const uint32_t ph = (t_idx / STAGES) & 1u;
-        const bool ok = wait_bounded(ptx::smem_addr(&sm.full[s]), ph, &sm.abort_flag, p.ws_flags);
+        bool ok = wait_bounded(ptx::smem_addr(&sm.full[s]), ph, &sm.abort_flag, p.ws_flags);
+        if constexpr (Pol::kKeqV)
+            ok = ok && wait_bounded(ptx::smem_addr(&sm.ready[s]), ph, &sm.abort_flag, p.ws_flags);
         // all consumer warps take the same exit decision
         if (ptx::named_barrier_or(2, kConsumerThreads, !ok)) break;
         const TileDesc d = sm.desc[s];
@@ -683,7 +726,10 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
         if (d.flags & kDescFirst) {
             // q arrived with this tile; release the buffer once every lane has read it
             const uint32_t qb = q_n & 1u;
-            Pol::begin(st, &sm.q[qb][0], warp, lane);
+            if constexpr (Pol::kKeqV)
+                Pol::begin(st, &sm.q[qb][0], sm.scratch, warp, lane);
+            else
+                Pol::begin(st, &sm.q[qb][0], warp, lane);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.q_empty[qb]));
             ++q_n;
@@ -697,8 +743,11 @@ __global__ void __launch_bounds__((Pol::NC + 1) * 32, 1)
             }
         }
         const uint32_t k_tile = kv_base + s * kStageBytes;
-        const uint32_t v_tile = k_tile + KernelSmem<Pol>::kTileBytes;
-        Pol::tile(st, k_tile, v_tile, d.vlo, d.vhi, sm.scratch, t_idx, warp, lane);
+        const uint32_t v_tile = k_tile + (kTensors - 1) * KernelSmem<Pol>::kTileBytes;
+        if constexpr (Pol::kKeqV)
+            Pol::tile(st, v_tile, d.vlo, d.vhi, sm.scratch, t_idx, warp, lane);
+        else
+            Pol::tile(st, k_tile, v_tile, d.vlo, d.vhi, sm.scratch, t_idx, warp, lane);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.empty[s]));
         ++t_idx;

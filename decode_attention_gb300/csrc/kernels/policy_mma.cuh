@@ -43,6 +43,7 @@ struct MmaPolicy {
     // every warp holds the full running max/normaliser and its own slice of the
     // output, so results are stored straight from registers
     static constexpr bool kDirectEpilogue = true;
+    static constexpr bool kKeqV = false;   // separate K and V tiles
 
     struct Scratch {
         alignas(16) float S[2][2][G][kSStride];   // [tile parity][half of D][head][position]
@@ -120,7 +121,16 @@ struct MmaPolicy {
             if (gid < G) *reinterpret_cast<float2*>(&S[warp >> 2][gid][pos]) = make_float2(s0, s1);
         }
         ptx::named_barrier_sync(1, NC * 32);
+        softmax_pv(st, S, v_tile, vlo, vhi, warp, lane);
+    }
 
+    // Online softmax over the 32 half-score pairs of tile S (heads in rows 0..G-1),
+    // then P.V for this warp's D/8-wide slice of the output.  St holds acc, m, l.
+    template <class St>
+    __device__ static __forceinline__ void softmax_pv(St& st, const float (*S)[G][kSStride],
+                                                      uint32_t v_tile, int vlo, int vhi, int warp,
+                                                      int lane) {
+        const int gid = lane >> 2, t4 = lane & 3;
         // ---- online softmax over the 32 positions of head gid (rows >= G stay empty) ----
         float sv[2][4];
         const int hrow = gid < G ? gid : 0;
@@ -204,7 +214,8 @@ struct MmaPolicy {
     // The piece's result for head gid, dims [warp D/8, +D/8) of this warp: the
     // normalised output (slot < 0; the piece is the whole segment) or the partial
     // (acc, m, l) at workspace slot `slot`.  A bad page turns it into NaN.
-    __device__ static __forceinline__ void store(const State& st, const DecodeParams& p,
+    template <class St>
+    __device__ static __forceinline__ void store(const St& st, const DecodeParams& p,
                                                  size_t out_base, int slot, bool bad, int warp,
                                                  int lane) {
         const int gid = lane >> 2, t4 = lane & 3;

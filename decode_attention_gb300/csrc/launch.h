@@ -30,9 +30,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // shared-memory limit on first use on a device and launches one persistent grid.
 cudaError_t launch_sliding(const LaunchArgs& a, bool paged);
 cudaError_t launch_global(const LaunchArgs& a, bool paged);
+// decodeGQA over a single K=V cache: a.k and a.v are both the value cache.
+cudaError_t launch_global_keqv(const LaunchArgs& a, bool paged);
 
 // Bytes of dynamic shared memory each geometry's kernel requests.
 size_t smem_bytes_sliding();
 size_t smem_bytes_global();
+size_t smem_bytes_global_keqv();
 
 }  // namespace gqa

@@ -75,7 +75,7 @@ cudaError_t launch_decode(const LaunchArgs& a) {
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.grid));
-    cfg.blockDim = dim3((Pol::NC + 1) * 32);
+    cfg.blockDim = dim3(block_threads<Pol>());
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = a.stream;
     cfg.attrs = pdl;

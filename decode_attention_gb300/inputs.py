@@ -35,7 +35,7 @@ PAGE_SIZE = 16                                    # "Shape domain" row of "At a 
 _RMS_EPS = 1e-6
 _CHUNK_ELEMS = 1 << 27
 
-_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "k_pages": 4, "v_pages": 5}
+_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "k_pages": 4, "v_pages": 5, "w_k": 6}
 
 
 def rms_normalised_bf16(shape, seed: int, device="cpu") -> torch.Tensor:
@@ -56,6 +56,15 @@ def rms_normalised_bf16(shape, seed: int, device="cpu") -> torch.Tensor:
         x = x * torch.rsqrt(x.square().mean(dim=-1, keepdim=True) + _RMS_EPS)
         flat[r0:r1].copy_(x)
     return out
+
+
+def k_norm_weight_bf16(D: int, seed: int, device="cpu") -> torch.Tensor:
+    """Synthetic k_norm weight [D] (bf16): 1 + 0.25 * N(0, 1), a learned per-channel
+    scale around 1 (the checkpoint's values are not available)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    x = torch.randn((D,), generator=gen, device=device, dtype=torch.float32)
+    return (1.0 + 0.25 * x).to(torch.bfloat16)
 
 
 def tensor_seed(seed: int, name: str) -> int:
@@ -103,6 +112,7 @@ class Workload:
     layers: tuple = ()       # ("sliding",) / ("global",) / ("sliding", "global")
     paged: bool = False
     rings: tuple = ()        # windows of ring-cache sliding calls (ring length = window)
+    keqv: bool = False       # global layer over a single K=V cache (values only)
 
     def seq_lens(self) -> np.ndarray:
         return self.lengths(np.random.default_rng(self.seed))
@@ -131,6 +141,14 @@ WORKLOADS = {
                  "on [1, 32768]; four ring-cache calls, windows 1024/2048/4096/8192",
                  B=64, S=32768, seed=6, lengths=lengths_uniform(1, 32768, 64),
                  layers=("sliding",), rings=(1024, 2048, 4096, 8192)),
+        # The long-context global shape over a single K=V cache: keys derived from the
+        # cached values in the kernel (Model Spec "What to watch for": values = keys).
+        Workload("global_keqv_b16_s131072", "decodeGQA long context over a single K=V cache, "
+                 "B=16, seq_lens uniform on [65536, 131072]", B=16, S=131072, seed=7,
+                 lengths=lengths_uniform(65536, 131072, 16), layers=("global",), keqv=True),
+        Workload("global_keqv_b8_s8192", "decodeGQA over a single K=V cache, B=8, seq_lens "
+                 "uniform on [1, 8192]", B=8, S=8192, seed=8, lengths=lengths_uniform(1, 8192, 8),
+                 layers=("global",), keqv=True),
         # Smaller instance of the batched sliding shape for profiler captures: the same
         # bytes per call as sliding_b64_s32768 (every sequence reads its full 1024-position
         # window) with a 2 GB cache instead of 34 GB.
@@ -148,6 +166,19 @@ def geometry(layer: str) -> dict:
 # ----------------------------------------------------------------------------
 # Case builders
 # ----------------------------------------------------------------------------
+
+def keqv_case(B: int, S: int, H: int, KVH: int, D: int, seq_lens, seed: int,
+              device="cpu") -> dict:
+    """q [B,H,D], the value cache v [B,S,KVH,D], k_norm weight w_k [D] (bf16) and
+    seq_lens [B]: a single K=V cache (no k tensor)."""
+    lens = torch.as_tensor(np.asarray(seq_lens, dtype=np.int32), device=device)
+    return dict(
+        q=rms_normalised_bf16((B, H, D), tensor_seed(seed, "q"), device),
+        v=rms_normalised_bf16((B, S, KVH, D), tensor_seed(seed, "v"), device),
+        w_k=k_norm_weight_bf16(D, tensor_seed(seed, "w_k"), device),
+        seq_lens=lens,
+    )
+
 
 def contiguous_case(B: int, S: int, H: int, KVH: int, D: int, seq_lens, seed: int,
                     device="cpu") -> dict:

@@ -219,6 +219,41 @@ gqa_status_t gqa_decode_ring(const void *q, const void *k, const void *v,
                              size_t workspace_bytes, gqa_stream_t stream);
 
 /*
+ * decodeGQA over a single K=V cache: only the values are cached, and the kernel
+ * derives each key from its value.  On the global layers keys and values come
+ * from the same projection (gemma-4-31B Model Spec, "What to watch for": values
+ * = keys; "Gemma 4 31B-it Text Architecture", decoder listing: V = v_norm(K_raw),
+ * K = rope(k_norm(K_raw))).  Both norms divide K_raw by the same root mean
+ * square, so the key of the cached value row v at position s is
+ *     k = rope(w_k * v, s)
+ * with the global layers' rope (Model Spec, `attn.rope` row for layers 5, 11,
+ * ..., 59): the pairs (i, i + 256), i < 64, rotated by s * 1e6^(-2i/512),
+ * k[i] = x[i] cos - x[i+256] sin, k[i+256] = x[i+256] cos + x[i] sin, every other
+ * coordinate unchanged.  Then the attention core is decodeGQA's, full history.
+ * Reads half the bytes of separate K and V caches.
+ *
+ *   q          bf16 [B, 32, 512] (already normed and rotated at its position)
+ *   v          bf16 [B, S, 4, 512] contiguous; row s is position s
+ *   v_pages    bf16 [P, 16, 4, 512] (paged form); position s of sequence b is
+ *              slot s % 16 of page block_table[b][s / 16]
+ *   w_k        bf16 [512], the layer's k_norm weight (device memory)
+ * Only the decodeGQA geometry (H = 32, KVH = 4, D = 512) is accepted; the
+ * slidingDecodeGQA geometry returns GQA_ERR_UNSUPPORTED (its layers project
+ * separate values).  Everything else is as for gqa_decode / gqa_decode_paged
+ * with window = 0.
+ */
+gqa_status_t gqa_decode_keqv(const void *q, const void *v, const void *w_k,
+                             const int32_t *seq_lens, int B, int S, int H, int KVH, int D,
+                             void *out, gqa_out_dtype_t out_dtype, void *workspace,
+                             size_t workspace_bytes, gqa_stream_t stream);
+
+gqa_status_t gqa_decode_keqv_paged(const void *q, const void *v_pages, const void *w_k,
+                                   const int32_t *block_table, const int32_t *seq_lens, int B,
+                                   int P, int max_pages, int page_size, int H, int KVH, int D,
+                                   void *out, gqa_out_dtype_t out_dtype, void *workspace,
+                                   size_t workspace_bytes, gqa_stream_t stream);
+
+/*
  * Host-side check of the device-resident inputs, for tests and debugging: the
  * caller copies seq_lens (and the block table) to host memory and passes them
  * here.  The decode calls never read these arrays on the host (they stay on the

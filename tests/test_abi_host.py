@@ -200,3 +200,21 @@ def test_ring_argument_checks(lib):
         gqa.GQA_ERR_UNSUPPORTED
     assert lib.gqa_decode_ring(None, None, None, None, 0, 1024, H, KVH, D, 1024, None, 1, None, 0,
                                None) == gqa.GQA_OK
+
+
+def test_keqv_argument_checks(lib):
+    F = FAKE
+    H, KVH, D = GLOBAL
+    # values = keys only on the global geometry
+    assert lib.gqa_decode_keqv(F, F, F, F, 2, 64, *SLIDING, F, 1, None, 0, None) == \
+        gqa.GQA_ERR_UNSUPPORTED
+    assert lib.gqa_decode_keqv(F, F, None, F, 2, 64, H, KVH, D, F, 1, None, 0, None) == \
+        gqa.GQA_ERR_INVALID_ARGUMENT
+    assert lib.gqa_decode_keqv(F, F, F, F, 2, 0, H, KVH, D, F, 1, None, 0, None) == \
+        gqa.GQA_ERR_INVALID_ARGUMENT
+    assert lib.gqa_decode_keqv(None, None, None, None, 0, 64, H, KVH, D, None, 1, None, 0,
+                               None) == gqa.GQA_OK
+    assert lib.gqa_decode_keqv_paged(F, F, F, F, F, 2, 4, 4, 8, H, KVH, D, F, 1, None, 0, None) == \
+        gqa.GQA_ERR_INVALID_ARGUMENT   # page size must be 16
+    assert lib.gqa_decode_keqv_paged(F, F, F, F, F, 2, 4, 4, 16, *SLIDING, F, 1, None, 0, None) == \
+        gqa.GQA_ERR_UNSUPPORTED

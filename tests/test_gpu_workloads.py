@@ -18,7 +18,8 @@ if not torch.cuda.is_available():
 import decode_attention_gb300 as gqa  # noqa: E402
 
 WORKLOADS = ["sliding_b1_s2048", "global_b8_s8192", "sliding_b64_s32768",
-             "global_b16_s131072", "paged_mixed_b256", "retrofit_block_b64"]
+             "global_b16_s131072", "paged_mixed_b256", "retrofit_block_b64",
+             "global_keqv_b16_s131072"]
 
 
 def sampled(lens, k=3, seed=0):
