@@ -58,6 +58,9 @@ def _bind(path: str):
     lib.oracle_gqa_decode_keqv_f64.argtypes = [u16p, u16p, u16p, i32p, ci, ci, ci, ci, ci, ci,
                                                ci, ctypes.c_double, ci, f64p]
     lib.oracle_gqa_decode_keqv_f64.restype = ci
+    lib.oracle_prepare_decode_f64.argtypes = [u16p, u16p, u16p, u16p, u16p, i32p, ci, ci, ci, ci,
+                                              ci, ctypes.c_double, f64p, f64p, f64p]
+    lib.oracle_prepare_decode_f64.restype = ci
     lib.oracle_default_threads.argtypes = []
     lib.oracle_default_threads.restype = ci
     return lib
@@ -204,6 +207,41 @@ def gqa_decode_keqv_f64(q: np.ndarray, v: np.ndarray, w_k: np.ndarray, seq_lens,
     return out
 
 
+# RoPE of the sliding layers (Model Spec, `attn.rope` row for the other 50 layers)
+SLIDING_ROPE_PAIRS = 128
+SLIDING_ROPE_THETA = 1.0e4
+
+
+def prepare_decode_f64(q_raw: np.ndarray, k_raw: np.ndarray, v_raw, w_q: np.ndarray,
+                       w_k: np.ndarray, seq_lens, n_rot: int, theta: float,
+                       _lib_override=None):
+    """The decode-step producer for one new token per sequence, exact up to fp64.
+
+    q_raw [B, H, D], k_raw [B, KVH, D], v_raw [B, KVH, D] or None (values = keys),
+    w_q, w_k [D]: uint16 bf16 bits.  Returns (q, k, v) float64: q = rope(q_norm(q_raw)),
+    k = rope(k_norm(k_raw)), v = v_norm(v_raw or k_raw), at position seq_lens[b] - 1
+    (NaN where seq_lens[b] < 1).
+    """
+    q_raw, k_raw, w_q, w_k = _u16(q_raw), _u16(k_raw), _u16(w_q), _u16(w_k)
+    B, H, D = q_raw.shape
+    _, KVH, _ = k_raw.shape
+    if v_raw is not None:
+        v_raw = _u16(v_raw)
+        if v_raw.shape != k_raw.shape:
+            raise ValueError("v_raw must match k_raw")
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    q = np.zeros((B, H, D)); k = np.zeros((B, KVH, D)); v = np.zeros((B, KVH, D))
+    lib = _lib_override if _lib_override is not None else _load()
+    rc = lib.oracle_prepare_decode_f64(
+        _ptr(q_raw, ctypes.c_uint16), _ptr(k_raw, ctypes.c_uint16),
+        None if v_raw is None else _ptr(v_raw, ctypes.c_uint16), _ptr(w_q, ctypes.c_uint16),
+        _ptr(w_k, ctypes.c_uint16), _ptr(lens, ctypes.c_int32), B, H, KVH, D, int(n_rot),
+        float(theta), _ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return q, k, v
+
+
 class OracleLibrary:
     """The oracle API bound to a specific compiled copy of the C source.
 
@@ -225,6 +263,9 @@ class OracleLibrary:
 
     def gqa_decode_keqv_f64(self, *args, **kw):
         return gqa_decode_keqv_f64(*args, _lib_override=self._lib, **kw)
+
+    def prepare_decode_f64(self, *args, **kw):
+        return prepare_decode_f64(*args, _lib_override=self._lib, **kw)
 
 
 def compile_variant(source_text: str, out_path: str) -> str:

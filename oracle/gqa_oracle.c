@@ -528,3 +528,87 @@ int oracle_gqa_decode_keqv_f64(const uint16_t *q, const uint16_t *v, const uint1
     (void)nthreads;
     return err;
 }
+
+/* ---- decode-step producer: the nodes ahead of attn.core for one new token per
+ *      sequence ("Gemma 4 31B-it Text Architecture", decoder listing: Q =
+ *      rope(q_norm(Q)), K = rope(k_norm(K_raw)), V = v_norm(V_raw), with V_raw =
+ *      K_raw on global layers; the new K/V are appended before attention).
+ *      Model Spec rows: attn.qk_norm (per head, x / sqrt(mean x^2 + eps) * w),
+ *      attn.v_norm (the same without a weight), eps 1e-6; attn.rope (pairs
+ *      (i, i + D/2), i < n_rot, rotated by pos * theta^(-2i/D)).  The token's
+ *      position is L - 1, L = seq_lens[b] counting the new token. ---- */
+
+#define PRODUCER_EPS 1e-6
+
+/* per-head RMS norm of D bf16 values; w = NULL for the unit (weightless) form */
+static void rms_norm_head(const uint16_t *x, const uint16_t *w, int D, double *y)
+{
+    int d;
+    double ss = 0.0;
+    for (d = 0; d < D; ++d) {
+        const double v = bf16_bits_to_double(x[d]);
+        ss += v * v;
+    }
+    const double inv = 1.0 / sqrt(ss / (double)D + PRODUCER_EPS);
+    for (d = 0; d < D; ++d) {
+        y[d] = bf16_bits_to_double(x[d]) * inv;
+        if (w) y[d] *= bf16_bits_to_double(w[d]);
+    }
+}
+
+/* rotate the pairs (i, i + D/2), i < n_rot, by pos * theta^(-2i/D), in place */
+static void rope_head(double *y, int D, int n_rot, double theta, int64_t pos)
+{
+    int i;
+    const int half = D / 2;
+    for (i = 0; i < n_rot; ++i) {
+        const double a = (double)pos * pow(theta, -2.0 * (double)i / (double)D);
+        const double c = cos(a), s = sin(a);
+        const double x0 = y[i], x1 = y[i + half];
+        y[i] = x0 * c - x1 * s;
+        y[i + half] = x1 * c + x0 * s;
+    }
+}
+
+/*
+ * q_raw [B, H, D], k_raw [B, KVH, D], v_raw [B, KVH, D] or NULL (values = keys:
+ * v = v_norm(k_raw)), w_q and w_k [D]: bf16 bits.  seq_lens [B]: lengths after the
+ * append.  Outputs, in doubles: q_out [B, H, D], k_out and v_out [B, KVH, D].
+ * Sequences with L < 1 have no new token: their outputs are NaN.
+ */
+int oracle_prepare_decode_f64(const uint16_t *q_raw, const uint16_t *k_raw, const uint16_t *v_raw,
+                              const uint16_t *w_q, const uint16_t *w_k, const int32_t *seq_lens,
+                              int B, int H, int KVH, int D, int n_rot, double theta,
+                              double *q_out, double *k_out, double *v_out)
+{
+    int b, h, d;
+    if (B < 0 || H <= 0 || KVH <= 0 || D <= 0 || D % 2 != 0 || n_rot < 0 || n_rot > D / 2 ||
+        !(theta > 0.0))
+        return ORACLE_EINVAL;
+    for (b = 0; b < B; ++b) {
+        const int64_t pos = (int64_t)seq_lens[b] - 1;
+        for (h = 0; h < H; ++h) {
+            double *y = q_out + ((int64_t)b * H + h) * D;
+            if (pos < 0) {
+                for (d = 0; d < D; ++d) y[d] = NAN;
+                continue;
+            }
+            rms_norm_head(q_raw + ((int64_t)b * H + h) * D, w_q, D, y);
+            rope_head(y, D, n_rot, theta, pos);
+        }
+        for (h = 0; h < KVH; ++h) {
+            double *yk = k_out + ((int64_t)b * KVH + h) * D;
+            double *yv = v_out + ((int64_t)b * KVH + h) * D;
+            const uint16_t *kr = k_raw + ((int64_t)b * KVH + h) * D;
+            const uint16_t *vr = v_raw ? v_raw + ((int64_t)b * KVH + h) * D : kr;
+            if (pos < 0) {
+                for (d = 0; d < D; ++d) yk[d] = yv[d] = NAN;
+                continue;
+            }
+            rms_norm_head(kr, w_k, D, yk);
+            rope_head(yk, D, n_rot, theta, pos);
+            rms_norm_head(vr, NULL, D, yv);
+        }
+    }
+    return ORACLE_OK;
+}

@@ -69,8 +69,11 @@ MUTANTS = {
         "attend(q_row, D, hi - lo, ring_k",
         "attend(q_row, D, hi - lo - (hi - lo > 1), ring_k"),
     "keqv_frequency_exponent": (
-        "pow(theta, -2.0 * (double)i / (double)D)",
-        "pow(theta, -2.0 * (double)i / (double)(D / 2))"),
+        "(double)s * pow(theta, -2.0 * (double)i / (double)D)",
+        "(double)s * pow(theta, -2.0 * (double)i / (double)(D / 2))"),
+    "producer_frequency_exponent": (
+        "(double)pos * pow(theta, -2.0 * (double)i / (double)D)",
+        "(double)pos * pow(theta, -2.0 * (double)i / (double)(D / 2))"),
     "keqv_sine_sign": (
         "k[i] = x0 * c - x1 * sn;",
         "k[i] = x0 * c + x1 * sn;"),
@@ -83,6 +86,27 @@ MUTANTS = {
     "keqv_weight_ignored": (
         "for (d = 0; d < D; ++d) k[d] = w[d] * bf16_bits_to_double(vr[d]);",
         "for (d = 0; d < D; ++d) k[d] = bf16_bits_to_double(vr[d]);"),
+    "producer_eps_outside_root": (
+        "1.0 / sqrt(ss / (double)D + PRODUCER_EPS);",
+        "1.0 / (sqrt(ss / (double)D) + PRODUCER_EPS);"),
+    "producer_norm_over_d_minus_1": (
+        "1.0 / sqrt(ss / (double)D + PRODUCER_EPS);",
+        "1.0 / sqrt(ss / (double)(D - 1) + PRODUCER_EPS);"),
+    "producer_weight_ignored": (
+        "        if (w) y[d] *= bf16_bits_to_double(w[d]);\n",
+        "\n"),
+    "producer_position_is_length": (
+        "const int64_t pos = (int64_t)seq_lens[b] - 1;",
+        "const int64_t pos = (int64_t)seq_lens[b];"),
+    "producer_rope_pair_offset": (
+        "    const int half = D / 2;\n    for (i = 0; i < n_rot; ++i) {\n        const double a = (double)pos",
+        "    const int half = D / 2 - 1;\n    for (i = 0; i < n_rot; ++i) {\n        const double a = (double)pos"),
+    "producer_rope_sign": (
+        "        y[i] = x0 * c - x1 * s;",
+        "        y[i] = x0 * c + x1 * s;"),
+    "producer_value_weighted": (
+        "            rms_norm_head(vr, NULL, D, yv);",
+        "            rms_norm_head(vr, w_k, D, yv);"),
     "empty_range_not_zero": (
         "if (n <= 0) return; /* empty sum */",
         "if (n <= 0) { for (d = 0; d < D; ++d) out[d] = 1.0; return; }"),

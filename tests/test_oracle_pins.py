@@ -506,6 +506,87 @@ def test_keqv_unrotated_dims_equal_plain_keys(oracle_lib):
     assert np.array_equal(keqv, plain)
 
 
+# ---------------------------------------------------------------------------
+# decode-step producer: q = rope(q_norm(q_raw)), k = rope(k_norm(k_raw)),
+# v = v_norm(v_raw) at position L - 1 (Model Spec rows attn.qk_norm, attn.v_norm,
+# attn.rope; decoder listing of the architecture page)
+# ---------------------------------------------------------------------------
+
+PRODUCER_GEOMS = [(32, 16, 256, 128, 1.0e4), (32, 4, 512, 64, 1.0e6), (4, 2, 16, 3, 50.0)]
+
+
+def producer_case(B, H, KVH, D, seed):
+    rng = np.random.default_rng(seed)
+    scale = rng.uniform(0.2, 5.0, size=(B, H, 1))       # raw projections: arbitrary scales
+    q = to_bits(rng.standard_normal((B, H, D)) * scale)
+    k = to_bits(rng.standard_normal((B, KVH, D)) * scale[:, :KVH])
+    v = to_bits(rng.standard_normal((B, KVH, D)) * 2.0)
+    w_q = to_bits(1.0 + 0.25 * rng.standard_normal(D))
+    w_k = to_bits(1.0 + 0.25 * rng.standard_normal(D))
+    return q, k, v, w_q, w_k
+
+
+def test_producer_constant_heads_closed_form(oracle_lib):
+    """At position 0 (L = 1) nothing rotates: a head of constant c normalises to
+    c / sqrt(c^2 + 1e-6), times the weight for q and k."""
+    H, KVH, D = 4, 2, 8
+    c = np.array([0.5, -2.0, 3.0, 1.0])
+    q = exact_bits(np.broadcast_to(c[None, :, None], (1, H, D)))
+    k = exact_bits(np.broadcast_to(c[None, :KVH, None], (1, KVH, D)))
+    w = exact_bits(np.array([1.0, 2.0, 0.5, 1.5, 1.0, 0.25, 4.0, 1.0]))
+    qo, ko, vo = oracle_lib.prepare_decode_f64(q, k, k, w, w, [1], 3, 10.0)
+    f = c / np.sqrt(c * c + 1e-6)
+    np.testing.assert_allclose(qo[0], f[:, None] * to_vals(w)[None, :], rtol=1e-14)
+    np.testing.assert_allclose(ko[0], f[:KVH, None] * to_vals(w)[None, :], rtol=1e-14)
+    np.testing.assert_allclose(vo[0], np.broadcast_to(f[:KVH, None], (KVH, D)), rtol=1e-14)
+
+
+@pytest.mark.parametrize("H,KVH,D,n_rot,theta", PRODUCER_GEOMS)
+def test_producer_torch_rms_norm_and_complex_rope(oracle_lib, H, KVH, D, n_rot, theta):
+    """torch's rms_norm in float64, then the complex-exponential rotation."""
+    B = 3
+    q, k, v, w_q, w_k = producer_case(B, H, KVH, D, seed=30 + D)
+    lens = [1, 77, 131075]
+    qo, ko, vo = oracle_lib.prepare_decode_f64(q, k, v, w_q, w_k, lens, n_rot, theta)
+    F = torch.nn.functional
+    qn = F.rms_norm(torch.from_numpy(to_vals(q)), (D,), torch.from_numpy(to_vals(w_q)), 1e-6).numpy()
+    kn = F.rms_norm(torch.from_numpy(to_vals(k)), (D,), torch.from_numpy(to_vals(w_k)), 1e-6).numpy()
+    vn = F.rms_norm(torch.from_numpy(to_vals(v)), (D,), None, 1e-6).numpy()
+    ones = np.ones(D)
+    for b, L in enumerate(lens):
+        # at position ~1.3e5 the fp64 angle itself carries ~1e-11 rad of rounding
+        q_ref = complex_rope_keys(qn[b][None], ones, [L - 1], n_rot, theta)[0]
+        k_ref = complex_rope_keys(kn[b][None], ones, [L - 1], n_rot, theta)[0]
+        np.testing.assert_allclose(qo[b], q_ref, rtol=1e-9, atol=1e-9)
+        np.testing.assert_allclose(ko[b], k_ref, rtol=1e-9, atol=1e-9)
+        np.testing.assert_allclose(vo[b], vn[b], rtol=1e-13, atol=1e-15)
+
+
+def test_producer_rotation_keeps_same_position_dot_products(oracle_lib):
+    """q and k of one token share the position, and the rotation is orthogonal:
+    <q, k> per query head and its KV head does not depend on the position."""
+    H, KVH, D = 32, 4, 512
+    q, k, v, w_q, w_k = producer_case(1, H, KVH, D, seed=31)
+    ref_q, ref_k, _ = oracle_lib.prepare_decode_f64(q, k, v, w_q, w_k, [1], 64, 1.0e6)
+    ref = np.einsum("hd,hd->h", ref_q[0], np.repeat(ref_k[0], H // KVH, axis=0))
+    for L in (2, 1000, 65537, 262144):
+        q2 = np.repeat(q, 1, axis=0)
+        qo, ko, _ = oracle_lib.prepare_decode_f64(q2, k, v, w_q, w_k, [L], 64, 1.0e6)
+        dots = np.einsum("hd,hd->h", qo[0], np.repeat(ko[0], H // KVH, axis=0))
+        np.testing.assert_allclose(dots, ref, rtol=1e-9, atol=1e-9)
+        assert np.max(np.abs(qo[0] - ref_q[0])) > 1e-3   # and the vectors did move
+
+
+def test_producer_values_equal_keys_form(oracle_lib):
+    """Without v_raw (global layers) the value is v_norm(k_raw)."""
+    q, k, v, w_q, w_k = producer_case(2, 32, 4, 512, seed=32)
+    a = oracle_lib.prepare_decode_f64(q, k, None, w_q, w_k, [5, 9], 64, 1.0e6)
+    b = oracle_lib.prepare_decode_f64(q, k, k, w_q, w_k, [5, 9], 64, 1.0e6)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    assert np.all(np.isnan(oracle_lib.prepare_decode_f64(q, k, v, w_q, w_k, [0, 3], 64, 1e6)[0][0]))
+
+
 def test_oracle_rejects_ranges_outside_the_cache(oracle_lib):
     q, k, v = random_case(1, 8, 4, 2, 8, seed=16)
     with pytest.raises(ValueError):
