@@ -26,6 +26,8 @@ from ._native import (  # noqa: F401
     gqa_decode_keqv,
     gqa_decode_keqv_paged,
     gqa_decode_noalloc,
+    gqa_prepare_decode,
+    gqa_prepare_decode_paged,
     gqa_decode_ring,
     gqa_decode_paged,
     gqa_check_inputs_host,

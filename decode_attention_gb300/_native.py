@@ -33,7 +33,8 @@ PAGE_SIZE = 16
 
 EXPORTED_SYMBOLS = ("gqa_workspace_size", "gqa_workspace_init", "gqa_decode", "gqa_decode_paged",
                     "gqa_device_status", "gqa_decode_noalloc", "gqa_decode_ring",
-                    "gqa_decode_keqv", "gqa_decode_keqv_paged",
+                    "gqa_decode_keqv", "gqa_decode_keqv_paged", "gqa_prepare_decode",
+                    "gqa_prepare_decode_paged",
                     "gqa_check_inputs_host",
                     "gqa_status_string")
 
@@ -83,6 +84,12 @@ def load_library(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.gqa_decode_keqv_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp,
                                               ci, vp, sz, vp]
         lib.gqa_decode_keqv_paged.restype = ci
+        lib.gqa_prepare_decode.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, vp, ci,
+                                           ci, vp]
+        lib.gqa_prepare_decode.restype = ci
+        lib.gqa_prepare_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
+                                                 ci, vp, vp, vp, vp]
+        lib.gqa_prepare_decode_paged.restype = ci
         lib.gqa_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gqa_device_status.restype = ci
         lib.gqa_check_inputs_host.argtypes = [vp, ci, ci, ci, vp, ci, ci, ctypes.POINTER(ci)]
@@ -281,6 +288,61 @@ def gqa_decode_keqv_paged(q: torch.Tensor, v_pages: torch.Tensor, w_k: torch.Ten
         ws_bytes, _stream_handle(stream, q.device))
     _check("gqa_decode_keqv_paged", st)
     return out
+
+
+def gqa_prepare_decode(q_raw: torch.Tensor, k_raw: torch.Tensor, v_raw, w_q: torch.Tensor,
+                       w_k: torch.Tensor, seq_lens: torch.Tensor, q_out: torch.Tensor,
+                       k_cache, v_cache: torch.Tensor, ring: bool = False, stream=None):
+    """Decode-step producer: q_out = rope(q_norm(q_raw)); appends rope(k_norm(k_raw)) and
+    v_norm(v_raw) (v_norm(k_raw) when v_raw is None, values = keys; k_cache unused) at
+    position seq_lens[b] - 1 of a contiguous cache [B, rows, KVH, D] (row (L-1) % rows
+    when ring)."""
+    _check_tensor("q_raw", q_raw, torch.bfloat16, 3)
+    _check_tensor("k_raw", k_raw, torch.bfloat16, 3)
+    if v_raw is not None:
+        _check_tensor("v_raw", v_raw, torch.bfloat16, 3)
+    _check_tensor("w_q", w_q, torch.bfloat16, 1)
+    _check_tensor("w_k", w_k, torch.bfloat16, 1)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    _check_tensor("q_out", q_out, torch.bfloat16, 3)
+    _check_tensor("v_cache", v_cache, torch.bfloat16, 4)
+    if k_cache is not None:
+        _check_tensor("k_cache", k_cache, torch.bfloat16, 4)
+    B, H, D = q_raw.shape
+    KVH = k_raw.shape[1]
+    _require(tuple(v_cache.shape[2:]) == (KVH, D) and v_cache.shape[0] == B, "cache shape mismatch")
+    _require(q_out.shape == q_raw.shape, "q_out must match q_raw")
+    st = load_library().gqa_prepare_decode(
+        _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(w_q), _ptr(w_k), _ptr(seq_lens), B, H, KVH, D,
+        _ptr(q_out), _ptr(k_cache), _ptr(v_cache), v_cache.shape[1], 1 if ring else 0,
+        _stream_handle(stream, q_raw.device))
+    _check("gqa_prepare_decode", st)
+
+
+def gqa_prepare_decode_paged(q_raw: torch.Tensor, k_raw: torch.Tensor, v_raw, w_q: torch.Tensor,
+                             w_k: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                             q_out: torch.Tensor, k_pages, v_pages: torch.Tensor, stream=None):
+    """gqa_prepare_decode into page pools [P, 16, KVH, D] through a block table."""
+    _check_tensor("q_raw", q_raw, torch.bfloat16, 3)
+    _check_tensor("k_raw", k_raw, torch.bfloat16, 3)
+    if v_raw is not None:
+        _check_tensor("v_raw", v_raw, torch.bfloat16, 3)
+    _check_tensor("w_q", w_q, torch.bfloat16, 1)
+    _check_tensor("w_k", w_k, torch.bfloat16, 1)
+    _check_tensor("block_table", block_table, torch.int32, 2)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    _check_tensor("q_out", q_out, torch.bfloat16, 3)
+    _check_tensor("v_pages", v_pages, torch.bfloat16, 4)
+    if k_pages is not None:
+        _check_tensor("k_pages", k_pages, torch.bfloat16, 4)
+    B, H, D = q_raw.shape
+    KVH = k_raw.shape[1]
+    P, page_size = v_pages.shape[0], v_pages.shape[1]
+    st = load_library().gqa_prepare_decode_paged(
+        _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(w_q), _ptr(w_k), _ptr(block_table),
+        _ptr(seq_lens), B, P, block_table.shape[1], page_size, H, KVH, D, _ptr(q_out),
+        _ptr(k_pages), _ptr(v_pages), _stream_handle(stream, q_raw.device))
+    _check("gqa_prepare_decode_paged", st)
 
 
 def gqa_decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,

@@ -113,6 +113,7 @@ class Workload:
     paged: bool = False
     rings: tuple = ()        # windows of ring-cache sliding calls (ring length = window)
     keqv: bool = False       # global layer over a single K=V cache (values only)
+    step: bool = False       # each ring call is preceded by the decode-step producer
 
     def seq_lens(self) -> np.ndarray:
         return self.lengths(np.random.default_rng(self.seed))
@@ -141,6 +142,14 @@ WORKLOADS = {
                  "on [1, 32768]; four ring-cache calls, windows 1024/2048/4096/8192",
                  B=64, S=32768, seed=6, lengths=lengths_uniform(1, 32768, 64),
                  layers=("sliding",), rings=(1024, 2048, 4096, 8192)),
+        # One sliding layer's decode step: the producer (norms, rope, append at L - 1)
+        # then the attention core over a window-capped ring, at the batched sliding
+        # shape's lengths.
+        Workload("sliding_step_b64", "sliding layer decode step, B=64, seq_lens uniform on "
+                 "[1, 32768]: producer (q/k/v norms, rope, ring append) then the attention core "
+                 "over a 1024-row ring", B=64, S=32768, seed=9,
+                 lengths=lengths_uniform(1, 32768, 64), layers=("sliding",), rings=(1024,),
+                 step=True),
         # The long-context global shape over a single K=V cache: keys derived from the
         # cached values in the kernel (Model Spec "What to watch for": values = keys).
         Workload("global_keqv_b16_s131072", "decodeGQA long context over a single K=V cache, "
@@ -166,6 +175,20 @@ def geometry(layer: str) -> dict:
 # ----------------------------------------------------------------------------
 # Case builders
 # ----------------------------------------------------------------------------
+
+def raw_projections(B: int, H: int, KVH: int, D: int, seed: int, device="cpu") -> dict:
+    """Synthetic projection outputs for the decode-step producer: q_raw [B,H,D],
+    k_raw, v_raw [B,KVH,D] drawn N(0,1) times a per-head scale in [0.2, 5.2), and
+    the q_norm / k_norm weights [D]."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed) * 16 + 7)
+    scale = 0.2 + 5.0 * torch.rand((B, H, 1), generator=gen, device=device)
+    q = (torch.randn((B, H, D), generator=gen, device=device) * scale).to(torch.bfloat16)
+    k = (torch.randn((B, KVH, D), generator=gen, device=device) * scale[:, :KVH]).to(torch.bfloat16)
+    v = (torch.randn((B, KVH, D), generator=gen, device=device) * 2.0).to(torch.bfloat16)
+    return dict(q_raw=q, k_raw=k, v_raw=v, w_q=k_norm_weight_bf16(D, int(seed) * 16 + 8, device),
+                w_k=k_norm_weight_bf16(D, int(seed) * 16 + 9, device))
+
 
 def keqv_case(B: int, S: int, H: int, KVH: int, D: int, seq_lens, seed: int,
               device="cpu") -> dict:

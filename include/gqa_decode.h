@@ -254,6 +254,51 @@ gqa_status_t gqa_decode_keqv_paged(const void *q, const void *v_pages, const voi
                                    size_t workspace_bytes, gqa_stream_t stream);
 
 /*
+ * Decode-step producer: the nodes ahead of the attention core, fused, for one new
+ * token per sequence.  "Gemma 4 31B-it Text Architecture", decoder listing:
+ * Q = rope(q_norm(Q)), K = rope(k_norm(K_raw)), V = v_norm(V_raw) with V_raw =
+ * K_raw on the global layers, and the new K/V appended to the cache before
+ * attention.  gemma-4-31B Model Spec rows: attn.qk_norm (per head
+ * x / sqrt(mean(x^2) + 1e-6) * w), attn.v_norm (the same without w), attn.rope
+ * (pairs (i, i + D/2) rotated by pos * theta^(-2i/D): 128 pairs, theta 1e4 on
+ * slidingDecodeGQA layers; 64 pairs, theta 1e6 on decodeGQA layers).
+ *
+ *   q_raw     bf16 [B, H, D]        projections of the new token (device)
+ *   k_raw     bf16 [B, KVH, D]
+ *   v_raw     bf16 [B, KVH, D], or NULL on a global layer with one K=V cache:
+ *             then v = v_norm(k_raw) is written to v_cache and k_cache is unused
+ *             (gqa_decode_keqv derives the keys)
+ *   w_q, w_k  bf16 [D], the q_norm and k_norm weights
+ *   seq_lens  int32 [B] (device): lengths AFTER the append; the new token sits at
+ *             position L - 1.  Sequences with L < 1 are skipped.
+ *   q_out     bf16 [B, H, D]: the attention core's q
+ *   gqa_prepare_decode: k_cache, v_cache bf16 [B, rows, KVH, D]; the token goes
+ *             to row L - 1 (ring = 0; skipped when L > rows) or row (L - 1) mod
+ *             rows (ring = 1, the window-capped cache of gqa_decode_ring)
+ *   gqa_prepare_decode_paged: page pools [P, 16, KVH, D]; the token goes to slot
+ *             (L - 1) % 16 of page block_table[b][(L - 1) / 16]; a page id outside
+ *             [0, P) skips the write (the decode call then reports it)
+ * Outputs are rounded to bf16 (round to nearest even) from fp32 arithmetic; the
+ * rotation angles are reduced mod 2 pi in fp64.  One kernel launch on `stream`,
+ * with programmatic dependent launch so a decode call right behind it overlaps its
+ * start.  Errors: GQA_ERR_UNSUPPORTED for other geometries (or v_raw = NULL on a
+ * sliding geometry), GQA_ERR_INVALID_ARGUMENT for null or misaligned pointers
+ * (16 bytes; 4 for the weights, seq_lens and the block table) and bad sizes,
+ * GQA_ERR_CUDA for a failed launch.
+ */
+gqa_status_t gqa_prepare_decode(const void *q_raw, const void *k_raw, const void *v_raw,
+                                const void *w_q, const void *w_k, const int32_t *seq_lens, int B,
+                                int H, int KVH, int D, void *q_out, void *k_cache, void *v_cache,
+                                int rows, int ring, gqa_stream_t stream);
+
+gqa_status_t gqa_prepare_decode_paged(const void *q_raw, const void *k_raw, const void *v_raw,
+                                      const void *w_q, const void *w_k,
+                                      const int32_t *block_table, const int32_t *seq_lens, int B,
+                                      int P, int max_pages, int page_size, int H, int KVH, int D,
+                                      void *q_out, void *k_pages, void *v_pages,
+                                      gqa_stream_t stream);
+
+/*
  * Host-side check of the device-resident inputs, for tests and debugging: the
  * caller copies seq_lens (and the block table) to host memory and passes them
  * here.  The decode calls never read these arrays on the host (they stay on the

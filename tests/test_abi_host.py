@@ -218,3 +218,22 @@ def test_keqv_argument_checks(lib):
         gqa.GQA_ERR_INVALID_ARGUMENT   # page size must be 16
     assert lib.gqa_decode_keqv_paged(F, F, F, F, F, 2, 4, 4, 16, *SLIDING, F, 1, None, 0, None) == \
         gqa.GQA_ERR_UNSUPPORTED
+
+
+def test_prepare_argument_checks(lib):
+    F = FAKE
+    H, KVH, D = SLIDING
+    bad = gqa.GQA_ERR_INVALID_ARGUMENT
+    assert lib.gqa_prepare_decode(F, F, F, F, F, F, 2, 32, 8, 256, F, F, F, 64, 0, None) == \
+        gqa.GQA_ERR_UNSUPPORTED
+    # values = keys (v_raw NULL) exists on the global geometry only
+    assert lib.gqa_prepare_decode(F, F, None, F, F, F, 2, H, KVH, D, F, F, F, 64, 0, None) == \
+        gqa.GQA_ERR_UNSUPPORTED
+    assert lib.gqa_prepare_decode(F, F, F, F, F, F, 2, H, KVH, D, F, F, F, 0, 0, None) == bad
+    assert lib.gqa_prepare_decode(F, F, F, F, F, F, 2, H, KVH, D, F, F, F, 64, 2, None) == bad
+    assert lib.gqa_prepare_decode(F, F, F, F, F, F, 2, H, KVH, D, F, None, F, 64, 0, None) == bad
+    assert lib.gqa_prepare_decode(F + 2, F, F, F, F, F, 2, H, KVH, D, F, F, F, 64, 0, None) == bad
+    assert lib.gqa_prepare_decode(None, None, None, None, None, None, 0, H, KVH, D, None, None,
+                                  None, 64, 0, None) == gqa.GQA_OK
+    assert lib.gqa_prepare_decode_paged(F, F, F, F, F, F, F, 2, 4, 4, 8, H, KVH, D, F, F, F,
+                                        None) == bad
