@@ -61,6 +61,12 @@ def _bind(path: str):
     lib.oracle_prepare_decode_f64.argtypes = [u16p, u16p, u16p, u16p, u16p, i32p, ci, ci, ci, ci,
                                               ci, ctypes.c_double, f64p, f64p, f64p]
     lib.oracle_prepare_decode_f64.restype = ci
+    lib.oracle_gqa_decode_mq_f64.argtypes = [u16p, u16p, u16p, i32p, ci, ci, ci, ci, ci, ci,
+                                             ci, ci, f64p]
+    lib.oracle_gqa_decode_mq_f64.restype = ci
+    lib.oracle_gqa_decode_mq_paged_f64.argtypes = [u16p, u16p, u16p, i32p, i32p, ci, ci, ci,
+                                                   ci, ci, ci, ci, ci, ci, ci, f64p]
+    lib.oracle_gqa_decode_mq_paged_f64.restype = ci
     lib.oracle_default_threads.argtypes = []
     lib.oracle_default_threads.restype = ci
     return lib
@@ -174,6 +180,64 @@ def gqa_decode_ring_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, seq_lens, w
     return out
 
 
+def gqa_decode_mq_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, seq_lens, window: int,
+                      nthreads: int = 0, _lib_override=None) -> np.ndarray:
+    """Multi-query decode attention over a contiguous cache, exact up to fp64 rounding.
+
+    q: uint16 [B, T, H, D]; k, v: uint16 [B, S, KVH, D], row s = position s;
+    seq_lens: lengths after the T new tokens were appended.  Query t of sequence b
+    sits at position L_b - T + t and attends to [max(0, p + 1 - window), p + 1)
+    (sliding) or [0, p + 1) (window 0); a negative position attends to nothing
+    (o = 0).  Returns float64 [B, T, H, D].
+    """
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, T, H, D = q.shape
+    Bk, S, KVH, Dk = k.shape
+    if k.shape != v.shape or Bk != B or Dk != D:
+        raise ValueError("shape mismatch between q, k and v")
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError("seq_lens must have shape [B]")
+    out = np.zeros((B, T, H, D), dtype=np.float64)
+    lib = _lib_override if _lib_override is not None else _load()
+    rc = lib.oracle_gqa_decode_mq_f64(
+        _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
+        _ptr(lens, ctypes.c_int32), B, T, S, H, KVH, D, int(window), int(nthreads),
+        _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out
+
+
+def gqa_decode_mq_paged_f64(q: np.ndarray, k_pages: np.ndarray, v_pages: np.ndarray,
+                            block_table: np.ndarray, seq_lens, window: int,
+                            nthreads: int = 0, _lib_override=None) -> np.ndarray:
+    """Multi-query decode attention over a paged cache, exact up to fp64 rounding.
+
+    q: uint16 [B, T, H, D]; pools uint16 [P, page_size, KVH, D]; block_table int32
+    [B, max_pages].  A query whose attended range names a page outside [0, P) gets
+    NaN for all of its heads.
+    """
+    q, k_pages, v_pages = _u16(q), _u16(k_pages), _u16(v_pages)
+    B, T, H, D = q.shape
+    P, page_size, KVH, Dk = k_pages.shape
+    if k_pages.shape != v_pages.shape or Dk != D:
+        raise ValueError("shape mismatch between q and the page pools")
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    if bt.ndim != 2 or bt.shape[0] != B:
+        raise ValueError("block_table must have shape [B, max_pages]")
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    out = np.zeros((B, T, H, D), dtype=np.float64)
+    lib = _lib_override if _lib_override is not None else _load()
+    rc = lib.oracle_gqa_decode_mq_paged_f64(
+        _ptr(q, ctypes.c_uint16), _ptr(k_pages, ctypes.c_uint16), _ptr(v_pages, ctypes.c_uint16),
+        _ptr(bt, ctypes.c_int32), _ptr(lens, ctypes.c_int32), B, T, P, bt.shape[1], page_size,
+        H, KVH, D, int(window), int(nthreads), _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out
+
+
 # RoPE of the global layers (Model Spec, `attn.rope` row for layers 5, 11, ..., 59)
 GLOBAL_ROPE_PAIRS = 64
 GLOBAL_ROPE_THETA = 1.0e6
@@ -266,6 +330,12 @@ class OracleLibrary:
 
     def prepare_decode_f64(self, *args, **kw):
         return prepare_decode_f64(*args, _lib_override=self._lib, **kw)
+
+    def gqa_decode_mq_f64(self, *args, **kw):
+        return gqa_decode_mq_f64(*args, _lib_override=self._lib, **kw)
+
+    def gqa_decode_mq_paged_f64(self, *args, **kw):
+        return gqa_decode_mq_paged_f64(*args, _lib_override=self._lib, **kw)
 
 
 def compile_variant(source_text: str, out_path: str) -> str:

@@ -612,3 +612,176 @@ int oracle_prepare_decode_f64(const uint16_t *q_raw, const uint16_t *k_raw, cons
     }
     return ORACLE_OK;
 }
+
+/* ---- multi-query decode: T new tokens per sequence ("Gemma 4 31B-it Text
+ *      Architecture", "Inference behavior: Prefill, Cache, and Long Context" and
+ *      "Compact form").  The T tokens of a step are appended to the cache before
+ *      attention, so with L_b the length after the append, query t (0 <= t < T)
+ *      sits at position p = L_b - T + t (positions = past_seen_tokens +
+ *      arange(T_current)) and sees the keys the masks allow for that position:
+ *          full layers    (window == 0): s <= p          -> s in [0, p + 1)
+ *          sliding layers (window  > 0): p - window < s <= p
+ *                                                        -> s in [max(0, p + 1 - window), p + 1)
+ *      A query whose position is negative (L_b < T - t) sees nothing and gets the
+ *      empty sum, o = 0.  Tokens of the same step are causal among themselves:
+ *      query t never sees the tokens after it. ---- */
+static void query_range(int64_t L, int T, int t, int window, int64_t *lo, int64_t *hi)
+{
+    const int64_t p = L - T + t; /* position of query t */
+    *hi = p + 1 > 0 ? p + 1 : 0;
+    *lo = (window > 0 && *hi > window) ? *hi - window : 0;
+}
+
+/*
+ * q:        [B, T, H, D] bf16 bits, query t of sequence b at position L_b - T + t
+ * k, v:     [B, S, KVH, D] bf16 bits, row s = position s (the T new rows included)
+ * seq_lens: [B] lengths after the append, 0 <= L_b <= S
+ * out:      [B, T, H, D] doubles
+ */
+int oracle_gqa_decode_mq_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                             const int32_t *seq_lens, int B, int T, int S, int H, int KVH,
+                             int D, int window, int nthreads, double *out)
+{
+    int b;
+    if (B < 0 || T < 1 || S < 0 || H <= 0 || KVH <= 0 || D <= 0 || window < 0)
+        return ORACLE_EINVAL;
+    if (H % KVH != 0) return ORACLE_EINVAL;
+    int64_t max_n = 1; /* longest attended range (scratch size) */
+    for (b = 0; b < B; ++b) {
+        int t;
+        if (seq_lens[b] < 0 || seq_lens[b] > S) return ORACLE_EINVAL;
+        for (t = 0; t < T; ++t) { /* every attended row lies in the cache */
+            int64_t lo, hi;
+            query_range(seq_lens[b], T, t, window, &lo, &hi);
+            if (lo < 0 || hi > S) return ORACLE_EINVAL;
+            if (hi - lo > max_n) max_n = hi - lo;
+        }
+    }
+    const int g = H / KVH;
+    const int64_t items = (int64_t)B * T * H;
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#endif
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)max_n);
+        double *q_row = (double *)malloc(sizeof(double) * (size_t)D);
+        const int have_scratch = scores != NULL && q_row != NULL;
+        int64_t it;
+        /* every thread reaches the work-sharing loop (it ends in a barrier) */
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (it = 0; it < items; ++it) {
+            if (!have_scratch) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+                err = ORACLE_ENOMEM;
+                continue;
+            }
+            {
+                const int64_t bb = it / ((int64_t)T * H);
+                const int t = (int)((it / H) % T);
+                const int64_t h = it % H;
+                const int64_t row = (bb * T + t) * H + h; /* [B, T, H] index */
+                const int64_t kvh = h / g; /* the query head's KV head */
+                int64_t lo, hi;
+                int d;
+                query_range(seq_lens[bb], T, t, window, &lo, &hi);
+                for (d = 0; d < D; ++d) q_row[d] = bf16_bits_to_double(q[row * D + d]);
+                const int64_t n = hi - lo;
+                contig_ctx cq = {k, v, bb, kvh, lo, 0, S, KVH, D};
+                attend(q_row, D, n, contig_k, contig_v, &cq, scores, out + row * D);
+            }
+        }
+        free(scores);
+        free(q_row);
+    }
+    (void)nthreads;
+    return err;
+}
+
+/*
+ * Paged multi-query variant: pools [P, page_size, KVH, D], block_table [B,
+ * max_pages].  A query whose attended range names a page outside [0, P) gets NaN
+ * for all of its heads; the other queries of the sequence are unaffected.
+ */
+int oracle_gqa_decode_mq_paged_f64(const uint16_t *q, const uint16_t *k_pages,
+                                   const uint16_t *v_pages, const int32_t *block_table,
+                                   const int32_t *seq_lens, int B, int T, int P, int max_pages,
+                                   int page_size, int H, int KVH, int D, int window,
+                                   int nthreads, double *out)
+{
+    int b;
+    if (B < 0 || T < 1 || P <= 0 || max_pages <= 0 || page_size <= 0 || H <= 0 || KVH <= 0 ||
+        D <= 0 || window < 0)
+        return ORACLE_EINVAL;
+    if (H % KVH != 0) return ORACLE_EINVAL;
+    int64_t max_n = 1; /* longest attended range (scratch size) */
+    for (b = 0; b < B; ++b) {
+        int t;
+        if (seq_lens[b] < 0 || (int64_t)seq_lens[b] > (int64_t)max_pages * page_size)
+            return ORACLE_EINVAL;
+        for (t = 0; t < T; ++t) { /* every attended row has a block-table entry */
+            int64_t lo, hi;
+            query_range(seq_lens[b], T, t, window, &lo, &hi);
+            if (lo < 0 || hi > (int64_t)max_pages * page_size) return ORACLE_EINVAL;
+            if (hi - lo > max_n) max_n = hi - lo;
+        }
+    }
+    const int g = H / KVH;
+    const int64_t items = (int64_t)B * T * H;
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel num_threads(nt)
+#endif
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)max_n);
+        double *q_row = (double *)malloc(sizeof(double) * (size_t)D);
+        const int have_scratch = scores != NULL && q_row != NULL;
+        int64_t it;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (it = 0; it < items; ++it) {
+            if (!have_scratch) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+                err = ORACLE_ENOMEM;
+                continue;
+            }
+            {
+                const int64_t bb = it / ((int64_t)T * H);
+                const int t = (int)((it / H) % T);
+                const int64_t h = it % H;
+                const int64_t row = (bb * T + t) * H + h;
+                const int32_t *bt_row = block_table + bb * (int64_t)max_pages;
+                double *o = out + row * D;
+                const int64_t kvh = h / g;
+                int64_t lo, hi, s;
+                int d, bad = 0;
+                query_range(seq_lens[bb], T, t, window, &lo, &hi);
+                for (s = lo; s < hi; ++s) {
+                    const int32_t pg = bt_row[s / page_size];
+                    if (pg < 0 || pg >= P) bad = 1;
+                }
+                if (bad) {
+                    for (d = 0; d < D; ++d) o[d] = NAN;
+                    continue;
+                }
+                for (d = 0; d < D; ++d) q_row[d] = bf16_bits_to_double(q[row * D + d]);
+                const int64_t n = hi - lo;
+                paged_ctx cq = {k_pages, v_pages, bt_row, kvh, lo, page_size, KVH, D};
+                attend(q_row, D, n, paged_k, paged_v, &cq, scores, o);
+            }
+        }
+        free(scores);
+        free(q_row);
+    }
+    (void)nthreads;
+    return err;
+}

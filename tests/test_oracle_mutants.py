@@ -107,6 +107,30 @@ MUTANTS = {
     "producer_value_weighted": (
         "            rms_norm_head(vr, NULL, D, yv);",
         "            rms_norm_head(vr, w_k, D, yv);"),
+    "mq_position_one_late": (
+        "const int64_t p = L - T + t; /* position of query t */",
+        "const int64_t p = L - T + t + 1;"),
+    "mq_position_one_early": (
+        "const int64_t p = L - T + t; /* position of query t */",
+        "const int64_t p = L - T + t - 1;"),
+    "mq_every_query_at_the_last_position": (
+        "const int64_t p = L - T + t; /* position of query t */",
+        "const int64_t p = L - 1 + 0 * t;"),
+    "mq_window_anchored_at_the_length": (
+        "*lo = (window > 0 && *hi > window) ? *hi - window : 0;",
+        "*lo = (window > 0 && L > window) ? L - window : 0;"),
+    "mq_queries_reversed": (
+        "query_range(seq_lens[bb], T, t, window, &lo, &hi);\n                for (d = 0; d < D; ++d) q_row[d] = bf16_bits_to_double(q[row * D + d]);\n                const int64_t n = hi - lo;\n                contig_ctx",
+        "query_range(seq_lens[bb], T, T - 1 - t, window, &lo, &hi);\n                for (d = 0; d < D; ++d) q_row[d] = bf16_bits_to_double(q[row * D + d]);\n                const int64_t n = hi - lo;\n                contig_ctx"),
+    "mq_head_map_modulo": (
+        "const int64_t kvh = h / g; /* the query head's KV head */",
+        "const int64_t kvh = h % KVH;"),
+    "mq_query_rows_head_major": (
+        "const int64_t row = (bb * T + t) * H + h; /* [B, T, H] index */",
+        "const int64_t row = (bb * H + h) * T + t;"),
+    "mq_paged_head_map_modulo": (
+        "const int64_t kvh = h / g;\n                int64_t lo, hi, s;",
+        "const int64_t kvh = h % KVH;\n                int64_t lo, hi, s;"),
     "empty_range_not_zero": (
         "if (n <= 0) return; /* empty sum */",
         "if (n <= 0) { for (d = 0; d < D; ++d) out[d] = 1.0; return; }"),

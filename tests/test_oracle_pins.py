@@ -602,3 +602,128 @@ def test_thread_count_does_not_change_results(oracle_lib):
     a = oracle_lib.gqa_decode_f64(q, k, v, [64, 50], 0, nthreads=1)
     b = oracle_lib.gqa_decode_f64(q, k, v, [64, 50], 0, nthreads=4)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# multi-query decode: T new tokens per sequence ("Gemma 4 31B-it Text
+# Architecture", "Inference behavior: Prefill, Cache, and Long Context" and
+# "Compact form": positions = past_seen_tokens + arange(T_current), masks
+# s <= t and t - 1024 < s <= t)
+# ---------------------------------------------------------------------------
+
+def mq_case(B, T, S, H, KVH, D, seed):
+    rng = np.random.default_rng(seed)
+    q = to_bits(rng.standard_normal((B, T, H, D)))
+    k = to_bits(rng.standard_normal((B, S, KVH, D)))
+    v = to_bits(rng.standard_normal((B, S, KVH, D)))
+    return q, k, v
+
+
+@pytest.mark.parametrize("T,W", [(1, 0), (3, 0), (4, 5), (5, 16), (8, 1)])
+def test_mq_each_query_is_a_decode_step_at_its_position(oracle_lib, T, W):
+    """Query t of a T-token step sees what a one-token decode step at length
+    L - T + t + 1 sees (bitwise): the single-query oracle, with its own pins."""
+    B, S, H, KVH, D = 4, 40, 8, 2, 16
+    q, k, v = mq_case(B, T, S, H, KVH, D, seed=40 + T)
+    lens = [40, 21, T, max(1, T - 2)]
+    out = oracle_lib.gqa_decode_mq_f64(q, k, v, lens, W)
+    for t in range(T):
+        step_lens = [max(0, L - T + t + 1) for L in lens]
+        one = oracle_lib.gqa_decode_f64(np.ascontiguousarray(q[:, t]), k, v, step_lens, W)
+        assert np.array_equal(out[:, t], one), f"query {t}"
+
+
+@pytest.mark.parametrize("H,KVH,T,W", [(32, 16, 4, 1024), (32, 16, 6, 7), (32, 4, 4, 0),
+                                       (32, 4, 3, 9)])
+def test_mq_torch_sdpa_float64(oracle_lib, H, KVH, T, W):
+    """SDPA in float64 with the Compact form's boolean mask built from the query
+    positions (L - T) + arange(T): keys s <= t, and t - W < s for a window."""
+    B, S, D = 3, 45, 16
+    q, k, v = mq_case(B, T, S, H, KVH, D, seed=50 + T + W)
+    lens = [45, 30, T + 1]
+    out = oracle_lib.gqa_decode_mq_f64(q, k, v, lens, W)
+    g = H // KVH
+    qt = torch.from_numpy(to_vals(q)).permute(0, 2, 1, 3)               # [B, H, T, D]
+    kt = torch.from_numpy(to_vals(k)).permute(0, 2, 1, 3).repeat_interleave(g, dim=1)
+    vt = torch.from_numpy(to_vals(v)).permute(0, 2, 1, 3).repeat_interleave(g, dim=1)
+    s = torch.arange(S)[None, :]
+    mask = torch.zeros(B, 1, T, S, dtype=torch.bool)
+    for b, L in enumerate(lens):
+        t = (L - T) + torch.arange(T)[:, None]        # query positions
+        m = s <= t
+        if W > 0:
+            m &= s > t - W
+        mask[b, 0] = m
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=1.0)
+    np.testing.assert_allclose(out, ref.permute(0, 2, 1, 3).numpy(), rtol=1e-11, atol=1e-13)
+
+
+def test_mq_later_tokens_are_invisible_to_earlier_queries(oracle_lib):
+    """Changing the key/value of new token t' changes queries t >= t' only."""
+    B, T, S, H, KVH, D = 2, 5, 30, 8, 4, 16
+    q, k, v = mq_case(B, T, S, H, KVH, D, seed=60)
+    lens = [30, 17]
+    base = oracle_lib.gqa_decode_mq_f64(q, k, v, lens, 0)
+    for tp in range(T):
+        k2, v2 = k.copy(), v.copy()
+        for b, L in enumerate(lens):
+            k2[b, L - T + tp] = to_bits(-to_vals(k[b, L - T + tp]) * 3.0)
+            v2[b, L - T + tp] = to_bits(to_vals(v[b, L - T + tp]) + 2.0)
+        out = oracle_lib.gqa_decode_mq_f64(q, k2, v2, lens, 0)
+        for t in range(T):
+            same = np.array_equal(out[:, t], base[:, t])
+            assert same == (t < tp), f"token {tp}, query {t}"
+
+
+def test_mq_window_moves_with_each_query(oracle_lib):
+    """With a window, query t drops position L - T + t - W that query t - 1 still
+    sees: perturbing that one row changes query t - 1 and not query t."""
+    B, T, S, H, KVH, D, W = 1, 4, 40, 4, 2, 8, 6
+    q, k, v = mq_case(B, T, S, H, KVH, D, seed=61)
+    L = 40
+    base = oracle_lib.gqa_decode_mq_f64(q, k, v, [L], W)
+    for t in range(1, T):
+        s = L - T + t - W   # seen by query t - 1 only
+        v2 = v.copy()
+        v2[0, s] = to_bits(to_vals(v[0, s]) + 5.0)
+        out = oracle_lib.gqa_decode_mq_f64(q, k, v2, [L], W)
+        assert not np.array_equal(out[0, t - 1], base[0, t - 1])
+        assert np.array_equal(out[0, t:], base[0, t:])
+
+
+def test_mq_queries_before_the_start_are_zero(oracle_lib):
+    """L < T: queries at negative positions see nothing (o = 0); the first query at
+    position 0 sees v[0] alone."""
+    B, T, S, H, KVH, D = 1, 6, 8, 8, 2, 16
+    q, k, v = mq_case(B, T, S, H, KVH, D, seed=62)
+    L = 3
+    out = oracle_lib.gqa_decode_mq_f64(q, k, v, [L], 0)
+    n_neg = T - L
+    assert np.all(out[0, :n_neg] == 0.0)
+    g = H // KVH
+    for h in range(H):
+        np.testing.assert_array_equal(out[0, n_neg, h], to_vals(v[0, 0, h // g]))
+
+
+@pytest.mark.parametrize("H,KVH,D,T,W", [(32, 16, 16, 4, 20), (32, 4, 32, 3, 0)])
+def test_mq_paged_equals_contiguous(oracle_lib, H, KVH, D, T, W):
+    B, S = 3, 70
+    q, k, v = mq_case(B, T, S, H, KVH, D, seed=63)
+    lens = [70, 33, 17]
+    kp, vp, bt = scatter_to_pages(k, v, lens)
+    paged = oracle_lib.gqa_decode_mq_paged_f64(q, kp, vp, bt, lens, W)
+    contig = oracle_lib.gqa_decode_mq_f64(q, k, v, lens, W)
+    assert np.array_equal(paged, contig)
+
+
+def test_mq_paged_bad_page_hits_only_the_queries_that_see_it(oracle_lib):
+    """A bad id on the page of the last new token (position L - 1, first slot of its
+    page) turns only the last query into NaN."""
+    B, T, S, H, KVH, D = 2, 3, 50, 8, 2, 16
+    q, k, v = mq_case(B, T, S, H, KVH, D, seed=64)
+    lens = [49, 33]   # L - 1 = 48 and 32: the first slot of a page
+    kp, vp, bt = scatter_to_pages(k, v, lens)
+    bt[0, 48 // 16] = kp.shape[0] + 3
+    out = oracle_lib.gqa_decode_mq_paged_f64(q, kp, vp, bt, lens, 0)
+    assert np.all(np.isnan(out[0, T - 1]))
+    assert np.all(np.isfinite(out[0, :T - 1])) and np.all(np.isfinite(out[1]))
