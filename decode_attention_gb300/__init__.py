@@ -13,6 +13,8 @@ from ._native import (  # noqa: F401
     GQA_DEVICE_BAD_LENGTH,
     GQA_DEVICE_BAD_PAGE,
     GQA_DEVICE_WAIT_TIMEOUT,
+    GQA_MAX_QUERIES_GLOBAL,
+    GQA_MAX_QUERIES_SLIDING,
     GQA_ERR_CUDA,
     GQA_ERR_INVALID_ARGUMENT,
     GQA_ERR_UNSUPPORTED,
@@ -25,6 +27,8 @@ from ._native import (  # noqa: F401
     gqa_decode,
     gqa_decode_keqv,
     gqa_decode_keqv_paged,
+    gqa_decode_mq,
+    gqa_decode_mq_paged,
     gqa_decode_noalloc,
     gqa_prepare_decode,
     gqa_prepare_decode_paged,
@@ -35,6 +39,7 @@ from ._native import (  # noqa: F401
     gqa_status_string,
     gqa_workspace_init,
     gqa_workspace_size,
+    gqa_workspace_size_mq,
     library_path,
     load_library,
     new_workspace,

@@ -34,7 +34,8 @@ PAGE_SIZE = 16
 EXPORTED_SYMBOLS = ("gqa_workspace_size", "gqa_workspace_init", "gqa_decode", "gqa_decode_paged",
                     "gqa_device_status", "gqa_decode_noalloc", "gqa_decode_ring",
                     "gqa_decode_keqv", "gqa_decode_keqv_paged", "gqa_prepare_decode",
-                    "gqa_prepare_decode_paged",
+                    "gqa_prepare_decode_paged", "gqa_workspace_size_mq", "gqa_decode_mq",
+                    "gqa_decode_mq_paged",
                     "gqa_check_inputs_host",
                     "gqa_status_string")
 
@@ -90,6 +91,13 @@ def load_library(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.gqa_prepare_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
                                                  ci, vp, vp, vp, vp]
         lib.gqa_prepare_decode_paged.restype = ci
+        lib.gqa_workspace_size_mq.argtypes = [ci, ci, ci, ci, ci]
+        lib.gqa_workspace_size_mq.restype = sz
+        lib.gqa_decode_mq.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp, ci, vp, sz, vp]
+        lib.gqa_decode_mq.restype = ci
+        lib.gqa_decode_mq_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci,
+                                            vp, ci, vp, sz, vp]
+        lib.gqa_decode_mq_paged.restype = ci
         lib.gqa_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gqa_device_status.restype = ci
         lib.gqa_check_inputs_host.argtypes = [vp, ci, ci, ci, vp, ci, ci, ctypes.POINTER(ci)]
@@ -287,6 +295,69 @@ def gqa_decode_keqv_paged(q: torch.Tensor, v_pages: torch.Tensor, w_k: torch.Ten
         block_table.shape[1], page_size, H, KVH, D, _ptr(out), _out_code(out), _ptr(workspace),
         ws_bytes, _stream_handle(stream, q.device))
     _check("gqa_decode_keqv_paged", st)
+    return out
+
+
+GQA_MAX_QUERIES_SLIDING = 8
+GQA_MAX_QUERIES_GLOBAL = 4
+
+
+def gqa_workspace_size_mq(B: int, T: int, H: int, KVH: int, D: int) -> int:
+    return int(load_library().gqa_workspace_size_mq(B, T, H, KVH, D))
+
+
+def _mq_out(q, out, out_dtype):
+    B, T, H, D = q.shape
+    if out is None:
+        out = torch.empty((B, T, H, D), dtype=out_dtype, device=q.device)
+    _check_tensor("out", out, out.dtype, 4)
+    _require(tuple(out.shape) == (B, T, H, D), "out must be [B, T, H, D]")
+    return out
+
+
+def gqa_decode_mq(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
+                  window: int, out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+                  workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Multi-query decode over a contiguous cache: q [B,T,H,D], k/v [B,S,KVH,D] (bf16);
+    query t sits at position seq_lens[b] - T + t.  Returns out [B,T,H,D]."""
+    _check_tensor("q", q, torch.bfloat16, 4)
+    _check_tensor("k", k, torch.bfloat16, 4)
+    _check_tensor("v", v, torch.bfloat16, 4)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    B, T, H, D = q.shape
+    _, S, KVH, _ = k.shape
+    _require(tuple(k.shape) == (B, S, KVH, D) and v.shape == k.shape, "k/v shape mismatch")
+    _require(seq_lens.shape[0] == B, "seq_lens must have B entries")
+    out = _mq_out(q, out, out_dtype)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().gqa_decode_mq(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, T, S, H, KVH, D, int(window), _ptr(out),
+        _out_code(out), _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
+    _check("gqa_decode_mq", st)
+    return out
+
+
+def gqa_decode_mq_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                        block_table: torch.Tensor, seq_lens: torch.Tensor, window: int,
+                        out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+                        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Multi-query decode over a paged cache: pools [P,16,KVH,D], block_table [B,max_pages]."""
+    _check_tensor("q", q, torch.bfloat16, 4)
+    _check_tensor("k_pages", k_pages, torch.bfloat16, 4)
+    _check_tensor("v_pages", v_pages, torch.bfloat16, 4)
+    _check_tensor("block_table", block_table, torch.int32, 2)
+    _check_tensor("seq_lens", seq_lens, torch.int32, 1)
+    B, T, H, D = q.shape
+    P, page_size, KVH, _ = k_pages.shape
+    _require(v_pages.shape == k_pages.shape and k_pages.shape[3] == D, "page pool shape mismatch")
+    _require(block_table.shape[0] == B and seq_lens.shape[0] == B, "batch size mismatch")
+    out = _mq_out(q, out, out_dtype)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().gqa_decode_mq_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), B, T, P,
+        block_table.shape[1], page_size, H, KVH, D, int(window), _ptr(out), _out_code(out),
+        _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
+    _check("gqa_decode_mq_paged", st)
     return out
 
 

@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libgqadecode.so")
 
 SOURCES = ["gqa_decode.cu", "gqa_decode_noalloc.cu", "kernels_sliding.cu", "kernels_global.cu",
-           "kernels_global_keqv.cu", "gqa_prepare.cu"]
+           "kernels_global_keqv.cu", "gqa_prepare.cu", "kernels_mq.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

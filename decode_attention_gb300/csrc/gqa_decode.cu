@@ -106,7 +106,13 @@ namespace {
 struct CallShape {
     Geometry geo;
     int B, H, KVH, D, window;
+    int T = 1;   // query tokens per sequence
 };
+
+// Query tokens one multi-query call may carry for a geometry.
+bool queries_ok(Geometry geo, int T) {
+    return T >= 1 && T <= gqa::mq_max_queries(geo == Geometry::kSliding);
+}
 
 gqa_status_t check_common(const CallShape& c, const void* q, const void* out,
                           const int32_t* seq_lens, gqa_out_dtype_t out_dtype) {
@@ -124,7 +130,7 @@ gqa_status_t check_common(const CallShape& c, const void* q, const void* out,
 gqa_status_t prepare(const CallShape& c, void* workspace, size_t workspace_bytes,
                      cudaStream_t stream, void** ws_out, WorkspaceLayout* lay, int* grid) {
     const int G = heads_per_kv(c.geo);
-    *lay = layout_for(c.B, c.KVH, G, c.D);
+    *lay = layout_for(c.B, c.KVH, G * c.T, c.D);   // partials hold T * g query rows
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
     DeviceState& ds = g_dev[dev];
@@ -164,7 +170,7 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
                  const int32_t* block_table, const int32_t* seq_lens, uint64_t rows,
                  uint64_t outer, int capacity, int ring, int num_pages, int max_pages, void* out,
                  gqa_out_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
-                 cudaStream_t stream, const void* w_k = nullptr) {
+                 cudaStream_t stream, const void* w_k = nullptr, bool multi_query = false) {
     if (!gqa::tensor_map_encoder()) return GQA_ERR_CUDA;
     void* ws = nullptr;
     WorkspaceLayout lay;
@@ -199,6 +205,7 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
     a.p.num_pages = num_pages;
     a.p.max_pages = max_pages;
     a.p.out_f32 = out_dtype == GQA_OUT_F32 ? 1 : 0;
+    a.p.T = c.T;
     a.grid = grid;
     a.stream = stream;
     if (w_k) {
@@ -209,6 +216,9 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
             a.p.rope_freq[i] = std::pow(kGlobalRopeTheta, -2.0 * i / static_cast<double>(c.D));
         return gqa::launch_global_keqv(a, paged) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
     }
+    if (multi_query)
+        return gqa::launch_mq(a, c.geo == Geometry::kSliding, paged) == cudaSuccess ? GQA_OK
+                                                                                   : GQA_ERR_CUDA;
     const cudaError_t e = c.geo == Geometry::kSliding ? gqa::launch_sliding(a, paged)
                                                       : gqa::launch_global(a, paged);
     return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
@@ -341,6 +351,50 @@ gqa_status_t gqa_decode_keqv_paged(const void* q, const void* v_pages, const voi
     return run(c, true, q, v_pages, v_pages, block_table, seq_lens, GQA_PAGE_SIZE,
                static_cast<uint64_t>(P), max_pages * GQA_PAGE_SIZE, 0, P, max_pages, out,
                out_dtype, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), w_k);
+}
+
+size_t gqa_workspace_size_mq(int B, int T, int H, int KVH, int D) {
+    const Geometry geo = geometry_of(H, KVH, D);
+    if (geo == Geometry::kNone || B < 0 || B > GQA_MAX_BATCH || !queries_ok(geo, T)) return 0;
+    return layout_for(B, KVH, heads_per_kv(geo) * T, D).total;
+}
+
+gqa_status_t gqa_decode_mq(const void* q, const void* k, const void* v, const int32_t* seq_lens,
+                           int B, int T, int S, int H, int KVH, int D, int window, void* out,
+                           gqa_out_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
+                           gqa_stream_t stream) {
+    CallShape c{geometry_of(H, KVH, D), B, H, KVH, D, window};
+    c.T = T;
+    if (S < 1 || S > GQA_MAX_SEQ) return GQA_ERR_INVALID_ARGUMENT;
+    if (c.geo != Geometry::kNone && !queries_ok(c.geo, T)) return GQA_ERR_INVALID_ARGUMENT;
+    gqa_status_t st = check_common(c, q, out, seq_lens, out_dtype);
+    if (st != GQA_OK || B == 0) return st;
+    if (!k || !v || !aligned(k, 16) || !aligned(v, 16)) return GQA_ERR_INVALID_ARGUMENT;
+    return run(c, false, q, k, v, nullptr, seq_lens, static_cast<uint64_t>(S),
+               static_cast<uint64_t>(B), S, 0, 0, 0, out, out_dtype, workspace, workspace_bytes,
+               reinterpret_cast<cudaStream_t>(stream), nullptr, true);
+}
+
+gqa_status_t gqa_decode_mq_paged(const void* q, const void* k_pages, const void* v_pages,
+                                 const int32_t* block_table, const int32_t* seq_lens, int B,
+                                 int T, int P, int max_pages, int page_size, int H, int KVH,
+                                 int D, int window, void* out, gqa_out_dtype_t out_dtype,
+                                 void* workspace, size_t workspace_bytes, gqa_stream_t stream) {
+    CallShape c{geometry_of(H, KVH, D), B, H, KVH, D, window};
+    c.T = T;
+    if (page_size != GQA_PAGE_SIZE || P < 1 || max_pages < 1 ||
+        static_cast<int64_t>(max_pages) * GQA_PAGE_SIZE > GQA_MAX_SEQ)
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (c.geo != Geometry::kNone && !queries_ok(c.geo, T)) return GQA_ERR_INVALID_ARGUMENT;
+    gqa_status_t st = check_common(c, q, out, seq_lens, out_dtype);
+    if (st != GQA_OK || B == 0) return st;
+    if (!k_pages || !v_pages || !block_table || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+        !aligned(block_table, 4))
+        return GQA_ERR_INVALID_ARGUMENT;
+    return run(c, true, q, k_pages, v_pages, block_table, seq_lens, GQA_PAGE_SIZE,
+               static_cast<uint64_t>(P), max_pages * GQA_PAGE_SIZE, 0, P, max_pages, out,
+               out_dtype, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
+               nullptr, true);
 }
 
 gqa_status_t gqa_check_inputs_host(const int32_t* seq_lens, int B, int capacity, int window,

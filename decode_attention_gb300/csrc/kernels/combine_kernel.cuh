@@ -1,16 +1,20 @@
 // Log-sum-exp combine of split-softmax partials (second kernel of a call).
 //
 // A segment u = (b, kvh) whose attended positions were processed in more than
-// one piece has, per piece j, the running max m_j (log2 units), the normaliser
-// l_j = sum exp2(s - m_j) and the unnormalised acc_j = sum exp2(s - m_j) v in the
-// workspace.  The softmax over the whole range (gemma-4-31B Model Spec,
-// "Compute-graph nodes", attn.core rows) is recovered exactly by
+// one piece has, per piece j and query row r, the running max m_j (log2 units),
+// the normaliser l_j = sum exp2(s - m_j) and the unnormalised acc_j =
+// sum exp2(s - m_j) v in the workspace.  A segment has R = T * G query rows, row
+// r = t * G + h being query token t and head h of the KV head's group.  A piece in
+// which a row saw no key has m_j = -inf and l_j = 0 (weight 0); a row that saw no
+// key in any piece (a query before the start of its sequence) is the empty sum, 0.
+// The softmax over the whole range (gemma-4-31B Model Spec, "Compute-graph
+// nodes", attn.core rows) is recovered exactly by
 //     M = max_j m_j,  o = (sum_j exp2(m_j - M) acc_j) / (sum_j exp2(m_j - M) l_j),
 // evaluated here as a running merge over the pieces in the fixed order of
 // SegmentParts (static units, then dynamic chunks).
 //
-// Work items are (segment, 512-element chunk of its G*D outputs); one thread
-// owns 4 consecutive outputs of one head and issues the loads of all pieces
+// Work items are (segment, 512-element chunk of its R*D outputs); one thread
+// owns 4 consecutive outputs of one query row and issues the loads of all pieces
 // before it merges them.  The kernel is launched right behind the main kernel
 // with programmatic dependent launch and waits for it to complete before
 // reading the partials; it also resets the dynamic-chunk claim counter.
@@ -26,8 +30,10 @@ constexpr int kCombineBatch = 16;       // pieces whose loads are in flight toge
 template <int G, int D>
 __global__ void __launch_bounds__(kCombineThreads)
     gqa_combine_kernel(const DecodeParams p, int num_segments) {
-    constexpr int kF4PerSeg = G * D / 4;
-    constexpr int kChunksPerSeg = (kF4PerSeg + kCombineThreads - 1) / kCombineThreads;
+    const int T = p.T > 1 ? p.T : 1;
+    const int R = T * G;   // query rows per segment
+    const int kF4PerSeg = R * D / 4;
+    const int kChunksPerSeg = (kF4PerSeg + kCombineThreads - 1) / kCombineThreads;
     __shared__ int4 seg_s[kCombineThreads];
 
     ptx::grid_dependency_wait();   // the main kernel has finished; its writes are visible
@@ -51,7 +57,7 @@ __global__ void __launch_bounds__(kCombineThreads)
             const int u = item / kChunksPerSeg;
             const int f4 = (item - u * kChunksPerSeg) * kCombineThreads + tid;
             if (f4 >= kF4PerSeg) continue;
-            const int h = (f4 * 4) / D;
+            const int h = (f4 * 4) / D;   // query row t * G + head
             float M = -INFINITY, den = 0.0f;
             float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int j0 = 0; j0 < nparts; j0 += kCombineBatch) {
@@ -67,18 +73,19 @@ __global__ void __launch_bounds__(kCombineThreads)
                         const size_t sl = j < e.y
                                               ? static_cast<size_t>(e.x + j) + u
                                               : static_cast<size_t>(p.dyn_slot_base) + e.z + (j - e.y);
-                        const float2 ml = __ldg(reinterpret_cast<const float2*>(p.ws_ml) + sl * G + h);
+                        const float2 ml = __ldg(reinterpret_cast<const float2*>(p.ws_ml) + sl * R + h);
                         mj[q] = ml.x;
                         lj[q] = ml.y;
-                        aj[q] = __ldg(reinterpret_cast<const float4*>(p.ws_acc + sl * G * D) + f4);
+                        aj[q] = __ldg(reinterpret_cast<const float4*>(p.ws_acc + sl * R * D) + f4);
                     }
                 }
 #pragma unroll
                 for (int q = 0; q < kCombineBatch; ++q) {
                     if (j0 + q >= nparts) break;
                     const float Mn = fmaxf(M, mj[q]);
-                    const float sc = exp2f(M - Mn);   // 0 on the first piece (M = -inf)
-                    const float w = exp2f(mj[q] - Mn);
+                    // 0 on the first piece (M = -inf); a piece that saw no key weighs 0
+                    const float sc = M == -INFINITY ? 0.0f : exp2f(M - Mn);
+                    const float w = mj[q] == -INFINITY ? 0.0f : exp2f(mj[q] - Mn);
                     den = den * sc + w * lj[q];
                     num.x = num.x * sc + w * aj[q].x;
                     num.y = num.y * sc + w * aj[q].y;
@@ -87,9 +94,14 @@ __global__ void __launch_bounds__(kCombineThreads)
                     M = Mn;
                 }
             }
-            const float inv = 1.0f / den;
-            // output rows of segment u start at (b H + kvh G) D = u G D (H = KVH G)
-            store_out4(p, static_cast<size_t>(u) * G * D + static_cast<size_t>(f4) * 4,
+            // no key in any piece: the empty sum (a NaN normaliser from a bad page stays NaN)
+            const float inv = den == 0.0f ? 0.0f : 1.0f / den;
+            // row t * G + g of segment u = (b, kvh) is output row (b T + t) H + kvh G + g
+            // of [B, T, H, D] (for T = 1: u G + g)
+            const int KVH = p.KVH;
+            const int b = u / KVH, kvh = u - b * KVH, t = h / G, g = h - t * G;
+            const size_t row = (static_cast<size_t>(b) * T + t) * p.H + kvh * G + g;
+            store_out4(p, row * D + (f4 * 4 - h * D),
                        make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv));
         }
         __syncthreads();   // seg_s is refilled for the next group of items

@@ -91,6 +91,8 @@ struct DecodeParams {
     int num_pages;                // P (paged)
     int max_pages;                // block-table row length (paged)
     int out_f32;                  // 1: fp32 output, 0: bf16
+    int T;                        // query tokens per sequence, at positions L - T .. L - 1
+                                  // (0 or 1: the single decode token at L - 1)
     // single K=V cache (policies with kKeqV): the k_norm weight [D] and the rotary
     // frequencies theta^(-2i/D) of the rotated pairs, in fp64
     const __nv_bfloat16* w_k;
@@ -312,7 +314,10 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
                 bad = b < B;
                 x = x < 0 ? 0 : p.capacity;
             }
-            const int lo = (p.window > 0 && x > p.window) ? x - p.window : 0;
+            // union of the queries' ranges: query 0 (position x - T) starts the
+            // earliest window, the last query ends at x
+            const int span = p.window > 0 ? p.window + (p.T > 1 ? p.T - 1 : 0) : 0;
+            const int lo = (span > 0 && x > span) ? x - span : 0;
             n[j] = b < B ? x - lo : 0;
             if (b < B) {
                 pl.lo[b] = lo;

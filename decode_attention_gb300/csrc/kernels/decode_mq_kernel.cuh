@@ -1,0 +1,690 @@
+// Multi-query decode attention on the 5th-generation tensor cores (tcgen05).
+//
+// Operation ("Gemma 4 31B-it Text Architecture", "Inference behavior: Prefill,
+// Cache, and Long Context" and "Compact form"; gemma-4-31B Model Spec, the two
+// attn.core rows): a step appends T new tokens per sequence to the cache, then
+// query t, at position p = L - T + t, attends to the keys s <= p (full layers) or
+// p - W < s <= p (sliding layers), with scale 1; the g query heads of a KV head
+// share its keys and values.  A query at a negative position sees nothing (o = 0).
+//
+// Orientation.  A segment (b, kvh) has R = T * g query rows (r = t * g + h, at
+// most 32).  Tiles of 128 positions fill the M dimension of a cta_group::1 mma,
+// so both contractions run transposed:
+//   scores  S^T[pos, r]  = sum_d K[pos, d] Q[r, d]          A = K tile (K-major),
+//                                                          B = Q (K-major)
+//   P.V     O^T[d, r]   += sum_pos V^T[d, pos] P^T[pos, r]  A = the V tile read
+//                                                          MN-major, B = P (K-major)
+// with N = R rounded up to 16.  S^T (two buffers) and O^T (D/128 blocks of 128
+// head-dim lanes) live in TMEM.  One K or V stage is 128 positions x 64 head-dim
+// elements (16 KB, 128-byte swizzled, exactly what TMA writes); the P.V mma of a
+// 128-wide head-dim block reads two adjacent stages.
+//
+// Warp roles (192 threads).  Warp 0, lane 0: the producer.  It walks the same
+// schedule as the single-query kernel (static units, then claimed dynamic chunks)
+// and streams the tiles in the order K(0), K(1), V(0), K(2), V(1), ...: the scores
+// of tile i+1 are computed while the softmax of tile i runs.  It also loads each
+// piece's Q with TMA (box: 64 elements x g heads x T tokens) into one of two
+// buffers.  Warp 1: owns the TMEM allocation; lane 0 issues every mma and commit;
+// the whole warp zeroes the V rows of a tile that lie outside its sequence's
+// attended range before the P.V mma reads them (0 * NaN would poison the sum).
+// Warps 2..5: thread j owns TMEM lane j, i.e. position j of the tile's scores and
+// head-dim element j of each O^T block; they run the softmax and the epilogue.
+//
+// Softmax.  Each query row keeps a reference max m (log2 units) that all threads
+// share; P = exp2(s - m), and m moves only when a score of the tile exceeds it by
+// more than kMqTau (then the O^T columns and the normaliser shares are rescaled
+// by exp2(m_old - m_new)).  P <= 2^kMqTau keeps every fp32 sum finite.  P is
+// applied as a bf16 hi part and a bf16 lo part (two mma into the same
+// accumulator), about 16 significant bits.  The epilogue of a piece writes the
+// normalised output, or the partial (acc, m, l) that the combine kernel merges.
+//
+// Every wait is bounded; a wait that gives up raises the status word's timeout
+// bit, the roles leave together, in-flight copies and mma are drained, and TMEM is
+// released before the CTA exits.
+#pragma once
+
+#include "decode_kernel.cuh"
+
+namespace gqa {
+
+constexpr int kMqTile = 128;                       // positions per tile (mma M)
+constexpr int kMqStageBytes = kMqTile * 128;       // 128 rows x 64 bf16
+constexpr float kMqTau = 24.0f;                    // rescale threshold, log2 units
+constexpr int kMqPLbo = 144;                       // P core matrices along positions (padded
+                                                   // from 128 B so stores hit distinct banks)
+constexpr int kMqPSbo = (kMqTile / 8) * kMqPLbo;   // P 8-row groups: 2304 B
+constexpr int kMqThreads = 192;
+constexpr int kMqSoftmaxThreads = 128;
+
+constexpr int tmem_cols_for(int cols) {
+    int c = 32;
+    while (c < cols) c *= 2;
+    return c;
+}
+
+template <int kD, int kG, int kMaxT, int kStages>
+struct MqCfg {
+    static constexpr int D = kD, G = kG, MAXT = kMaxT, STAGES = kStages;
+    static constexpr int NSUB = D / 64;                 // stages per tile of one tensor
+    static constexpr int NB = D / 128;                  // 128-wide head-dim blocks of O^T
+    static constexpr int RMAX = G * MAXT;               // query rows of a segment
+    static constexpr int NMAX = RMAX <= 16 ? 16 : 32;   // mma N bound
+    static constexpr int QATOM = NMAX * 128;            // Q rows of one 64-element column block
+    static constexpr int QBYTES = NSUB * QATOM;
+    static constexpr int PBYTES = (NMAX / 8) * kMqPSbo; // one P part (hi or lo)
+    static constexpr int TMEM_S = 0;                    // S^T buffers: columns [0, 2 NMAX)
+    static constexpr int TMEM_O = 2 * NMAX;             // O^T blocks: NB x NMAX columns
+    static constexpr int TMEM_COLS = tmem_cols_for(TMEM_O + NB * NMAX);
+    static_assert(STAGES % 2 == 0, "a P.V block reads two adjacent stages");
+    static_assert(NSUB % 2 == 0 && RMAX <= 32, "geometry");
+    static_assert(RMAX == NMAX, "query rows fill the mma N bound");
+};
+
+using MqGlobal = MqCfg<512, 8, 4, 6>;     // decodeGQA, T <= 4
+using MqSliding = MqCfg<256, 2, 8, 10>;   // slidingDecodeGQA, T <= 8
+
+struct MqTile {
+    int b, kvh;
+    int t;          // position of tile row 0 (= its cache row on a contiguous cache)
+    int vlo, vhi;   // rows [vlo, vhi) belong to this piece
+    int zlo, zhi;   // rows outside [zlo, zhi) lie outside the sequence's attended range
+    int slot;       // workspace slot of the piece
+    int flags;      // kDescFirst / kDescLast of the piece, kDescDone
+    int qb;         // Q buffer of the piece
+};
+
+constexpr int kMqKindK = 0, kMqKindV = 1, kMqKindDone = 2;
+
+template <class Cfg>
+struct alignas(1024) MqSmem {
+    uint8_t stage[Cfg::STAGES][kMqStageBytes];   // K or V: [128 rows][128 B], swizzled
+    uint8_t q[2][Cfg::QBYTES];                    // [column block][NMAX rows][128 B], swizzled
+    uint8_t pm[2][2][Cfg::PBYTES];                // P^T [buffer][hi, lo], core-matrix layout
+    alignas(8) uint64_t full[Cfg::STAGES];
+    alignas(8) uint64_t empty[Cfg::STAGES];
+    alignas(8) uint64_t q_empty[2];   // last scores of the piece using Q buffer j done
+    alignas(8) uint64_t s_full[2];    // scores of tile i in S buffer i % 2 (+ its tile)
+    alignas(8) uint64_t p_full[2];    // P of tile i written (softmax warps)
+    alignas(8) uint64_t p_empty[2];   // P.V of tile i no longer reads P buffer i % 2
+    alignas(8) uint64_t o_ready[2];   // P.V of tile i complete
+    alignas(8) uint64_t drain;        // the mma warp's final commit
+    int kind[Cfg::STAGES];
+    MqTile desc[Cfg::STAGES];         // tile of a K block (its first stage)
+    MqTile s_desc[2];                 // tile whose scores are in S buffer j
+    PlanSmem plan;
+    float red[4][Cfg::NMAX];
+    uint32_t red_bad[4];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Byte offset of P^T element (query row r, tile position j): K-major, no swizzle.
+__device__ __forceinline__ uint32_t mq_p_off(int r, int j) {
+    return (j >> 3) * kMqPLbo + (r >> 3) * kMqPSbo + (r & 7) * 16 + (j & 7) * 2;
+}
+
+template <class Cfg, bool kPaged>
+__global__ void __launch_bounds__(kMqThreads, 1)
+    gqa_mq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+    constexpr int D = Cfg::D, G = Cfg::G, NSUB = Cfg::NSUB, NB = Cfg::NB, STAGES = Cfg::STAGES;
+    constexpr int NMAX = Cfg::NMAX, RMAX = Cfg::RMAX, MAXT = Cfg::MAXT;
+
+    extern __shared__ uint8_t smem_raw[];
+    MqSmem<Cfg>& sm = *reinterpret_cast<MqSmem<Cfg>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int B = p.B, KVH = p.KVH, H = p.H;
+    const int T = p.T > 1 ? p.T : 1;
+    const int R = T * G;
+    const int N = (R + 15) & ~15;   // mma N
+    const int cta = blockIdx.x;
+    PlanSmem& pl = sm.plan;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&sm.full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sm.empty[s]), 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            ptx::mbar_init(ptx::smem_addr(&sm.q_empty[j]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sm.s_full[j]), 2);   // mma commit + the tile's descriptor
+            ptx::mbar_init(ptx::smem_addr(&sm.p_full[j]), 4);   // one arrival per softmax warp
+            ptx::mbar_init(ptx::smem_addr(&sm.p_empty[j]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sm.o_ready[j]), 1);
+        }
+        ptx::mbar_init(ptx::smem_addr(&sm.drain), 1);
+        ptx::fence_mbar_init();
+        sm.abort_flag = 0;
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+        ptx::prefetch_tensormap(&tm_q);
+    }
+    ptx::grid_dependency_wait();
+    ptx::allow_dependent_launch();
+
+    if (warp == 0) build_plan(pl, p, gridDim.x, lane, cta, kMqTile);
+    __syncthreads();
+
+    // sequences with nothing to attend produce zeros for all T queries
+    for (int b = cta; b < B; b += gridDim.x) {
+        if (pl.n[b] != 0) continue;
+        const size_t base = static_cast<size_t>(b) * T * H * D;
+        for (int i = tid; i < T * H * D; i += blockDim.x) store_out(p, base + i, 0.0f);
+    }
+    // partial list of every segment, for the combine kernel
+    {
+        const int U = B * KVH;
+        const int u_end = static_cast<int>(static_cast<long long>(cta + 1) * U / gridDim.x);
+        for (int u = static_cast<int>(static_cast<long long>(cta) * U / gridDim.x) + tid; u < u_end;
+             u += blockDim.x) {
+            const int b = u / KVH, kvh = u - (u / KVH) * KVH;
+            int4 e = make_int4(0, 0, 0, 0);
+            if (pl.n[b] != 0 && pl.g_eff > 0) {
+                const SegmentParts sp(pl, b, kvh, p.dyn_slot_base);
+                e = make_int4(sp.first_s, sp.ns_parts, sp.dk0, sp.nd_parts);
+            }
+            p.ws_segs[u] = e;
+        }
+    }
+    if (cta >= pl.g_eff) return;   // also covers an all-empty batch
+
+    if (warp == 1) ptx::tmem_alloc(ptx::smem_addr(&sm.tmem_base), Cfg::TMEM_COLS);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    const uint32_t stage0 = ptx::smem_addr(&sm.stage[0][0]);
+
+    if (warp == 0) {
+        // ============================ producer ============================
+        if (lane == 0) {
+            const uint64_t policy = ptx::policy_evict_first();
+            const uint32_t q_bytes = static_cast<uint32_t>(NSUB * R * 128);
+            constexpr uint32_t kPageBytes = kPageRows * 128;
+            uint32_t seq = 0;        // stages issued
+            uint32_t n_piece = 0;    // pieces started (Q buffer n_piece & 1)
+            bool ok = true;
+            const bool dynamic = pl.n_dyn > 0;
+            int claimed = -1;
+            MqTile prev;
+            bool have_prev = false;
+
+            // One block (NSUB stages) of tile d: its K or V rows, or (kind Done) empty stages.
+            auto emit_block = [&](const MqTile& d, int kind) -> bool {
+                const int32_t* bt_row =
+                    kPaged ? p.block_table + static_cast<size_t>(d.b) * p.max_pages : nullptr;
+                // paged: load the pages that hold attended positions of the sequence
+                const int npage = kPaged ? (d.zhi + kPageRows - 1) / kPageRows : 0;
+                for (int sub = 0; sub < NSUB; ++sub) {
+                    const int s = seq % STAGES;
+                    const uint32_t ph = (seq / STAGES) & 1u;
+                    if (!wait_bounded(ptx::smem_addr(&sm.empty[s]), ph ^ 1u, &sm.abort_flag, p.ws_flags))
+                        return false;
+                    sm.kind[s] = kind;
+                    const uint32_t full_bar = ptx::smem_addr(&sm.full[s]);
+                    if (kind == kMqKindDone) {
+                        ptx::mbar_arrive(full_bar);
+                        ++seq;
+                        continue;
+                    }
+                    const bool with_q = kind == kMqKindK && sub == 0 && (d.flags & kDescFirst);
+                    if (kind == kMqKindK && sub == 0) sm.desc[s] = d;
+                    const uint32_t bytes =
+                        (kPaged ? static_cast<uint32_t>(npage) * kPageBytes : kMqStageBytes) +
+                        (with_q ? q_bytes : 0u);
+                    ptx::mbar_arrive_expect_tx(full_bar, bytes);
+                    if (with_q) {
+                        const uint32_t qdst = ptx::smem_addr(&sm.q[d.qb][0]);
+                        for (int c = 0; c < NSUB; ++c)
+                            ptx::tma_load_4d(qdst + c * Cfg::QATOM, &tm_q, full_bar, 64 * c, d.kvh * G,
+                                             0, d.b, policy);
+                    }
+                    const CUtensorMap* map = kind == kMqKindK ? &tm_k : &tm_v;
+                    const uint32_t dst = stage0 + s * kMqStageBytes;
+                    const int chunk = d.kvh * NSUB + sub;
+                    if (kPaged) {
+                        for (int j = 0; j < npage; ++j) {
+                            int page = bt_row[(d.t >> 4) + j];
+                            if (page < 0 || page >= p.num_pages) page = 0;   // flagged by the softmax warps
+                            ptx::tma_load_4d(dst + j * kPageBytes, map, full_bar, 0, 0, chunk, page, policy);
+                        }
+                    } else {
+                        // rows past the end of the cache read as zeros
+                        ptx::tma_load_4d(dst, map, full_bar, 0, d.t, chunk, d.b, policy);
+                    }
+                    ++seq;
+                }
+                return true;
+            };
+            auto emit_tile = [&](MqTile cur) -> bool {
+                if (!emit_block(cur, kMqKindK)) return false;
+                if (have_prev && !emit_block(prev, kMqKindV)) return false;
+                prev = cur;
+                have_prev = true;
+                return true;
+            };
+            // The tiles of positions [p0, p1) of segment (b, kvh).
+            auto emit_piece = [&](int b, int kvh, int p0, int p1, int slot, bool unit_end) -> bool {
+                const uint32_t qb = n_piece & 1u;
+                if (!wait_bounded(ptx::smem_addr(&sm.q_empty[qb]), ((n_piece >> 1) & 1u) ^ 1u,
+                                  &sm.abort_flag, p.ws_flags))
+                    return false;
+                ++n_piece;
+                const int lo = pl.lo[b], L = lo + pl.n[b];
+                const int t_first = kPaged ? (p0 & ~(kPageRows - 1)) : p0;
+                for (int t = t_first; t < p1; t += kMqTile) {
+                    const bool last = t + kMqTile >= p1;
+                    if (dynamic && unit_end && last)
+                        claimed = static_cast<int>(atomicAdd(p.ws_claim, 1u));
+                    MqTile d;
+                    d.b = b;
+                    d.kvh = kvh;
+                    d.t = t;
+                    d.vlo = (p0 > t ? p0 : t) - t;
+                    d.vhi = (p1 < t + kMqTile ? p1 : t + kMqTile) - t;
+                    d.zlo = lo > t ? lo - t : 0;
+                    d.zhi = L < t + kMqTile ? L - t : kMqTile;
+                    d.slot = slot;
+                    d.flags = (t == t_first ? kDescFirst : 0) | (last ? kDescLast : 0);
+                    d.qb = static_cast<int>(qb);
+                    if (!emit_tile(d)) return false;
+                }
+                return true;
+            };
+
+            // the static unit of this CTA, then dynamic chunks (as in the single-query kernel)
+            long long pos = static_unit_begin(pl, cta);
+            const long long stop = static_unit_begin(pl, cta + 1);
+            while (ok && pos < stop) {
+                const int b = upper_seq(pl.spref, B, pos);
+                const int sn = pl.sn[b];
+                const long long rel = pos - pl.spref[b];
+                const int kvh = static_cast<int>(rel / sn);
+                const int off = static_cast<int>(rel - static_cast<long long>(kvh) * sn);
+                const int take = static_cast<int>(stop - pos < sn - off ? stop - pos : sn - off);
+                pos += take;
+                const int p0 = pl.lo[b] + off;
+                ok = emit_piece(b, kvh, p0, p0 + take, cta + b * KVH + kvh, pos >= stop);
+            }
+            while (ok && dynamic) {
+                if (claimed < 0) claimed = static_cast<int>(atomicAdd(p.ws_claim, 1u));
+                const int k = claimed;
+                claimed = -1;
+                if (k >= pl.n_dyn) break;
+                const bool is_long = k < pl.n_dyn0;
+                const int kk = is_long ? k : k - pl.n_dyn0;
+                const int* pref = is_long ? pl.dpref : pl.dpref1;
+                const int b = upper_seq(pref, B, kk);
+                const int per = is_long ? pl.dn[b] : pl.dn1[b];
+                const int rel = kk - pref[b];
+                const int kvh = rel / per;
+                const int idx = rel - kvh * per;
+                const int len = is_long ? pl.c_dyn : pl.c_dyn1;
+                const int local = is_long ? idx : pl.dn[b] + idx;
+                const int p0 = pl.lo[b] + pl.sn[b] + (is_long ? 0 : pl.dn[b] * pl.c_dyn) + idx * len;
+                const int slot = p.dyn_slot_base + pl.dpref[b] + pl.dpref1[b] +
+                                 kvh * (pl.dn[b] + pl.dn1[b]) + local;
+                ok = emit_piece(b, kvh, p0, p0 + len, slot, true);
+            }
+            // end of work: a Done block where the next K block would be, then the
+            // last tile's V block
+            if (ok) {
+                MqTile none;
+                none.b = none.kvh = none.t = none.vlo = none.vhi = none.zlo = none.zhi = 0;
+                none.slot = none.qb = 0;
+                none.flags = kDescDone;
+                ok = emit_block(none, kMqKindDone);
+                if (ok && have_prev) ok = emit_block(prev, kMqKindV);
+            }
+            if (!ok) {
+                // let every copy already issued land before the CTA exits
+                const uint32_t first = seq > static_cast<uint32_t>(STAGES) ? seq - STAGES : 0u;
+                for (uint32_t tt = first; tt < seq; ++tt)
+                    wait_drain(ptx::smem_addr(&sm.full[tt % STAGES]), (tt / STAGES) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ====================== mma issue (lane 0) + V fix-up (warp) ======================
+        const uint32_t idesc_s = ptx::idesc_bf16_f32(kMqTile, N, 0, 0);
+        const uint32_t idesc_o = ptx::idesc_bf16_f32(kMqTile, N, 1, 0);
+        uint32_t seq = 0;
+        uint32_t i_s = 0, i_pv = 0;   // tiles whose scores / P.V were issued
+        MqTile pend[2];               // tiles between their scores and their P.V
+        bool done = false;
+        auto wait_full = [&](uint32_t sq) -> bool {
+            return __all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&sm.full[sq % STAGES]),
+                                                         (sq / STAGES) & 1u, &sm.abort_flag, p.ws_flags));
+        };
+        while (!(done && i_pv == i_s)) {
+            if (!wait_full(seq)) break;
+            ptx::tc_fence_after();
+            const int kind = sm.kind[seq % STAGES];
+            if (kind == kMqKindDone) {
+                bool ok = true;
+                for (int sub = 0; sub < NSUB && ok; ++sub) {
+                    if (sub > 0) ok = wait_full(seq);
+                    if (ok && lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.empty[seq % STAGES]));
+                    ++seq;
+                }
+                if (!ok) break;
+                // no tile i_s: the softmax warps leave
+                if (lane == 0) {
+                    sm.s_desc[i_s & 1].flags = kDescDone;
+                    ptx::mbar_arrive(ptx::smem_addr(&sm.s_full[i_s & 1]));
+                    ptx::mbar_arrive(ptx::smem_addr(&sm.s_full[i_s & 1]));
+                }
+                done = true;
+                continue;
+            }
+            if (kind == kMqKindK) {
+                // ---- scores of tile i: S^T[pos, r] over the NSUB column blocks ----
+                const MqTile d = sm.desc[seq % STAGES];
+                const uint32_t i = i_s++;
+                const uint32_t s_col = tmem + Cfg::TMEM_S + (i & 1u) * NMAX;
+                const uint32_t qbase = ptx::smem_addr(&sm.q[d.qb][0]);
+                bool ok = true;
+                for (int sub = 0; sub < NSUB; ++sub) {
+                    if (sub > 0) {
+                        ok = wait_full(seq);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                    }
+                    const int s = seq % STAGES;
+                    if (lane == 0) {
+                        const uint32_t a0 = stage0 + s * kMqStageBytes;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = ptx::smem_desc(a0 + kk * 32, 16, 1024, ptx::kSwizzle128B);
+                            const uint64_t bq = ptx::smem_desc(qbase + sub * Cfg::QATOM + kk * 32, 16,
+                                                               1024, ptx::kSwizzle128B);
+                            ptx::umma_ss(s_col, a, bq, idesc_s, (sub | kk) != 0 ? 1u : 0u);
+                        }
+                        ptx::umma_commit(ptx::smem_addr(&sm.empty[s]));
+                    }
+                    __syncwarp();
+                    ++seq;
+                }
+                if (!ok) break;
+                if (lane == 0) {
+                    if (d.flags & kDescLast) ptx::umma_commit(ptx::smem_addr(&sm.q_empty[d.qb]));
+                    ptx::umma_commit(ptx::smem_addr(&sm.s_full[i & 1u]));
+                    sm.s_desc[i & 1u] = d;
+                    ptx::mbar_arrive(ptx::smem_addr(&sm.s_full[i & 1u]));
+                }
+                pend[i & 1u] = d;
+                __syncwarp();
+                continue;
+            }
+            // ---- P.V of tile i: O^T[d, r] += V^T[d, pos] P^T[pos, r] ----
+            const uint32_t i = i_pv++;
+            const MqTile d = pend[i & 1u];
+            if (!__all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&sm.p_full[i & 1u]), (i >> 1) & 1u,
+                                                      &sm.abort_flag, p.ws_flags)))
+                break;
+            ptx::tc_fence_after();
+            const bool fix = d.zlo > 0 || d.zhi < kMqTile;
+            const uint32_t ph_base = ptx::smem_addr(&sm.pm[i & 1u][0][0]);
+            const uint32_t pl_base = ptx::smem_addr(&sm.pm[i & 1u][1][0]);
+            bool ok = true;
+            for (int mb = 0; mb < NB; ++mb) {
+                // the two stages of head-dim block mb (adjacent: seq is even here)
+                if (mb > 0) ok = wait_full(seq);
+                ok = ok && wait_full(seq + 1);
+                if (!ok) break;
+                const int s = seq % STAGES;
+                if (fix) {
+                    // rows outside the attended range of the sequence may hold anything
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t st = stage0 + (s + h) * kMqStageBytes;
+                        for (int row = lane; row < kMqTile; row += 32) {
+                            if (row >= d.zlo && row < d.zhi) continue;
+                            const uint32_t ra = st + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) ptx::sts128(ra + u * 16, 0u, 0u, 0u, 0u);
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                }
+                __syncwarp();
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t a0 = stage0 + s * kMqStageBytes;
+                    const uint32_t o_col = tmem + Cfg::TMEM_O + mb * NMAX;
+#pragma unroll
+                    for (int kk = 0; kk < kMqTile / 16; ++kk) {
+                        const uint64_t a = ptx::smem_desc(a0 + kk * 2048, kMqStageBytes, 1024,
+                                                          ptx::kSwizzle128B);
+                        const uint64_t bh = ptx::smem_desc(ph_base + kk * 2 * kMqPLbo, kMqPLbo, kMqPSbo,
+                                                           ptx::kSwizzleNone);
+                        const uint64_t bl = ptx::smem_desc(pl_base + kk * 2 * kMqPLbo, kMqPLbo, kMqPSbo,
+                                                           ptx::kSwizzleNone);
+                        ptx::umma_ss(o_col, a, bh, idesc_o,
+                                     ((d.flags & kDescFirst) && kk == 0) ? 0u : 1u);
+                        ptx::umma_ss(o_col, a, bl, idesc_o, 1u);
+                    }
+                    ptx::umma_commit(ptx::smem_addr(&sm.empty[s]));
+                    ptx::umma_commit(ptx::smem_addr(&sm.empty[s + 1]));
+                }
+                __syncwarp();
+                seq += 2;
+            }
+            if (!ok) break;
+            if (lane == 0) {
+                ptx::umma_commit(ptx::smem_addr(&sm.o_ready[i & 1u]));
+                ptx::umma_commit(ptx::smem_addr(&sm.p_empty[i & 1u]));
+            }
+            __syncwarp();
+        }
+        // every mma issued has completed before TMEM is released
+        if (lane == 0) {
+            ptx::umma_commit(ptx::smem_addr(&sm.drain));
+            wait_drain(ptx::smem_addr(&sm.drain), 0u);
+        }
+        __syncwarp();
+    } else {
+        // ====================== softmax and epilogue (warps 2..5) ======================
+        const int j = 32 * (warp & 3) + lane;   // TMEM lane: tile position / head-dim element
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+        const float nan = __uint_as_float(0x7fc00000u);
+        float m_ref[RMAX], l_part[RMAX];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+            m_ref[r] = -INFINITY;
+            l_part[r] = 0.0f;
+        }
+        uint32_t bad_q = 0;   // bit t: query t attended a bad page in this piece
+        for (uint32_t i = 0;; ++i) {
+            bool ok = wait_bounded(ptx::smem_addr(&sm.s_full[i & 1u]), (i >> 1) & 1u, &sm.abort_flag,
+                                   p.ws_flags);
+            if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
+            ptx::tc_fence_after();
+            const MqTile d = sm.s_desc[i & 1u];
+            if (d.flags & kDescDone) break;
+            if (d.flags & kDescFirst) {
+#pragma unroll
+                for (int r = 0; r < RMAX; ++r) {
+                    m_ref[r] = -INFINITY;
+                    l_part[r] = 0.0f;
+                }
+                bad_q = 0;
+            }
+            const int L = pl.lo[d.b] + pl.n[d.b];
+            const int pos = d.t + j;
+            const bool in_piece = j >= d.vlo && j < d.vhi;
+            bool page_bad = false;
+            if (kPaged && in_piece) {
+                const int page = p.block_table[static_cast<size_t>(d.b) * p.max_pages + (pos >> 4)];
+                page_bad = page < 0 || page >= p.num_pages;
+            }
+            // scores of position j, log2 units, masked per query
+            uint32_t sr0[16], sr1[16];
+            ptx::tmem_ld16(lane_addr + Cfg::TMEM_S + (i & 1u) * NMAX, sr0);
+            if (N > 16) ptx::tmem_ld16(lane_addr + Cfg::TMEM_S + (i & 1u) * NMAX + 16, sr1);
+            ptx::tmem_wait_ld();
+            float s[RMAX];
+            bool need = false;
+#pragma unroll
+            for (int t = 0; t < MAXT; ++t) {
+                const int hi_t = L - T + t + 1;
+                const int lo_t = (p.window > 0 && hi_t > p.window) ? hi_t - p.window : 0;
+                const bool valid = t < T && in_piece && pos >= lo_t && pos < hi_t;
+                if (valid && page_bad) bad_q |= 1u << t;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const int r = t * G + g;
+                    const uint32_t raw = r < 16 ? sr0[r & 15] : sr1[r & 15];
+                    s[r] = valid ? __uint_as_float(raw) * kLog2e : -INFINITY;
+                    need |= s[r] > m_ref[r] + kMqTau;
+                }
+            }
+            if (ptx::named_barrier_or(2, kMqSoftmaxThreads, need)) {
+                // new reference max of every row: the tile's max where it is larger
+#pragma unroll
+                for (int r = 0; r < RMAX; ++r) {
+                    float mx = s[r];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    if (lane == 0) sm.red[warp & 3][r] = mx;
+                }
+                ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+                float alpha[RMAX];
+#pragma unroll
+                for (int r = 0; r < RMAX; ++r) {
+                    const float mt = fmaxf(fmaxf(sm.red[0][r], sm.red[1][r]), fmaxf(sm.red[2][r], sm.red[3][r]));
+                    const float mn = fmaxf(m_ref[r], mt);
+                    alpha[r] = (m_ref[r] == -INFINITY || mn == -INFINITY) ? 0.0f : exp2f(m_ref[r] - mn);
+                    m_ref[r] = mn;
+                }
+                ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+                if (!(d.flags & kDescFirst)) {
+                    // O^T holds the earlier tiles of this piece: rescale it once their
+                    // P.V is complete (the P.V of this tile waits for p_full)
+                    const uint32_t ip = i - 1;
+                    ok = wait_bounded(ptx::smem_addr(&sm.o_ready[ip & 1u]), (ip >> 1) & 1u,
+                                      &sm.abort_flag, p.ws_flags);
+                    if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int mb = 0; mb < NB; ++mb) {
+#pragma unroll
+                        for (int c0 = 0; c0 < NMAX; c0 += 16) {
+                            if (c0 >= N) break;
+                            uint32_t o[16];
+                            const uint32_t ta = lane_addr + Cfg::TMEM_O + mb * NMAX + c0;
+                            ptx::tmem_ld16(ta, o);
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[c0 + c]);
+                            ptx::tmem_st16(ta, o);
+                        }
+                    }
+                    ptx::tmem_wait_st();
+#pragma unroll
+                    for (int r = 0; r < RMAX; ++r) l_part[r] *= alpha[r];
+                }
+            }
+            // P buffer i % 2 is free once the P.V of tile i - 2 is done
+            ok = wait_bounded(ptx::smem_addr(&sm.p_empty[i & 1u]), ((i >> 1) & 1u) ^ 1u, &sm.abort_flag,
+                              p.ws_flags);
+            if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
+            {
+                const uint32_t ph = ptx::smem_addr(&sm.pm[i & 1u][0][0]);
+                const uint32_t plo = ptx::smem_addr(&sm.pm[i & 1u][1][0]);
+#pragma unroll
+                for (int r = 0; r < NMAX; ++r) {
+                    if (r >= N) break;
+                    // rows past R (padding up to N) stay zero
+                    const float pv = (r < R && s[r] != -INFINITY) ? exp2f(s[r] - m_ref[r]) : 0.0f;
+                    l_part[r] += pv;
+                    const __nv_bfloat16 hb = __float2bfloat16_rn(pv);
+                    const __nv_bfloat16 lb = __float2bfloat16_rn(pv - __bfloat162float(hb));
+                    const uint32_t off = mq_p_off(r, j);
+                    ptx::sts16(ph + off, *reinterpret_cast<const uint16_t*>(&hb));
+                    ptx::sts16(plo + off, *reinterpret_cast<const uint16_t*>(&lb));
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.p_full[i & 1u]));
+            if (!(d.flags & kDescLast)) continue;
+
+            // ---------------- epilogue of the piece ----------------
+            ok = wait_bounded(ptx::smem_addr(&sm.o_ready[i & 1u]), (i >> 1) & 1u, &sm.abort_flag,
+                              p.ws_flags);
+            if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
+            ptx::tc_fence_after();
+            float l[RMAX];
+#pragma unroll
+            for (int r = 0; r < RMAX; ++r) {
+                float v = l_part[r];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == 0) sm.red[warp & 3][r] = v;
+            }
+            const uint32_t bq = __reduce_or_sync(0xffffffffu, bad_q);
+            if (lane == 0) sm.red_bad[warp & 3] = bq;
+            ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+#pragma unroll
+            for (int r = 0; r < RMAX; ++r) l[r] = (sm.red[0][r] + sm.red[1][r]) + (sm.red[2][r] + sm.red[3][r]);
+            const uint32_t bad_all = sm.red_bad[0] | sm.red_bad[1] | sm.red_bad[2] | sm.red_bad[3];
+            ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+            if (bad_all && j == 0) atomicOr(p.ws_flags, kFlagBadPage);
+            const SegmentParts sp(pl, d.b, d.kvh, p.dyn_slot_base);
+            const bool direct = sp.count() == 1;
+#pragma unroll
+            for (int mb = 0; mb < NB; ++mb) {
+#pragma unroll
+                for (int c0 = 0; c0 < NMAX; c0 += 16) {
+                    if (c0 >= N) break;
+                    uint32_t o[16];
+                    ptx::tmem_ld16(lane_addr + Cfg::TMEM_O + mb * NMAX + c0, o);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int r = c0 + c;
+                        if (r >= R) break;
+                        const int t = r / G, g = r - (r / G) * G;
+                        const bool bad = (bad_all >> t) & 1u;
+                        const int dd = mb * 128 + j;
+                        const float acc = __uint_as_float(o[c]);
+                        if (direct) {
+                            const size_t row = (static_cast<size_t>(d.b) * T + t) * H + d.kvh * G + g;
+                            // no key at all: the empty sum (a NaN normaliser stays NaN)
+                            store_out(p, row * D + dd, bad ? nan : (l[r] == 0.0f ? 0.0f : acc / l[r]));
+                        } else {
+                            p.ws_acc[(static_cast<size_t>(d.slot) * R + r) * D + dd] = bad ? nan : acc;
+                        }
+                    }
+                }
+            }
+            if (!direct && j < R) {
+                const bool bad = (bad_all >> (j / G)) & 1u;
+                float mj = 0.0f, lj = 0.0f;
+#pragma unroll
+                for (int r = 0; r < RMAX; ++r)
+                    if (r == j) {
+                        mj = m_ref[r];
+                        lj = l[r];
+                    }
+                float* ml = p.ws_ml + (static_cast<size_t>(d.slot) * R + j) * 2;
+                ml[0] = bad ? 0.0f : mj;
+                ml[1] = bad ? nan : lj;
+            }
+            ptx::tc_fence_before();
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem, Cfg::TMEM_COLS);
+}
+
+}  // namespace gqa

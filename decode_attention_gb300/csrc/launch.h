@@ -33,6 +33,12 @@ cudaError_t launch_global(const LaunchArgs& a, bool paged);
 // decodeGQA over a single K=V cache: a.k and a.v are both the value cache.
 cudaError_t launch_global_keqv(const LaunchArgs& a, bool paged);
 
+// Multi-query decode (tcgen05): a.p.T query tokens per sequence, q [B, T, H, D],
+// out [B, T, H, D]; at most mq_max_queries(sliding) tokens.
+cudaError_t launch_mq(const LaunchArgs& a, bool sliding, bool paged);
+int mq_max_queries(bool sliding);
+size_t smem_bytes_mq(bool sliding);
+
 // Bytes of dynamic shared memory each geometry's kernel requests.
 size_t smem_bytes_sliding();
 size_t smem_bytes_global();

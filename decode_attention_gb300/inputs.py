@@ -255,3 +255,21 @@ def paged_case(B: int, H: int, KVH: int, D: int, seq_lens, seed: int, max_pages:
         seq_lens=lens,
     )
 
+
+
+def mq_case(B: int, T: int, S: int, H: int, KVH: int, D: int, seq_lens, seed: int,
+            device="cpu") -> dict:
+    """Multi-query step: q [B,T,H,D] (T new tokens per sequence), k/v [B,S,KVH,D]
+    (bf16) already holding the new tokens' rows, seq_lens [B] (lengths after them)."""
+    case = contiguous_case(B, S, H, KVH, D, seq_lens, seed, device)
+    case["q"] = rms_normalised_bf16((B, T, H, D), tensor_seed(seed, "q"), device)
+    return case
+
+
+def paged_mq_case(B: int, T: int, H: int, KVH: int, D: int, seq_lens, seed: int,
+                  max_pages: int | None = None, device="cpu", spare_pages: int = 0,
+                  table=None) -> dict:
+    """paged_case with a multi-query q [B,T,H,D]."""
+    case = paged_case(B, H, KVH, D, seq_lens, seed, max_pages, device, spare_pages, table)
+    case["q"] = rms_normalised_bf16((B, T, H, D), tensor_seed(seed, "q"), device)
+    return case

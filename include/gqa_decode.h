@@ -299,6 +299,53 @@ gqa_status_t gqa_prepare_decode_paged(const void *q_raw, const void *k_raw, cons
                                       gqa_stream_t stream);
 
 /*
+ * Multi-query decode: T new tokens per sequence attend in one call (speculative
+ * decoding's draft tokens, or a short chunk of prefill).  "Gemma 4 31B-it Text
+ * Architecture", "Inference behavior: Prefill, Cache, and Long Context" and
+ * "Compact form": the step's positions are past_seen_tokens + arange(T), the new
+ * K/V rows are appended before attention, and every query keeps its own mask
+ * (keys s <= t on full layers, t - 1024 < s <= t on sliding layers).  With L_b =
+ * seq_lens[b] the length AFTER the append, query t (0 <= t < T) sits at position
+ * p = L_b - T + t and attends to
+ *     [max(0, p + 1 - window), p + 1)   (window > 0), or [0, p + 1)   (window 0);
+ * a query at a negative position (L_b < T - t) attends to nothing and gets o = 0.
+ * Each cached K/V row is read once for all T * g query rows of its KV head.
+ *
+ *   q         bf16 [B, T, H, D]: token t's heads at q[b, t]
+ *   k, v      bf16 [B, S, KVH, D] (gqa_decode_mq) or page pools [P, 16, KVH, D] with
+ *             block_table [B, max_pages] (gqa_decode_mq_paged), as for gqa_decode
+ *             and gqa_decode_paged; only rows of attended positions are used
+ *   T         1 .. GQA_MAX_QUERIES_SLIDING (slidingDecodeGQA geometry) or
+ *             1 .. GQA_MAX_QUERIES_GLOBAL (decodeGQA geometry)
+ *   out       [B, T, H, D], bf16 or fp32 per out_dtype
+ *   workspace at least gqa_workspace_size_mq(B, T, H, KVH, D) bytes, prepared by
+ *             gqa_workspace_init; NULL = the library-owned per-device buffer
+ * Everything else -- seq_lens, window, errors, status bits -- is as for gqa_decode
+ * and gqa_decode_paged; a T outside its range returns GQA_ERR_INVALID_ARGUMENT.  A
+ * block-table entry outside [0, P) turns into NaN the outputs of exactly the
+ * queries whose attended range covers that page.  Rows outside a sequence's
+ * attended range are never used; a non-finite value inside it may reach every
+ * query of that sequence (the P.V product multiplies it by a zero weight).
+ * Runs on the tcgen05 tensor cores: scores and P.V as 128-position mma with
+ * TMEM accumulators.
+ */
+#define GQA_MAX_QUERIES_SLIDING 8
+#define GQA_MAX_QUERIES_GLOBAL 4
+
+size_t gqa_workspace_size_mq(int B, int T, int H, int KVH, int D);
+
+gqa_status_t gqa_decode_mq(const void *q, const void *k, const void *v, const int32_t *seq_lens,
+                           int B, int T, int S, int H, int KVH, int D, int window, void *out,
+                           gqa_out_dtype_t out_dtype, void *workspace, size_t workspace_bytes,
+                           gqa_stream_t stream);
+
+gqa_status_t gqa_decode_mq_paged(const void *q, const void *k_pages, const void *v_pages,
+                                 const int32_t *block_table, const int32_t *seq_lens, int B,
+                                 int T, int P, int max_pages, int page_size, int H, int KVH,
+                                 int D, int window, void *out, gqa_out_dtype_t out_dtype,
+                                 void *workspace, size_t workspace_bytes, gqa_stream_t stream);
+
+/*
  * Host-side check of the device-resident inputs, for tests and debugging: the
  * caller copies seq_lens (and the block table) to host memory and passes them
  * here.  The decode calls never read these arrays on the host (they stay on the
