@@ -98,14 +98,17 @@ def rank_seed(base_seed: int, rank: int) -> int:
 # workload construction and byte accounting
 # ---------------------------------------------------------------------------
 
-def attended_count(L: int, window: int) -> int:
-    lo = max(0, L - window) if window > 0 else 0
+def attended_count(L: int, window: int, T: int = 1) -> int:
+    """Positions a call reads for one sequence: the union of its T queries' ranges
+    (query t at position L - T + t; the earliest window starts at L - T + 1 - window)."""
+    span = window + T - 1 if window > 0 else 0
+    lo = max(0, L - span) if span > 0 else 0
     return max(0, L - lo)
 
 
-def kv_bytes(seq_lens, geo: dict) -> int:
+def kv_bytes(seq_lens, geo: dict, T: int = 1) -> int:
     """Algorithmic K+V bytes one call reads: KVH x D x 2 B x 2 tensors per attended position."""
-    n = sum(attended_count(int(L), geo["window"]) for L in np.asarray(seq_lens).tolist())
+    n = sum(attended_count(int(L), geo["window"], T) for L in np.asarray(seq_lens).tolist())
     return n * geo["KVH"] * geo["D"] * 2 * 2
 
 
@@ -113,21 +116,27 @@ class Call:
     """One library call of a step, with its inputs resident on the device."""
 
     def __init__(self, layer: str, geo: dict, case: dict, paged: bool, seq_lens: np.ndarray,
-                 device="cuda", ring: int = 0, keqv: bool = False, raw: dict | None = None):
+                 device="cuda", ring: int = 0, keqv: bool = False, raw: dict | None = None,
+                 queries: int = 0):
         self.layer, self.geo, self.case, self.paged = layer, geo, case, paged
+        self.queries = queries   # > 0: multi-query call with this many tokens per sequence
         self.ring = ring   # > 0: window-capped ring cache of `ring` rows
         self.keqv = keqv   # single K=V cache: only values are read
         self.raw = raw     # set: the decode-step producer writing into `case`, not a decode
         self.name = f"{layer}_ring{ring}" if ring else (f"{layer}_keqv" if keqv else layer)
+        if queries:
+            self.name = f"{layer}_mq{queries}"
         if raw is not None:
             self.name += "_producer"
         self.seq_lens = seq_lens
         # the producer reads no cache: it adds time, not KV bytes
-        self.bytes = 0 if raw is not None else kv_bytes(seq_lens, geo) // (2 if keqv else 1)
+        self.bytes = 0 if raw is not None else (
+            kv_bytes(seq_lens, geo, max(1, queries)) // (2 if keqv else 1))
         self.times_ms = []
         if str(device).startswith("cuda"):
             B = len(seq_lens)
-            self.out = torch.empty((B, geo["H"], geo["D"]), dtype=torch.bfloat16, device=device)
+            shape = (B, queries, geo["H"], geo["D"]) if queries else (B, geo["H"], geo["D"])
+            self.out = torch.empty(shape, dtype=torch.bfloat16, device=device)
             self.start = torch.cuda.Event(enable_timing=True)
             self.end = torch.cuda.Event(enable_timing=True)
 
@@ -139,6 +148,8 @@ class Call:
             r = self.raw
             gqa.gqa_prepare_decode(r["q_raw"], r["k_raw"], r["v_raw"], r["w_q"], r["w_k"], lens, q,
                                    c["k"], c["v"], ring=self.ring > 0)
+        elif self.queries:
+            gqa.gqa_decode_mq(q, c["k"], c["v"], lens, self.geo["window"], out=self.out)
         elif self.paged:
             gqa.gqa_decode_paged(q, c["k_pages"], c["v_pages"], c["block_table"], lens,
                                  self.geo["window"], out=self.out)
@@ -160,6 +171,11 @@ def build_calls(wl: inputs.Workload, seed: int, device="cuda"):
             case = inputs.paged_case(wl.B, geo["H"], geo["KVH"], geo["D"], lens, seed + 100 * i,
                                      device=device, table=table)
             calls.append(Call(layer, geo, case, True, lens, device))
+    elif wl.queries:
+        geo = inputs.geometry(wl.layers[0])
+        case = inputs.mq_case(wl.B, wl.queries, wl.S, geo["H"], geo["KVH"], geo["D"], lens, seed,
+                              device=device)
+        calls.append(Call(wl.layers[0], geo, case, False, lens, device, queries=wl.queries))
     elif wl.keqv:
         geo = inputs.geometry(wl.layers[0])
         case = inputs.keqv_case(wl.B, wl.S, geo["H"], geo["KVH"], geo["D"], lens, seed,
@@ -300,6 +316,12 @@ def host_slices(call: Call, b: int):
     L = int(call.seq_lens[b])
     lo = max(0, L - geo["window"]) if geo["window"] > 0 else 0
     qb = inputs.bf16_bits(c["q"][b:b + 1])
+    if call.queries:
+        # the union of the queries' ranges, shifted to start at row 0: the masks
+        # depend only on positions relative to L, so the result is unchanged
+        n = attended_count(L, geo["window"], call.queries)
+        return (qb, inputs.bf16_bits(c["k"][b:b + 1, L - n:L]),
+                inputs.bf16_bits(c["v"][b:b + 1, L - n:L]), n, 0)
     if call.ring:
         return qb, inputs.bf16_bits(c["k"][b:b + 1]), inputs.bf16_bits(c["v"][b:b + 1]), L, 0
     if call.keqv:
@@ -327,10 +349,10 @@ def oracle_sample(calls, budget_s: float, max_seqs: int | None = None):
     order = [(ci, b) for b in range(len(calls[0].seq_lens)) for ci in range(len(calls))]
     for ci, b in order:
         call = calls[ci]
-        n = attended_count(int(call.seq_lens[b]), call.geo["window"])
+        n = attended_count(int(call.seq_lens[b]), call.geo["window"], max(1, call.queries))
         if n == 0 or call.raw is not None:   # the producer has no attention to sample
             continue
-        flops = 4.0 * n * call.geo["H"] * call.geo["D"]
+        flops = 4.0 * n * call.geo["H"] * call.geo["D"] * max(1, call.queries)
         if call.keqv:
             flops *= 5.0   # plus a pow, cos and sin per rotated pair of every derived key
         if items and est + flops / rate > budget_s:
@@ -347,6 +369,8 @@ def oracle_for(call: Call, slices):
     """The fp64 oracle's output [H, D] for one sequence, from host_slices()."""
     import oracle
     qb, kb, vb, L, base = slices
+    if call.queries:
+        return oracle.gqa_decode_mq_f64(qb, kb, vb, [L], call.geo["window"])[0]
     if call.ring:
         return oracle.gqa_decode_ring_f64(qb, kb, vb, [L], call.geo["window"])[0]
     if call.keqv:
@@ -545,7 +569,8 @@ def run_ours(args, wl):
     dom_ms = statistics.mean(dom.times_ms)
     achieved = dom.bytes / (dom_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
-    roofline = {"bound": "hbm", "kernel": f"gqa_decode_kernel<{dom.name}>",
+    kernel = "gqa_mq_kernel" if dom.queries else "gqa_decode_kernel"
+    roofline = {"bound": "hbm", "kernel": f"{kernel}<{dom.name}>",
                 "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": recorded_traffic(wl.name, dom.layer),

@@ -19,23 +19,33 @@
 // elements (16 KB, 128-byte swizzled, exactly what TMA writes); the P.V mma of a
 // 128-wide head-dim block reads two adjacent stages.
 //
-// Warp roles (192 threads).  Warp 0, lane 0: the producer.  It walks the same
+// Warp roles (224 threads).  Warp 0, lane 0: the producer.  It walks the same
 // schedule as the single-query kernel (static units, then claimed dynamic chunks)
 // and streams the tiles in the order K(0), K(1), V(0), K(2), V(1), ...: the scores
-// of tile i+1 are computed while the softmax of tile i runs.  It also loads each
+// of tile i+1 are computed while the softmax of tile i runs.  K blocks go to one
+// stage ring and V blocks to another, each consumed in order by one warp (with two
+// consumers on one ring, a one-bit phase wait could see the other consumer's
+// earlier fill of the same stage).  It also loads each
 // piece's Q with TMA (box: 64 elements x g heads x T tokens) into one of two
-// buffers.  Warp 1: owns the TMEM allocation; lane 0 issues every mma and commit;
-// the whole warp zeroes the V rows of a tile that lie outside its sequence's
-// attended range before the P.V mma reads them (0 * NaN would poison the sum).
+// buffers.  Warp 1: owns the TMEM allocation; lane 0 issues the scores' mma.
+// Warp 6: lane 0 issues the P.V mma, and the whole warp zeroes the V rows of a tile
+// that lie outside its sequence's attended range before they are read (0 * NaN
+// would poison the sum).  A tcgen05.mma costs its issuing thread about 75 cycles
+// whatever N is up to 128, so two issuing warps keep the tensor core busier.
 // Warps 2..5: thread j owns TMEM lane j, i.e. position j of the tile's scores and
 // head-dim element j of each O^T block; they run the softmax and the epilogue.
+//
+// Pieces alternate between two O^T buffers in TMEM: a piece's output is written
+// after the next tile's P has been published, so the softmax warps never wait
+// for the last P.V of a piece before starting the next one.
 //
 // Softmax.  Each query row keeps a reference max m (log2 units) that all threads
 // share; P = exp2(s - m), and m moves only when a score of the tile exceeds it by
 // more than kMqTau (then the O^T columns and the normaliser shares are rescaled
 // by exp2(m_old - m_new)).  P <= 2^kMqTau keeps every fp32 sum finite.  P is
-// applied as a bf16 hi part and a bf16 lo part (two mma into the same
-// accumulator), about 16 significant bits.  The epilogue of a piece writes the
+// applied as a bf16 hi part and a bf16 lo part, rows [0, NMAX) and [NMAX, 2 NMAX) of
+// the mma's B operand, whose two O^T columns are summed at the end: about 16
+// significant bits.  The epilogue of a piece writes the
 // normalised output, or the partial (acc, m, l) that the combine kernel merges.
 //
 // Every wait is bounded; a wait that gives up raises the status word's timeout
@@ -53,8 +63,9 @@ constexpr float kMqTau = 24.0f;                    // rescale threshold, log2 un
 constexpr int kMqPLbo = 144;                       // P core matrices along positions (padded
                                                    // from 128 B so stores hit distinct banks)
 constexpr int kMqPSbo = (kMqTile / 8) * kMqPLbo;   // P 8-row groups: 2304 B
-constexpr int kMqThreads = 192;
+constexpr int kMqThreads = 224;         // producer, scores, 4 softmax warps, P.V
 constexpr int kMqSoftmaxThreads = 128;
+constexpr int kMqPvWarp = 6;
 
 constexpr int tmem_cols_for(int cols) {
     int c = 32;
@@ -62,26 +73,32 @@ constexpr int tmem_cols_for(int cols) {
     return c;
 }
 
-template <int kD, int kG, int kMaxT, int kStages>
+template <int kD, int kG, int kMaxT, int kKStages, int kVStages, int kObufs>
 struct MqCfg {
-    static constexpr int D = kD, G = kG, MAXT = kMaxT, STAGES = kStages;
+    static constexpr int D = kD, G = kG, MAXT = kMaxT, OBUFS = kObufs;
+    // two stage rings, each consumed in order by one warp: K (scores warp) and V (P.V warp)
+    static constexpr int KST = kKStages, VST = kVStages, STAGES = kKStages + kVStages;
     static constexpr int NSUB = D / 64;                 // stages per tile of one tensor
     static constexpr int NB = D / 128;                  // 128-wide head-dim blocks of O^T
     static constexpr int RMAX = G * MAXT;               // query rows of a segment
     static constexpr int NMAX = RMAX <= 16 ? 16 : 32;   // mma N bound
     static constexpr int QATOM = NMAX * 128;            // Q rows of one 64-element column block
     static constexpr int QBYTES = NSUB * QATOM;
-    static constexpr int PBYTES = (NMAX / 8) * kMqPSbo; // one P part (hi or lo)
+    static constexpr int PBYTES = (2 * NMAX / 8) * kMqPSbo;   // P^T: hi rows, then lo rows
     static constexpr int TMEM_S = 0;                    // S^T buffers: columns [0, 2 NMAX)
-    static constexpr int TMEM_O = 2 * NMAX;             // O^T blocks: NB x NMAX columns
-    static constexpr int TMEM_COLS = tmem_cols_for(TMEM_O + NB * NMAX);
-    static_assert(STAGES % 2 == 0, "a P.V block reads two adjacent stages");
+    static constexpr int TMEM_O = 2 * NMAX;             // O^T: OBUFS piece buffers of NB blocks
+    static constexpr int OBUF = NB * 2 * NMAX;          // of 2 NMAX columns (hi part, lo part)
+    static constexpr int TMEM_COLS = tmem_cols_for(TMEM_O + OBUFS * OBUF);
+    static_assert(TMEM_O + OBUFS * OBUF <= 512, "TMEM holds 512 columns");
+    static_assert(OBUFS == 1 || OBUFS == 2, "one or two O^T buffers");
+    static_assert(VST % 2 == 0, "a P.V block reads two adjacent stages");
     static_assert(NSUB % 2 == 0 && RMAX <= 32, "geometry");
     static_assert(RMAX == NMAX, "query rows fill the mma N bound");
 };
 
-using MqGlobal = MqCfg<512, 8, 4, 6>;     // decodeGQA, T <= 4
-using MqSliding = MqCfg<256, 2, 8, 10>;   // slidingDecodeGQA, T <= 8
+using MqGlobal = MqCfg<512, 8, 4, 4, 4, 1>;     // decodeGQA, T <= 4
+using MqGlobal2 = MqCfg<512, 8, 2, 4, 6, 2>;   // decodeGQA, T <= 2: smaller Q and P, more stages
+using MqSliding = MqCfg<256, 2, 8, 4, 6, 2>;   // slidingDecodeGQA, T <= 8
 
 struct MqTile {
     int b, kvh;
@@ -90,30 +107,37 @@ struct MqTile {
     int zlo, zhi;   // rows outside [zlo, zhi) lie outside the sequence's attended range
     int slot;       // workspace slot of the piece
     int flags;      // kDescFirst / kDescLast of the piece, kDescDone
-    int qb;         // Q buffer of the piece
+    int ob;         // O^T buffer of the piece (pieces alternate)
 };
 
 constexpr int kMqKindK = 0, kMqKindV = 1, kMqKindDone = 2;
 
 template <class Cfg>
 struct alignas(1024) MqSmem {
-    uint8_t stage[Cfg::STAGES][kMqStageBytes];   // K or V: [128 rows][128 B], swizzled
-    uint8_t q[2][Cfg::QBYTES];                    // [column block][NMAX rows][128 B], swizzled
-    uint8_t pm[2][2][Cfg::PBYTES];                // P^T [buffer][hi, lo], core-matrix layout
+    uint8_t stage[Cfg::STAGES][kMqStageBytes];   // K ring, then V ring: [128 rows][128 B], swizzled
+    uint8_t q[Cfg::QBYTES];                       // [column block][NMAX rows][128 B], swizzled
+    uint8_t pm[2][Cfg::PBYTES];                   // P^T [buffer], core-matrix layout
     alignas(8) uint64_t full[Cfg::STAGES];
     alignas(8) uint64_t empty[Cfg::STAGES];
-    alignas(8) uint64_t q_empty[2];   // last scores of the piece using Q buffer j done
+    alignas(8) uint64_t q_empty;      // the last scores of the piece holding Q are done
     alignas(8) uint64_t s_full[2];    // scores of tile i in S buffer i % 2 (+ its tile)
     alignas(8) uint64_t p_full[2];    // P of tile i written (softmax warps)
     alignas(8) uint64_t p_empty[2];   // P.V of tile i no longer reads P buffer i % 2
     alignas(8) uint64_t o_ready[2];   // P.V of tile i complete
-    alignas(8) uint64_t drain;        // the mma warp's final commit
-    int kind[Cfg::STAGES];
-    MqTile desc[Cfg::STAGES];         // tile of a K block (its first stage)
+    alignas(8) uint64_t s_empty[2];   // the softmax warps have read S buffer i % 2
+    alignas(8) uint64_t drain[2];     // the two mma warps' final commits
+    int kind[Cfg::KST];               // K ring: a K block or the end-of-work marker
+    MqTile desc[Cfg::KST];            // tile of a K block (its first stage)
     MqTile s_desc[2];                 // tile whose scores are in S buffer j
+    MqTile p_desc[2];                 // tile whose P is in P buffer j
+    int pv_stop;                      // index of the first tile that does not exist (set
+                                      // with the last p_full; larger until then)
     PlanSmem plan;
     float red[4][Cfg::NMAX];
     uint32_t red_bad[4];
+    float epi_m[Cfg::NMAX];   // the finished piece whose epilogue is pending: reference max,
+    float epi_l[Cfg::NMAX];   // normaliser and bad-page bits per query row
+    uint32_t epi_bad;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -128,6 +152,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     gqa_mq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
     constexpr int D = Cfg::D, G = Cfg::G, NSUB = Cfg::NSUB, NB = Cfg::NB, STAGES = Cfg::STAGES;
+    constexpr int KST = Cfg::KST, VST = Cfg::VST;
     constexpr int NMAX = Cfg::NMAX, RMAX = Cfg::RMAX, MAXT = Cfg::MAXT;
 
     extern __shared__ uint8_t smem_raw[];
@@ -148,14 +173,16 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             ptx::mbar_init(ptx::smem_addr(&sm.full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&sm.empty[s]), 1);
         }
+        ptx::mbar_init(ptx::smem_addr(&sm.q_empty), 1);
         for (int j = 0; j < 2; ++j) {
-            ptx::mbar_init(ptx::smem_addr(&sm.q_empty[j]), 1);
             ptx::mbar_init(ptx::smem_addr(&sm.s_full[j]), 2);   // mma commit + the tile's descriptor
             ptx::mbar_init(ptx::smem_addr(&sm.p_full[j]), 4);   // one arrival per softmax warp
             ptx::mbar_init(ptx::smem_addr(&sm.p_empty[j]), 1);
             ptx::mbar_init(ptx::smem_addr(&sm.o_ready[j]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sm.s_empty[j]), 4);   // one arrival per softmax warp
+            ptx::mbar_init(ptx::smem_addr(&sm.drain[j]), 1);
         }
-        ptx::mbar_init(ptx::smem_addr(&sm.drain), 1);
+        sm.pv_stop = 0x7fffffff;
         ptx::fence_mbar_init();
         sm.abort_flag = 0;
     }
@@ -199,6 +226,16 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     const uint32_t stage0 = ptx::smem_addr(&sm.stage[0][0]);
+    // Stage q of the K ring is stage[q % KST]; stage q of the V ring is stage[KST + q % VST].
+    auto kst = [&](uint32_t q) { return static_cast<int>(q % KST); };
+    auto vst = [&](uint32_t q) { return KST + static_cast<int>(q % VST); };
+    // bounded wait (whole warp) for K-ring (v = false) or V-ring stage q to be full
+    auto wait_full = [&](bool v, uint32_t q) -> bool {
+        const int s = v ? vst(q) : kst(q);
+        const uint32_t ph = (q / (v ? VST : KST)) & 1u;
+        return __all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&sm.full[s]), ph, &sm.abort_flag,
+                                                     p.ws_flags));
+    };
 
     if (warp == 0) {
         // ============================ producer ============================
@@ -206,9 +243,48 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             const uint64_t policy = ptx::policy_evict_first();
             const uint32_t q_bytes = static_cast<uint32_t>(NSUB * R * 128);
             constexpr uint32_t kPageBytes = kPageRows * 128;
-            uint32_t seq = 0;        // stages issued
-            uint32_t n_piece = 0;    // pieces started (Q buffer n_piece & 1)
+            uint32_t kseq = 0, vseq = 0;   // stages issued on the K and V rings
+            uint32_t n_piece = 0;    // pieces started (O^T buffer n_piece & 1)
             bool ok = true;
+            // Q of the newest piece, when its load still waits for the previous piece's
+            // last scores: the load completes on the full barrier of the piece's first K
+            // stage, which already expects its bytes.  Every wait of the producer keeps
+            // servicing it, so the K stages of the piece stream meanwhile.
+            bool q_pend = false;
+            uint32_t q_issued = 0;   // pieces whose Q load was issued
+            int q_b = 0, q_kvh = 0;
+            uint32_t q_bar = 0;
+            const uint32_t q_empty_bar = ptx::smem_addr(&sm.q_empty);
+            auto service_q = [&]() {
+                // piece n (= q_issued) may overwrite Q once the last scores of piece n - 1 are done
+                if (q_pend && ptx::mbar_try_wait(q_empty_bar, (q_issued & 1u) ^ 1u)) {
+                    const uint32_t qdst = ptx::smem_addr(&sm.q[0]);
+                    for (int c = 0; c < NSUB; ++c)
+                        ptx::tma_load_4d(qdst + c * Cfg::QATOM, &tm_q, q_bar, 64 * c, q_kvh * G, 0, q_b,
+                                         policy);
+                    q_pend = false;
+                    ++q_issued;
+                }
+            };
+            // Bounded wait on a stage barrier (or, with bar == 0, for the pending Q to be
+            // issued) that services the pending Q while it waits.
+            auto wait_servicing = [&](uint32_t bar, uint32_t parity) -> bool {
+                auto done = [&]() { return bar ? ptx::mbar_try_wait(bar, parity) : !q_pend; };
+                service_q();
+                if (done()) return true;
+                const uint64_t t0 = ptx::globaltimer_ns();
+                for (uint32_t round = 0;; ++round) {
+                    service_q();
+                    for (int i = 0; i < 8; ++i)
+                        if (done()) return true;
+                    if (sm.abort_flag) return false;
+                    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs || round > kWaitMaxRounds) {
+                        sm.abort_flag = 1;
+                        atomicOr(p.ws_flags, kFlagWaitTimeout);
+                        return false;
+                    }
+                }
+            };
             const bool dynamic = pl.n_dyn > 0;
             int claimed = -1;
             MqTile prev;
@@ -220,12 +296,13 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                     kPaged ? p.block_table + static_cast<size_t>(d.b) * p.max_pages : nullptr;
                 // paged: load the pages that hold attended positions of the sequence
                 const int npage = kPaged ? (d.zhi + kPageRows - 1) / kPageRows : 0;
+                const bool on_v = kind == kMqKindV;
                 for (int sub = 0; sub < NSUB; ++sub) {
-                    const int s = seq % STAGES;
-                    const uint32_t ph = (seq / STAGES) & 1u;
-                    if (!wait_bounded(ptx::smem_addr(&sm.empty[s]), ph ^ 1u, &sm.abort_flag, p.ws_flags))
-                        return false;
-                    sm.kind[s] = kind;
+                    uint32_t& seq = on_v ? vseq : kseq;
+                    const int s = on_v ? vst(seq) : kst(seq);
+                    const uint32_t ph = (seq / (on_v ? VST : KST)) & 1u;
+                    if (!wait_servicing(ptx::smem_addr(&sm.empty[s]), ph ^ 1u)) return false;
+                    if (!on_v) sm.kind[s] = kind;
                     const uint32_t full_bar = ptx::smem_addr(&sm.full[s]);
                     if (kind == kMqKindDone) {
                         ptx::mbar_arrive(full_bar);
@@ -239,10 +316,11 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                         (with_q ? q_bytes : 0u);
                     ptx::mbar_arrive_expect_tx(full_bar, bytes);
                     if (with_q) {
-                        const uint32_t qdst = ptx::smem_addr(&sm.q[d.qb][0]);
-                        for (int c = 0; c < NSUB; ++c)
-                            ptx::tma_load_4d(qdst + c * Cfg::QATOM, &tm_q, full_bar, 64 * c, d.kvh * G,
-                                             0, d.b, policy);
+                        // (emit_piece made sure no other Q is pending)
+                        q_pend = true;
+                        q_b = d.b;
+                        q_kvh = d.kvh;
+                        q_bar = full_bar;
                     }
                     const CUtensorMap* map = kind == kMqKindK ? &tm_k : &tm_v;
                     const uint32_t dst = stage0 + s * kMqStageBytes;
@@ -258,6 +336,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                         ptx::tma_load_4d(dst, map, full_bar, 0, d.t, chunk, d.b, policy);
                     }
                     ++seq;
+                    service_q();
                 }
                 return true;
             };
@@ -270,10 +349,9 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             };
             // The tiles of positions [p0, p1) of segment (b, kvh).
             auto emit_piece = [&](int b, int kvh, int p0, int p1, int slot, bool unit_end) -> bool {
-                const uint32_t qb = n_piece & 1u;
-                if (!wait_bounded(ptx::smem_addr(&sm.q_empty[qb]), ((n_piece >> 1) & 1u) ^ 1u,
-                                  &sm.abort_flag, p.ws_flags))
-                    return false;
+                // at most one Q load pending: the previous piece's goes out first
+                if (!wait_servicing(0u, 0u)) return false;
+                const uint32_t ob = n_piece & 1u;
                 ++n_piece;
                 const int lo = pl.lo[b], L = lo + pl.n[b];
                 const int t_first = kPaged ? (p0 & ~(kPageRows - 1)) : p0;
@@ -291,7 +369,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                     d.zhi = L < t + kMqTile ? L - t : kMqTile;
                     d.slot = slot;
                     d.flags = (t == t_first ? kDescFirst : 0) | (last ? kDescLast : 0);
-                    d.qb = static_cast<int>(qb);
+                    d.ob = Cfg::OBUFS == 2 ? static_cast<int>(ob) : 0;
                     if (!emit_tile(d)) return false;
                 }
                 return true;
@@ -336,107 +414,111 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             if (ok) {
                 MqTile none;
                 none.b = none.kvh = none.t = none.vlo = none.vhi = none.zlo = none.zhi = 0;
-                none.slot = none.qb = 0;
+                none.slot = none.ob = 0;
                 none.flags = kDescDone;
                 ok = emit_block(none, kMqKindDone);
                 if (ok && have_prev) ok = emit_block(prev, kMqKindV);
             }
             if (!ok) {
                 // let every copy already issued land before the CTA exits
-                const uint32_t first = seq > static_cast<uint32_t>(STAGES) ? seq - STAGES : 0u;
-                for (uint32_t tt = first; tt < seq; ++tt)
-                    wait_drain(ptx::smem_addr(&sm.full[tt % STAGES]), (tt / STAGES) & 1u);
+                for (uint32_t tt = kseq > static_cast<uint32_t>(KST) ? kseq - KST : 0u; tt < kseq; ++tt)
+                    wait_drain(ptx::smem_addr(&sm.full[kst(tt)]), (tt / KST) & 1u);
+                for (uint32_t tt = vseq > static_cast<uint32_t>(VST) ? vseq - VST : 0u; tt < vseq; ++tt)
+                    wait_drain(ptx::smem_addr(&sm.full[vst(tt)]), (tt / VST) & 1u);
             }
         }
     } else if (warp == 1) {
-        // ====================== mma issue (lane 0) + V fix-up (warp) ======================
+        // =================== scores: S^T[pos, r] = K Q^T (lane 0 issues) ===================
         const uint32_t idesc_s = ptx::idesc_bf16_f32(kMqTile, N, 0, 0);
-        const uint32_t idesc_o = ptx::idesc_bf16_f32(kMqTile, N, 1, 0);
-        uint32_t seq = 0;
-        uint32_t i_s = 0, i_pv = 0;   // tiles whose scores / P.V were issued
-        MqTile pend[2];               // tiles between their scores and their P.V
-        bool done = false;
-        auto wait_full = [&](uint32_t sq) -> bool {
-            return __all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&sm.full[sq % STAGES]),
-                                                         (sq / STAGES) & 1u, &sm.abort_flag, p.ws_flags));
-        };
-        while (!(done && i_pv == i_s)) {
-            if (!wait_full(seq)) break;
+        for (uint32_t i = 0;; ++i) {
+            // tile i's K block (or the end-of-work marker) on the K ring
+            uint32_t seq = i * NSUB;
+            if (!wait_full(false, seq)) break;
             ptx::tc_fence_after();
-            const int kind = sm.kind[seq % STAGES];
-            if (kind == kMqKindDone) {
+            const bool done = sm.kind[kst(seq)] == kMqKindDone;
+            const MqTile d = sm.desc[kst(seq)];
+            // S buffer i % 2 is free once the softmax warps have read tile i - 2
+            if (!__all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&sm.s_empty[i & 1u]),
+                                                      ((i >> 1) & 1u) ^ 1u, &sm.abort_flag, p.ws_flags)))
+                break;
+            ptx::tc_fence_after();
+            if (done) {
+                // release the end-of-work stages; the softmax warps learn there is no tile i
                 bool ok = true;
                 for (int sub = 0; sub < NSUB && ok; ++sub) {
-                    if (sub > 0) ok = wait_full(seq);
-                    if (ok && lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.empty[seq % STAGES]));
+                    if (sub > 0) ok = wait_full(false, seq);
+                    if (ok && lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.empty[kst(seq)]));
                     ++seq;
                 }
-                if (!ok) break;
-                // no tile i_s: the softmax warps leave
-                if (lane == 0) {
-                    sm.s_desc[i_s & 1].flags = kDescDone;
-                    ptx::mbar_arrive(ptx::smem_addr(&sm.s_full[i_s & 1]));
-                    ptx::mbar_arrive(ptx::smem_addr(&sm.s_full[i_s & 1]));
-                }
-                done = true;
-                continue;
-            }
-            if (kind == kMqKindK) {
-                // ---- scores of tile i: S^T[pos, r] over the NSUB column blocks ----
-                const MqTile d = sm.desc[seq % STAGES];
-                const uint32_t i = i_s++;
-                const uint32_t s_col = tmem + Cfg::TMEM_S + (i & 1u) * NMAX;
-                const uint32_t qbase = ptx::smem_addr(&sm.q[d.qb][0]);
-                bool ok = true;
-                for (int sub = 0; sub < NSUB; ++sub) {
-                    if (sub > 0) {
-                        ok = wait_full(seq);
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                    }
-                    const int s = seq % STAGES;
-                    if (lane == 0) {
-                        const uint32_t a0 = stage0 + s * kMqStageBytes;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = ptx::smem_desc(a0 + kk * 32, 16, 1024, ptx::kSwizzle128B);
-                            const uint64_t bq = ptx::smem_desc(qbase + sub * Cfg::QATOM + kk * 32, 16,
-                                                               1024, ptx::kSwizzle128B);
-                            ptx::umma_ss(s_col, a, bq, idesc_s, (sub | kk) != 0 ? 1u : 0u);
-                        }
-                        ptx::umma_commit(ptx::smem_addr(&sm.empty[s]));
-                    }
-                    __syncwarp();
-                    ++seq;
-                }
-                if (!ok) break;
-                if (lane == 0) {
-                    if (d.flags & kDescLast) ptx::umma_commit(ptx::smem_addr(&sm.q_empty[d.qb]));
-                    ptx::umma_commit(ptx::smem_addr(&sm.s_full[i & 1u]));
-                    sm.s_desc[i & 1u] = d;
+                if (ok && lane == 0) {
+                    sm.s_desc[i & 1u].flags = kDescDone;
+                    ptx::mbar_arrive(ptx::smem_addr(&sm.s_full[i & 1u]));
                     ptx::mbar_arrive(ptx::smem_addr(&sm.s_full[i & 1u]));
                 }
-                pend[i & 1u] = d;
-                __syncwarp();
-                continue;
+                break;
             }
-            // ---- P.V of tile i: O^T[d, r] += V^T[d, pos] P^T[pos, r] ----
-            const uint32_t i = i_pv++;
-            const MqTile d = pend[i & 1u];
+            const uint32_t s_col = tmem + Cfg::TMEM_S + (i & 1u) * NMAX;
+            const uint32_t qbase = ptx::smem_addr(&sm.q[0]);
+            bool ok = true;
+            for (int sub = 0; sub < NSUB; ++sub) {
+                if (sub > 0) {
+                    ok = wait_full(false, seq);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                }
+                const int s = kst(seq);
+                if (lane == 0) {
+                    const uint32_t a0 = stage0 + s * kMqStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = ptx::smem_desc(a0 + kk * 32, 16, 1024, ptx::kSwizzle128B);
+                        const uint64_t bq = ptx::smem_desc(qbase + sub * Cfg::QATOM + kk * 32, 16, 1024,
+                                                           ptx::kSwizzle128B);
+                        ptx::umma_ss(s_col, a, bq, idesc_s, (sub | kk) != 0 ? 1u : 0u);
+                    }
+                    ptx::umma_commit(ptx::smem_addr(&sm.empty[s]));
+                }
+                __syncwarp();
+                ++seq;
+            }
+            if (!ok) break;
+            if (lane == 0) {
+                if (d.flags & kDescLast) ptx::umma_commit(ptx::smem_addr(&sm.q_empty));
+                ptx::umma_commit(ptx::smem_addr(&sm.s_full[i & 1u]));
+                sm.s_desc[i & 1u] = d;
+                ptx::mbar_arrive(ptx::smem_addr(&sm.s_full[i & 1u]));
+            }
+            __syncwarp();
+        }
+        // every mma issued has completed before TMEM is released
+        if (lane == 0) {
+            ptx::umma_commit(ptx::smem_addr(&sm.drain[0]));
+            wait_drain(ptx::smem_addr(&sm.drain[0]), 0u);
+        }
+        __syncwarp();
+    } else if (warp == kMqPvWarp) {
+        // ========= P.V: O^T[d, r] += V^T[d, pos] P^T[pos, r] (lane 0 issues) + V fix-up =========
+        // P^T holds the bf16 hi parts in rows [0, NMAX) and the lo parts in rows
+        // [NMAX, 2 NMAX): one mma applies P to ~16 significant bits.
+        const uint32_t idesc_o = ptx::idesc_bf16_f32(kMqTile, 2 * NMAX, 1, 0);
+        for (uint32_t i = 0;; ++i) {
             if (!__all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&sm.p_full[i & 1u]), (i >> 1) & 1u,
                                                       &sm.abort_flag, p.ws_flags)))
                 break;
             ptx::tc_fence_after();
+            // no tile i (the flag names the tile: it may be set while tile i - 1's P
+            // is read)
+            if (static_cast<int>(i) >= sm.pv_stop) break;
+            const MqTile d = sm.p_desc[i & 1u];
             const bool fix = d.zlo > 0 || d.zhi < kMqTile;
-            const uint32_t ph_base = ptx::smem_addr(&sm.pm[i & 1u][0][0]);
-            const uint32_t pl_base = ptx::smem_addr(&sm.pm[i & 1u][1][0]);
+            const uint32_t pbase = ptx::smem_addr(&sm.pm[i & 1u][0]);
+            uint32_t seq = i * NSUB;   // tile i's V block on the V ring
             bool ok = true;
             for (int mb = 0; mb < NB; ++mb) {
-                // the two stages of head-dim block mb (adjacent: seq is even here)
-                if (mb > 0) ok = wait_full(seq);
-                ok = ok && wait_full(seq + 1);
+                // the two stages of head-dim block mb (adjacent: seq is even, VST even)
+                ok = wait_full(true, seq) && wait_full(true, seq + 1);
                 if (!ok) break;
-                const int s = seq % STAGES;
+                const int s = vst(seq);
                 if (fix) {
                     // rows outside the attended range of the sequence may hold anything
                     for (int h = 0; h < 2; ++h) {
@@ -454,18 +536,14 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 ptx::tc_fence_after();
                 if (lane == 0) {
                     const uint32_t a0 = stage0 + s * kMqStageBytes;
-                    const uint32_t o_col = tmem + Cfg::TMEM_O + mb * NMAX;
+                    const uint32_t o_col = tmem + Cfg::TMEM_O + d.ob * Cfg::OBUF + mb * 2 * NMAX;
 #pragma unroll
                     for (int kk = 0; kk < kMqTile / 16; ++kk) {
                         const uint64_t a = ptx::smem_desc(a0 + kk * 2048, kMqStageBytes, 1024,
                                                           ptx::kSwizzle128B);
-                        const uint64_t bh = ptx::smem_desc(ph_base + kk * 2 * kMqPLbo, kMqPLbo, kMqPSbo,
+                        const uint64_t bp = ptx::smem_desc(pbase + kk * 2 * kMqPLbo, kMqPLbo, kMqPSbo,
                                                            ptx::kSwizzleNone);
-                        const uint64_t bl = ptx::smem_desc(pl_base + kk * 2 * kMqPLbo, kMqPLbo, kMqPSbo,
-                                                           ptx::kSwizzleNone);
-                        ptx::umma_ss(o_col, a, bh, idesc_o,
-                                     ((d.flags & kDescFirst) && kk == 0) ? 0u : 1u);
-                        ptx::umma_ss(o_col, a, bl, idesc_o, 1u);
+                        ptx::umma_ss(o_col, a, bp, idesc_o, ((d.flags & kDescFirst) && kk == 0) ? 0u : 1u);
                     }
                     ptx::umma_commit(ptx::smem_addr(&sm.empty[s]));
                     ptx::umma_commit(ptx::smem_addr(&sm.empty[s + 1]));
@@ -480,10 +558,9 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             }
             __syncwarp();
         }
-        // every mma issued has completed before TMEM is released
         if (lane == 0) {
-            ptx::umma_commit(ptx::smem_addr(&sm.drain));
-            wait_drain(ptx::smem_addr(&sm.drain), 0u);
+            ptx::umma_commit(ptx::smem_addr(&sm.drain[1]));
+            wait_drain(ptx::smem_addr(&sm.drain[1]), 0u);
         }
         __syncwarp();
     } else {
@@ -498,13 +575,84 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             l_part[r] = 0.0f;
         }
         uint32_t bad_q = 0;   // bit t: query t attended a bad page in this piece
+        // P rows past the query rows in use stay zero (the P.V mma reads 2 NMAX rows)
+        for (int i = j; i < 2 * Cfg::PBYTES / 16; i += kMqSoftmaxThreads)
+            ptx::sts128(ptx::smem_addr(&sm.pm[0][0]) + i * 16, 0u, 0u, 0u, 0u);
+        ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+        // A finished piece whose output is still to be written: its last tile and
+        // that tile's index; its reference max, normaliser and bad bits are in smem.
+        bool epi_pending = false;
+        MqTile epi;
+        uint32_t epi_i = 0;
+        epi.b = epi.kvh = epi.slot = epi.ob = 0;
+        // Writes the pending piece's output: waits for its last P.V, then reads its
+        // O^T buffer and stores the normalised rows (a piece that is its whole
+        // segment) or the partial (acc, m, l).  False when the CTA is aborting.
+        auto finish_piece = [&]() -> bool {
+            const bool okw = wait_bounded(ptx::smem_addr(&sm.o_ready[epi_i & 1u]), (epi_i >> 1) & 1u,
+                                          &sm.abort_flag, p.ws_flags);
+            if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !okw)) return false;
+            ptx::tc_fence_after();
+            const uint32_t bad_all = sm.epi_bad;
+            const SegmentParts sp(pl, epi.b, epi.kvh, p.dyn_slot_base);
+            const bool direct = sp.count() == 1;
+#pragma unroll
+            for (int mb = 0; mb < NB; ++mb) {
+#pragma unroll
+                for (int c0 = 0; c0 < NMAX; c0 += 16) {
+                    if (c0 >= N) break;
+                    // row r's sum is its hi column r plus its lo column NMAX + r
+                    uint32_t oh[16], ol[16];
+                    const uint32_t ob = lane_addr + Cfg::TMEM_O + epi.ob * Cfg::OBUF + mb * 2 * NMAX + c0;
+                    ptx::tmem_ld16(ob, oh);
+                    ptx::tmem_ld16(ob + NMAX, ol);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int r = c0 + c;
+                        if (r >= R) break;
+                        const int t = r / G, g = r - (r / G) * G;
+                        const bool bad = (bad_all >> t) & 1u;
+                        const int dd = mb * 128 + j;
+                        const float acc = __uint_as_float(oh[c]) + __uint_as_float(ol[c]);
+                        if (direct) {
+                            const size_t row = (static_cast<size_t>(epi.b) * T + t) * H + epi.kvh * G + g;
+                            const float lr = sm.epi_l[r];
+                            // no key at all: the empty sum (a NaN normaliser stays NaN)
+                            store_out(p, row * D + dd, bad ? nan : (lr == 0.0f ? 0.0f : acc / lr));
+                        } else {
+                            p.ws_acc[(static_cast<size_t>(epi.slot) * R + r) * D + dd] = bad ? nan : acc;
+                        }
+                    }
+                }
+            }
+            if (!direct && j < R) {
+                const bool bad = (bad_all >> (j / G)) & 1u;
+                float* ml = p.ws_ml + (static_cast<size_t>(epi.slot) * R + j) * 2;
+                ml[0] = bad ? 0.0f : sm.epi_m[j];
+                ml[1] = bad ? nan : sm.epi_l[j];
+            }
+            ptx::tc_fence_before();
+            return true;
+        };
         for (uint32_t i = 0;; ++i) {
             bool ok = wait_bounded(ptx::smem_addr(&sm.s_full[i & 1u]), (i >> 1) & 1u, &sm.abort_flag,
                                    p.ws_flags);
             if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
             ptx::tc_fence_after();
             const MqTile d = sm.s_desc[i & 1u];
-            if (d.flags & kDescDone) break;
+            if (d.flags & kDescDone) {
+                // no tile i: the P.V warp stops too (a pending piece is finished below).
+                // Like a tile's P, the signal waits until the P.V warp is done with tile
+                // i - 2, so p_full[i % 2] never runs two phases ahead of it.
+                ok = wait_bounded(ptx::smem_addr(&sm.p_empty[i & 1u]), ((i >> 1) & 1u) ^ 1u,
+                                  &sm.abort_flag, p.ws_flags);
+                if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
+                if (j == 0) sm.pv_stop = static_cast<int>(i);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.p_full[i & 1u]));
+                break;
+            }
             if (d.flags & kDescFirst) {
 #pragma unroll
                 for (int r = 0; r < RMAX; ++r) {
@@ -526,6 +674,10 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             ptx::tmem_ld16(lane_addr + Cfg::TMEM_S + (i & 1u) * NMAX, sr0);
             if (N > 16) ptx::tmem_ld16(lane_addr + Cfg::TMEM_S + (i & 1u) * NMAX + 16, sr1);
             ptx::tmem_wait_ld();
+            // S buffer i % 2 may take the scores of tile i + 2
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.s_empty[i & 1u]));
             float s[RMAX];
             bool need = false;
 #pragma unroll
@@ -546,6 +698,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 // new reference max of every row: the tile's max where it is larger
 #pragma unroll
                 for (int r = 0; r < RMAX; ++r) {
+                    if (r >= R) break;
                     float mx = s[r];
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -554,7 +707,10 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 ptx::named_barrier_sync(3, kMqSoftmaxThreads);
                 float alpha[RMAX];
 #pragma unroll
+                for (int r = 0; r < RMAX; ++r) alpha[r] = 1.0f;   // rows past R are unused
+#pragma unroll
                 for (int r = 0; r < RMAX; ++r) {
+                    if (r >= R) break;
                     const float mt = fmaxf(fmaxf(sm.red[0][r], sm.red[1][r]), fmaxf(sm.red[2][r], sm.red[3][r]));
                     const float mn = fmaxf(m_ref[r], mt);
                     alpha[r] = (m_ref[r] == -INFINITY || mn == -INFINITY) ? 0.0f : exp2f(m_ref[r] - mn);
@@ -574,14 +730,19 @@ __global__ void __launch_bounds__(kMqThreads, 1)
 #pragma unroll
                         for (int c0 = 0; c0 < NMAX; c0 += 16) {
                             if (c0 >= N) break;
-                            uint32_t o[16];
-                            const uint32_t ta = lane_addr + Cfg::TMEM_O + mb * NMAX + c0;
-                            ptx::tmem_ld16(ta, o);
-                            ptx::tmem_wait_ld();
+                            // the hi column and the lo column of each row
 #pragma unroll
-                            for (int c = 0; c < 16; ++c)
-                                o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[c0 + c]);
-                            ptx::tmem_st16(ta, o);
+                            for (int part = 0; part < 2; ++part) {
+                                uint32_t o[16];
+                                const uint32_t ta = lane_addr + Cfg::TMEM_O + d.ob * Cfg::OBUF +
+                                                    mb * 2 * NMAX + part * NMAX + c0;
+                                ptx::tmem_ld16(ta, o);
+                                ptx::tmem_wait_ld();
+#pragma unroll
+                                for (int c = 0; c < 16; ++c)
+                                    o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[c0 + c]);
+                                ptx::tmem_st16(ta, o);
+                            }
                         }
                     }
                     ptx::tmem_wait_st();
@@ -594,8 +755,8 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                               p.ws_flags);
             if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
             {
-                const uint32_t ph = ptx::smem_addr(&sm.pm[i & 1u][0][0]);
-                const uint32_t plo = ptx::smem_addr(&sm.pm[i & 1u][1][0]);
+                // hi part in row r, lo part in row NMAX + r
+                const uint32_t pb = ptx::smem_addr(&sm.pm[i & 1u][0]);
 #pragma unroll
                 for (int r = 0; r < NMAX; ++r) {
                     if (r >= N) break;
@@ -604,25 +765,38 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                     l_part[r] += pv;
                     const __nv_bfloat16 hb = __float2bfloat16_rn(pv);
                     const __nv_bfloat16 lb = __float2bfloat16_rn(pv - __bfloat162float(hb));
-                    const uint32_t off = mq_p_off(r, j);
-                    ptx::sts16(ph + off, *reinterpret_cast<const uint16_t*>(&hb));
-                    ptx::sts16(plo + off, *reinterpret_cast<const uint16_t*>(&lb));
+                    ptx::sts16(pb + mq_p_off(r, j), *reinterpret_cast<const uint16_t*>(&hb));
+                    ptx::sts16(pb + mq_p_off(NMAX + r, j), *reinterpret_cast<const uint16_t*>(&lb));
                 }
             }
+            // one O^T buffer: the pending piece's output is read before this new piece's
+            // first P.V overwrites it
+            if (Cfg::OBUFS == 1 && (d.flags & kDescFirst) && epi_pending) {
+                if (!finish_piece()) break;
+                epi_pending = false;
+            }
+            if (j == 0) sm.p_desc[i & 1u] = d;
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.p_full[i & 1u]));
-            if (!(d.flags & kDescLast)) continue;
+            if (!(d.flags & kDescLast)) {
+                if (epi_pending) {
+                    if (!finish_piece()) break;
+                    epi_pending = false;
+                }
+                continue;
+            }
 
-            // ---------------- epilogue of the piece ----------------
-            ok = wait_bounded(ptx::smem_addr(&sm.o_ready[i & 1u]), (i >> 1) & 1u, &sm.abort_flag,
-                              p.ws_flags);
-            if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
-            ptx::tc_fence_after();
-            float l[RMAX];
+            // ---- the piece is complete: its normaliser now, its output after the next
+            // tile's P (so the softmax of that tile does not wait for this P.V) ----
+            if (epi_pending) {
+                if (!finish_piece()) break;
+                epi_pending = false;
+            }
 #pragma unroll
             for (int r = 0; r < RMAX; ++r) {
+                if (r >= R) break;
                 float v = l_part[r];
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -631,54 +805,26 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             const uint32_t bq = __reduce_or_sync(0xffffffffu, bad_q);
             if (lane == 0) sm.red_bad[warp & 3] = bq;
             ptx::named_barrier_sync(3, kMqSoftmaxThreads);
-#pragma unroll
-            for (int r = 0; r < RMAX; ++r) l[r] = (sm.red[0][r] + sm.red[1][r]) + (sm.red[2][r] + sm.red[3][r]);
-            const uint32_t bad_all = sm.red_bad[0] | sm.red_bad[1] | sm.red_bad[2] | sm.red_bad[3];
-            ptx::named_barrier_sync(3, kMqSoftmaxThreads);
-            if (bad_all && j == 0) atomicOr(p.ws_flags, kFlagBadPage);
-            const SegmentParts sp(pl, d.b, d.kvh, p.dyn_slot_base);
-            const bool direct = sp.count() == 1;
-#pragma unroll
-            for (int mb = 0; mb < NB; ++mb) {
-#pragma unroll
-                for (int c0 = 0; c0 < NMAX; c0 += 16) {
-                    if (c0 >= N) break;
-                    uint32_t o[16];
-                    ptx::tmem_ld16(lane_addr + Cfg::TMEM_O + mb * NMAX + c0, o);
-                    ptx::tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const int r = c0 + c;
-                        if (r >= R) break;
-                        const int t = r / G, g = r - (r / G) * G;
-                        const bool bad = (bad_all >> t) & 1u;
-                        const int dd = mb * 128 + j;
-                        const float acc = __uint_as_float(o[c]);
-                        if (direct) {
-                            const size_t row = (static_cast<size_t>(d.b) * T + t) * H + d.kvh * G + g;
-                            // no key at all: the empty sum (a NaN normaliser stays NaN)
-                            store_out(p, row * D + dd, bad ? nan : (l[r] == 0.0f ? 0.0f : acc / l[r]));
-                        } else {
-                            p.ws_acc[(static_cast<size_t>(d.slot) * R + r) * D + dd] = bad ? nan : acc;
-                        }
-                    }
-                }
-            }
-            if (!direct && j < R) {
-                const bool bad = (bad_all >> (j / G)) & 1u;
-                float mj = 0.0f, lj = 0.0f;
+            if (j < NMAX) {
+                float mj = 0.0f;
 #pragma unroll
                 for (int r = 0; r < RMAX; ++r)
-                    if (r == j) {
-                        mj = m_ref[r];
-                        lj = l[r];
-                    }
-                float* ml = p.ws_ml + (static_cast<size_t>(d.slot) * R + j) * 2;
-                ml[0] = bad ? 0.0f : mj;
-                ml[1] = bad ? nan : lj;
+                    if (r == j) mj = m_ref[r];
+                sm.epi_m[j] = mj;
+                sm.epi_l[j] = (sm.red[0][j] + sm.red[1][j]) + (sm.red[2][j] + sm.red[3][j]);
             }
-            ptx::tc_fence_before();
+            if (j == 0) {
+                const uint32_t bad_all = sm.red_bad[0] | sm.red_bad[1] | sm.red_bad[2] | sm.red_bad[3];
+                sm.epi_bad = bad_all;
+                if (bad_all) atomicOr(p.ws_flags, kFlagBadPage);
+            }
+            ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+            epi = d;
+            epi_i = i;
+            epi_pending = true;
         }
+        // (uniform: every exit from the loop above is a collective decision)
+        if (epi_pending) finish_piece();
     }
 
     ptx::tc_fence_before();

@@ -99,6 +99,8 @@ cudaError_t launch_mq_impl(const LaunchArgs& a) {
 cudaError_t launch_mq(const LaunchArgs& a, bool sliding, bool paged) {
     if (sliding)
         return paged ? launch_mq_impl<MqSliding, true>(a) : launch_mq_impl<MqSliding, false>(a);
+    if (a.p.T <= MqGlobal2::MAXT)
+        return paged ? launch_mq_impl<MqGlobal2, true>(a) : launch_mq_impl<MqGlobal2, false>(a);
     return paged ? launch_mq_impl<MqGlobal, true>(a) : launch_mq_impl<MqGlobal, false>(a);
 }
 

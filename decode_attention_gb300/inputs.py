@@ -114,6 +114,7 @@ class Workload:
     rings: tuple = ()        # windows of ring-cache sliding calls (ring length = window)
     keqv: bool = False       # global layer over a single K=V cache (values only)
     step: bool = False       # each ring call is preceded by the decode-step producer
+    queries: int = 0         # > 0: multi-query calls with this many new tokens per sequence
 
     def seq_lens(self) -> np.ndarray:
         return self.lengths(np.random.default_rng(self.seed))
@@ -158,6 +159,29 @@ WORKLOADS = {
         Workload("global_keqv_b8_s8192", "decodeGQA over a single K=V cache, B=8, seq_lens "
                  "uniform on [1, 8192]", B=8, S=8192, seed=8, lengths=lengths_uniform(1, 8192, 8),
                  layers=("global",), keqv=True),
+        # Multi-query steps ("Gemma 4 31B-it Text Architecture", "Inference behavior":
+        # new query positions attend to the cache with the same masks): T new tokens
+        # per sequence, e.g. a speculative-decoding verify step of T - 1 draft tokens
+        # plus one.  The same length draws as the single-query shapes.
+        Workload("global_mq4_b16_s131072", "decodeGQA long context, 4 new tokens per sequence "
+                 "(multi-query), B=16, seq_lens uniform on [65536, 131072]", B=16, S=131072,
+                 seed=10, lengths=lengths_uniform(65536, 131072, 16), layers=("global",),
+                 queries=4),
+        Workload("sliding_mq8_b64_s32768", "slidingDecodeGQA batched, 8 new tokens per sequence "
+                 "(multi-query), B=64, seq_lens uniform on [1, 32768]", B=64, S=32768, seed=11,
+                 lengths=lengths_uniform(1, 32768, 64), layers=("sliding",), queries=8),
+        Workload("global_mq4_b8_s8192", "decodeGQA, 4 new tokens per sequence (multi-query), B=8, "
+                 "seq_lens uniform on [1, 8192]", B=8, S=8192, seed=12,
+                 lengths=lengths_uniform(1, 8192, 8), layers=("global",), queries=4),
+        # One new token through the multi-query (tensor-core) kernel, at the single-query
+        # shapes' seeds and lengths: the two kernels side by side on the same input.
+        Workload("global_mq1_b8_s8192", "decodeGQA, B=8, seq_lens uniform on [1, 8192], one "
+                 "new token through the multi-query kernel", B=8, S=8192, seed=1,
+                 lengths=lengths_uniform(1, 8192, 8), layers=("global",), queries=1),
+        Workload("global_mq1_b16_s131072", "decodeGQA long context, B=16, seq_lens uniform on "
+                 "[65536, 131072], one new token through the multi-query kernel", B=16,
+                 S=131072, seed=3, lengths=lengths_uniform(65536, 131072, 16),
+                 layers=("global",), queries=1),
         # Smaller instance of the batched sliding shape for profiler captures: the same
         # bytes per call as sliding_b64_s32768 (every sequence reads its full 1024-position
         # window) with a 2 GB cache instead of 34 GB.
