@@ -19,7 +19,7 @@
 // elements (16 KB, 128-byte swizzled, exactly what TMA writes); the P.V mma of a
 // 128-wide head-dim block reads two adjacent stages.
 //
-// Warp roles (224 threads).  Warp 0, lane 0: the producer.  It walks the same
+// Warp roles (352 threads).  Warp 0, lane 0: the producer.  It walks the same
 // schedule as the single-query kernel (static units, then claimed dynamic chunks)
 // and streams the tiles in the order K(0), K(1), V(0), K(2), V(1), ...: the scores
 // of tile i+1 are computed while the softmax of tile i runs.  K blocks go to one
@@ -28,12 +28,14 @@
 // earlier fill of the same stage).  It also loads each
 // piece's Q with TMA (box: 64 elements x g heads x T tokens) into one of two
 // buffers.  Warp 1: owns the TMEM allocation; lane 0 issues the scores' mma.
-// Warp 6: lane 0 issues the P.V mma, and the whole warp zeroes the V rows of a tile
+// Warp 10: lane 0 issues the P.V mma, and the whole warp zeroes the V rows of a tile
 // that lie outside its sequence's attended range before they are read (0 * NaN
 // would poison the sum).  A tcgen05.mma costs its issuing thread about 75 cycles
 // whatever N is up to 128, so two issuing warps keep the tensor core busier.
-// Warps 2..5: thread j owns TMEM lane j, i.e. position j of the tile's scores and
-// head-dim element j of each O^T block; they run the softmax and the epilogue.
+// Warps 2..9: thread j of lane quarter warp % 4 owns TMEM lane j, i.e. position j
+// of the tile's scores and head-dim element j of each O^T block; they run the
+// softmax and the epilogue, the two warps of a quarter splitting the query rows
+// (two warps per scheduler hide each other's latencies).
 //
 // Pieces alternate between two O^T buffers in TMEM: a piece's output is written
 // after the next tile's P has been published, so the softmax warps never wait
@@ -63,9 +65,9 @@ constexpr float kMqTau = 24.0f;                    // rescale threshold, log2 un
 constexpr int kMqPLbo = 144;                       // P core matrices along positions (padded
                                                    // from 128 B so stores hit distinct banks)
 constexpr int kMqPSbo = (kMqTile / 8) * kMqPLbo;   // P 8-row groups: 2304 B
-constexpr int kMqThreads = 224;         // producer, scores, 4 softmax warps, P.V
-constexpr int kMqSoftmaxThreads = 128;
-constexpr int kMqPvWarp = 6;
+constexpr int kMqThreads = 352;         // producer, scores, 8 softmax warps, P.V
+constexpr int kMqSoftmaxThreads = 256;
+constexpr int kMqPvWarp = 10;
 
 constexpr int tmem_cols_for(int cols) {
     int c = 32;
@@ -134,7 +136,7 @@ struct alignas(1024) MqSmem {
                                       // with the last p_full; larger until then)
     PlanSmem plan;
     float red[4][Cfg::NMAX];
-    uint32_t red_bad[4];
+    uint32_t red_bad[8];
     float epi_m[Cfg::NMAX];   // the finished piece whose epilogue is pending: reference max,
     float epi_l[Cfg::NMAX];   // normaliser and bad-page bits per query row
     uint32_t epi_bad;
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                   const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
     constexpr int D = Cfg::D, G = Cfg::G, NSUB = Cfg::NSUB, NB = Cfg::NB, STAGES = Cfg::STAGES;
     constexpr int KST = Cfg::KST, VST = Cfg::VST;
-    constexpr int NMAX = Cfg::NMAX, RMAX = Cfg::RMAX, MAXT = Cfg::MAXT;
+    constexpr int NMAX = Cfg::NMAX;
 
     extern __shared__ uint8_t smem_raw[];
     MqSmem<Cfg>& sm = *reinterpret_cast<MqSmem<Cfg>*>(
@@ -176,10 +178,10 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         ptx::mbar_init(ptx::smem_addr(&sm.q_empty), 1);
         for (int j = 0; j < 2; ++j) {
             ptx::mbar_init(ptx::smem_addr(&sm.s_full[j]), 2);   // mma commit + the tile's descriptor
-            ptx::mbar_init(ptx::smem_addr(&sm.p_full[j]), 4);   // one arrival per softmax warp
+            ptx::mbar_init(ptx::smem_addr(&sm.p_full[j]), 8);   // one arrival per softmax warp
             ptx::mbar_init(ptx::smem_addr(&sm.p_empty[j]), 1);
             ptx::mbar_init(ptx::smem_addr(&sm.o_ready[j]), 1);
-            ptx::mbar_init(ptx::smem_addr(&sm.s_empty[j]), 4);   // one arrival per softmax warp
+            ptx::mbar_init(ptx::smem_addr(&sm.s_empty[j]), 8);   // one arrival per softmax warp
             ptx::mbar_init(ptx::smem_addr(&sm.drain[j]), 1);
         }
         sm.pv_stop = 0x7fffffff;
@@ -564,19 +566,26 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         }
         __syncwarp();
     } else {
-        // ====================== softmax and epilogue (warps 2..5) ======================
-        const int j = 32 * (warp & 3) + lane;   // TMEM lane: tile position / head-dim element
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+        // ================ softmax and epilogue (warps 2..9, two per TMEM lane quarter) ================
+        // Thread j of lane quarter q (warp % 4) owns TMEM lane j: position j of the
+        // tile's scores and head-dim element j of each O^T block.  The two warps of a
+        // quarter split the query rows: warps 2..5 rows [0, RH), warps 6..9 [RH, 2 RH).
+        constexpr int RH = NMAX / 2;
+        const int q4 = warp & 3;
+        const int r0 = ((warp - 2) >> 2) * RH;      // first row of this warp
+        const int j = 32 * q4 + lane;
+        const int sid = tid - 64;                    // 0 .. 255 over the softmax warps
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         const float nan = __uint_as_float(0x7fc00000u);
-        float m_ref[RMAX], l_part[RMAX];
+        float m_ref[RH], l_part[RH];
 #pragma unroll
-        for (int r = 0; r < RMAX; ++r) {
-            m_ref[r] = -INFINITY;
-            l_part[r] = 0.0f;
+        for (int k = 0; k < RH; ++k) {
+            m_ref[k] = -INFINITY;
+            l_part[k] = 0.0f;
         }
         uint32_t bad_q = 0;   // bit t: query t attended a bad page in this piece
         // P rows past the query rows in use stay zero (the P.V mma reads 2 NMAX rows)
-        for (int i = j; i < 2 * Cfg::PBYTES / 16; i += kMqSoftmaxThreads)
+        for (int i = sid; i < 2 * Cfg::PBYTES / 16; i += kMqSoftmaxThreads)
             ptx::sts128(ptx::smem_addr(&sm.pm[0][0]) + i * 16, 0u, 0u, 0u, 0u);
         ptx::named_barrier_sync(3, kMqSoftmaxThreads);
         // A finished piece whose output is still to be written: its last tile and
@@ -585,9 +594,9 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         MqTile epi;
         uint32_t epi_i = 0;
         epi.b = epi.kvh = epi.slot = epi.ob = 0;
-        // Writes the pending piece's output: waits for its last P.V, then reads its
-        // O^T buffer and stores the normalised rows (a piece that is its whole
-        // segment) or the partial (acc, m, l).  False when the CTA is aborting.
+        // Writes the pending piece's output: waits for its last P.V, then reads this
+        // warp's rows of its O^T buffer and stores the normalised rows (a piece that is
+        // its whole segment) or the partial (acc, m, l).  False when the CTA is aborting.
         auto finish_piece = [&]() -> bool {
             const bool okw = wait_bounded(ptx::smem_addr(&sm.o_ready[epi_i & 1u]), (epi_i >> 1) & 1u,
                                           &sm.abort_flag, p.ws_flags);
@@ -596,25 +605,23 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             const uint32_t bad_all = sm.epi_bad;
             const SegmentParts sp(pl, epi.b, epi.kvh, p.dyn_slot_base);
             const bool direct = sp.count() == 1;
+            if (r0 < R) {
 #pragma unroll
-            for (int mb = 0; mb < NB; ++mb) {
-#pragma unroll
-                for (int c0 = 0; c0 < NMAX; c0 += 16) {
-                    if (c0 >= N) break;
+                for (int mb = 0; mb < NB; ++mb) {
                     // row r's sum is its hi column r plus its lo column NMAX + r
-                    uint32_t oh[16], ol[16];
-                    const uint32_t ob = lane_addr + Cfg::TMEM_O + epi.ob * Cfg::OBUF + mb * 2 * NMAX + c0;
-                    ptx::tmem_ld16(ob, oh);
-                    ptx::tmem_ld16(ob + NMAX, ol);
+                    uint32_t oh[RH], ol[RH];
+                    const uint32_t ob = lane_addr + Cfg::TMEM_O + epi.ob * Cfg::OBUF + mb * 2 * NMAX + r0;
+                    ptx::tmem_ld<RH>(ob, oh);
+                    ptx::tmem_ld<RH>(ob + NMAX, ol);
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const int r = c0 + c;
+                    for (int k = 0; k < RH; ++k) {
+                        const int r = r0 + k;
                         if (r >= R) break;
                         const int t = r / G, g = r - (r / G) * G;
                         const bool bad = (bad_all >> t) & 1u;
                         const int dd = mb * 128 + j;
-                        const float acc = __uint_as_float(oh[c]) + __uint_as_float(ol[c]);
+                        const float acc = __uint_as_float(oh[k]) + __uint_as_float(ol[k]);
                         if (direct) {
                             const size_t row = (static_cast<size_t>(epi.b) * T + t) * H + epi.kvh * G + g;
                             const float lr = sm.epi_l[r];
@@ -626,11 +633,11 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                     }
                 }
             }
-            if (!direct && j < R) {
-                const bool bad = (bad_all >> (j / G)) & 1u;
-                float* ml = p.ws_ml + (static_cast<size_t>(epi.slot) * R + j) * 2;
-                ml[0] = bad ? 0.0f : sm.epi_m[j];
-                ml[1] = bad ? nan : sm.epi_l[j];
+            if (!direct && sid < R) {
+                const bool bad = (bad_all >> (sid / G)) & 1u;
+                float* ml = p.ws_ml + (static_cast<size_t>(epi.slot) * R + sid) * 2;
+                ml[0] = bad ? 0.0f : sm.epi_m[sid];
+                ml[1] = bad ? nan : sm.epi_l[sid];
             }
             ptx::tc_fence_before();
             return true;
@@ -648,16 +655,16 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 ok = wait_bounded(ptx::smem_addr(&sm.p_empty[i & 1u]), ((i >> 1) & 1u) ^ 1u,
                                   &sm.abort_flag, p.ws_flags);
                 if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
-                if (j == 0) sm.pv_stop = static_cast<int>(i);
+                if (sid == 0) sm.pv_stop = static_cast<int>(i);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.p_full[i & 1u]));
                 break;
             }
             if (d.flags & kDescFirst) {
 #pragma unroll
-                for (int r = 0; r < RMAX; ++r) {
-                    m_ref[r] = -INFINITY;
-                    l_part[r] = 0.0f;
+                for (int k = 0; k < RH; ++k) {
+                    m_ref[k] = -INFINITY;
+                    l_part[k] = 0.0f;
                 }
                 bad_q = 0;
             }
@@ -669,52 +676,45 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 const int page = p.block_table[static_cast<size_t>(d.b) * p.max_pages + (pos >> 4)];
                 page_bad = page < 0 || page >= p.num_pages;
             }
-            // scores of position j, log2 units, masked per query
-            uint32_t sr0[16], sr1[16];
-            ptx::tmem_ld16(lane_addr + Cfg::TMEM_S + (i & 1u) * NMAX, sr0);
-            if (N > 16) ptx::tmem_ld16(lane_addr + Cfg::TMEM_S + (i & 1u) * NMAX + 16, sr1);
+            // scores of position j for this warp's rows, log2 units, masked per query
+            uint32_t sr[RH];
+            ptx::tmem_ld<RH>(lane_addr + Cfg::TMEM_S + (i & 1u) * NMAX + r0, sr);
             ptx::tmem_wait_ld();
             // S buffer i % 2 may take the scores of tile i + 2
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.s_empty[i & 1u]));
-            float s[RMAX];
+            float s[RH];
             bool need = false;
 #pragma unroll
-            for (int t = 0; t < MAXT; ++t) {
+            for (int k = 0; k < RH; ++k) {
+                const int r = r0 + k;
+                const int t = r / G;
                 const int hi_t = L - T + t + 1;
                 const int lo_t = (p.window > 0 && hi_t > p.window) ? hi_t - p.window : 0;
-                const bool valid = t < T && in_piece && pos >= lo_t && pos < hi_t;
+                const bool valid = r < R && in_piece && pos >= lo_t && pos < hi_t;
                 if (valid && page_bad) bad_q |= 1u << t;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const int r = t * G + g;
-                    const uint32_t raw = r < 16 ? sr0[r & 15] : sr1[r & 15];
-                    s[r] = valid ? __uint_as_float(raw) * kLog2e : -INFINITY;
-                    need |= s[r] > m_ref[r] + kMqTau;
-                }
+                s[k] = valid ? __uint_as_float(sr[k]) * kLog2e : -INFINITY;
+                need |= s[k] > m_ref[k] + kMqTau;
             }
             if (ptx::named_barrier_or(2, kMqSoftmaxThreads, need)) {
                 // new reference max of every row: the tile's max where it is larger
 #pragma unroll
-                for (int r = 0; r < RMAX; ++r) {
-                    if (r >= R) break;
-                    float mx = s[r];
+                for (int k = 0; k < RH; ++k) {
+                    float mx = s[k];
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                    if (lane == 0) sm.red[warp & 3][r] = mx;
+                    if (lane == 0) sm.red[q4][r0 + k] = mx;
                 }
                 ptx::named_barrier_sync(3, kMqSoftmaxThreads);
-                float alpha[RMAX];
+                float alpha[RH];
 #pragma unroll
-                for (int r = 0; r < RMAX; ++r) alpha[r] = 1.0f;   // rows past R are unused
-#pragma unroll
-                for (int r = 0; r < RMAX; ++r) {
-                    if (r >= R) break;
+                for (int k = 0; k < RH; ++k) {
+                    const int r = r0 + k;
                     const float mt = fmaxf(fmaxf(sm.red[0][r], sm.red[1][r]), fmaxf(sm.red[2][r], sm.red[3][r]));
-                    const float mn = fmaxf(m_ref[r], mt);
-                    alpha[r] = (m_ref[r] == -INFINITY || mn == -INFINITY) ? 0.0f : exp2f(m_ref[r] - mn);
-                    m_ref[r] = mn;
+                    const float mn = fmaxf(m_ref[k], mt);
+                    alpha[k] = (m_ref[k] == -INFINITY || mn == -INFINITY) ? 0.0f : exp2f(m_ref[k] - mn);
+                    m_ref[k] = mn;
                 }
                 ptx::named_barrier_sync(3, kMqSoftmaxThreads);
                 if (!(d.flags & kDescFirst)) {
@@ -727,46 +727,40 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                     ptx::tc_fence_after();
 #pragma unroll
                     for (int mb = 0; mb < NB; ++mb) {
+                        // the hi column and the lo column of each row
 #pragma unroll
-                        for (int c0 = 0; c0 < NMAX; c0 += 16) {
-                            if (c0 >= N) break;
-                            // the hi column and the lo column of each row
+                        for (int part = 0; part < 2; ++part) {
+                            uint32_t o[RH];
+                            const uint32_t ta = lane_addr + Cfg::TMEM_O + d.ob * Cfg::OBUF +
+                                                mb * 2 * NMAX + part * NMAX + r0;
+                            ptx::tmem_ld<RH>(ta, o);
+                            ptx::tmem_wait_ld();
 #pragma unroll
-                            for (int part = 0; part < 2; ++part) {
-                                uint32_t o[16];
-                                const uint32_t ta = lane_addr + Cfg::TMEM_O + d.ob * Cfg::OBUF +
-                                                    mb * 2 * NMAX + part * NMAX + c0;
-                                ptx::tmem_ld16(ta, o);
-                                ptx::tmem_wait_ld();
-#pragma unroll
-                                for (int c = 0; c < 16; ++c)
-                                    o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[c0 + c]);
-                                ptx::tmem_st16(ta, o);
-                            }
+                            for (int k = 0; k < RH; ++k)
+                                o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha[k]);
+                            ptx::tmem_st<RH>(ta, o);
                         }
                     }
                     ptx::tmem_wait_st();
 #pragma unroll
-                    for (int r = 0; r < RMAX; ++r) l_part[r] *= alpha[r];
+                    for (int k = 0; k < RH; ++k) l_part[k] *= alpha[k];
                 }
             }
             // P buffer i % 2 is free once the P.V of tile i - 2 is done
             ok = wait_bounded(ptx::smem_addr(&sm.p_empty[i & 1u]), ((i >> 1) & 1u) ^ 1u, &sm.abort_flag,
                               p.ws_flags);
             if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
-            {
-                // hi part in row r, lo part in row NMAX + r
+            if (r0 < N) {
+                // hi part in row r, lo part in row NMAX + r; rows past R stay zero
                 const uint32_t pb = ptx::smem_addr(&sm.pm[i & 1u][0]);
 #pragma unroll
-                for (int r = 0; r < NMAX; ++r) {
-                    if (r >= N) break;
-                    // rows past R (padding up to N) stay zero
-                    const float pv = (r < R && s[r] != -INFINITY) ? exp2f(s[r] - m_ref[r]) : 0.0f;
-                    l_part[r] += pv;
+                for (int k = 0; k < RH; ++k) {
+                    const float pv = s[k] != -INFINITY ? exp2f(s[k] - m_ref[k]) : 0.0f;
+                    l_part[k] += pv;
                     const __nv_bfloat16 hb = __float2bfloat16_rn(pv);
                     const __nv_bfloat16 lb = __float2bfloat16_rn(pv - __bfloat162float(hb));
-                    ptx::sts16(pb + mq_p_off(r, j), *reinterpret_cast<const uint16_t*>(&hb));
-                    ptx::sts16(pb + mq_p_off(NMAX + r, j), *reinterpret_cast<const uint16_t*>(&lb));
+                    ptx::sts16(pb + mq_p_off(r0 + k, j), *reinterpret_cast<const uint16_t*>(&hb));
+                    ptx::sts16(pb + mq_p_off(NMAX + r0 + k, j), *reinterpret_cast<const uint16_t*>(&lb));
                 }
             }
             // one O^T buffer: the pending piece's output is read before this new piece's
@@ -775,46 +769,41 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 if (!finish_piece()) break;
                 epi_pending = false;
             }
-            if (j == 0) sm.p_desc[i & 1u] = d;
+            if (sid == 0) sm.p_desc[i & 1u] = d;
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.p_full[i & 1u]));
-            if (!(d.flags & kDescLast)) {
-                if (epi_pending) {
-                    if (!finish_piece()) break;
-                    epi_pending = false;
-                }
-                continue;
-            }
-
-            // ---- the piece is complete: its normaliser now, its output after the next
-            // tile's P (so the softmax of that tile does not wait for this P.V) ----
             if (epi_pending) {
                 if (!finish_piece()) break;
                 epi_pending = false;
             }
+            if (!(d.flags & kDescLast)) continue;
+
+            // ---- the piece is complete: its normaliser now, its output after the next
+            // tile's P (so the softmax of that tile does not wait for this P.V) ----
 #pragma unroll
-            for (int r = 0; r < RMAX; ++r) {
-                if (r >= R) break;
-                float v = l_part[r];
+            for (int k = 0; k < RH; ++k) {
+                float v = l_part[k];
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                if (lane == 0) sm.red[warp & 3][r] = v;
+                if (lane == 0) sm.red[q4][r0 + k] = v;
             }
             const uint32_t bq = __reduce_or_sync(0xffffffffu, bad_q);
-            if (lane == 0) sm.red_bad[warp & 3] = bq;
+            if (lane == 0) sm.red_bad[warp - 2] = bq;
             ptx::named_barrier_sync(3, kMqSoftmaxThreads);
-            if (j < NMAX) {
-                float mj = 0.0f;
+            if (sid < NMAX)
+                sm.epi_l[sid] = (sm.red[0][sid] + sm.red[1][sid]) + (sm.red[2][sid] + sm.red[3][sid]);
+            if (q4 == 0 && lane < RH) {
+                float mk = 0.0f;
 #pragma unroll
-                for (int r = 0; r < RMAX; ++r)
-                    if (r == j) mj = m_ref[r];
-                sm.epi_m[j] = mj;
-                sm.epi_l[j] = (sm.red[0][j] + sm.red[1][j]) + (sm.red[2][j] + sm.red[3][j]);
+                for (int k = 0; k < RH; ++k)
+                    if (k == lane) mk = m_ref[k];
+                sm.epi_m[r0 + lane] = mk;
             }
-            if (j == 0) {
-                const uint32_t bad_all = sm.red_bad[0] | sm.red_bad[1] | sm.red_bad[2] | sm.red_bad[3];
+            if (sid == 0) {
+                uint32_t bad_all = 0;
+                for (int w = 0; w < 8; ++w) bad_all |= sm.red_bad[w];
                 sm.epi_bad = bad_all;
                 if (bad_all) atomicOr(p.ws_flags, kFlagBadPage);
             }
