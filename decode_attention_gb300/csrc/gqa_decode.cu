@@ -54,16 +54,20 @@ constexpr size_t kHeaderBytes = kSegsOff + kMaxSegments * 16;
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WorkspaceLayout {
-    size_t ml_off, acc_off, total;
+    size_t ml_off, acc_off, operand_off, total;
 };
 
+// G = query rows per segment.  On the decodeGQA geometry the workspace also holds the
+// single K=V path's scores operand, [B, KVH, 16, 512] bf16.
 WorkspaceLayout layout_for(int B, int KVH, int G, int D) {
     const size_t slots = static_cast<size_t>(kMaxCtas) + static_cast<size_t>(B) * KVH +
                          gqa::kMaxDynUnits;
     WorkspaceLayout w;
     w.ml_off = align256(kHeaderBytes);
     w.acc_off = align256(w.ml_off + slots * G * 2 * sizeof(float));
-    w.total = align256(w.acc_off + slots * G * D * sizeof(float));
+    w.operand_off = align256(w.acc_off + slots * G * D * sizeof(float));
+    const size_t operand = (KVH == 4 && D == 512) ? static_cast<size_t>(B) * KVH * 16 * D * 2 : 0;
+    w.total = align256(w.operand_off + operand);
     return w;
 }
 
@@ -214,7 +218,8 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
         a.p.w_k = static_cast<const __nv_bfloat16*>(w_k);
         for (int i = 0; i < 64; ++i)
             a.p.rope_freq[i] = std::pow(kGlobalRopeTheta, -2.0 * i / static_cast<double>(c.D));
-        return gqa::launch_global_keqv(a, paged) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+        a.p.keqv_operand = reinterpret_cast<__nv_bfloat16*>(w + lay.operand_off);
+        return gqa::launch_keqv_tc(a, paged) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
     }
     if (multi_query)
         return gqa::launch_mq(a, c.geo == Geometry::kSliding, paged) == cudaSuccess ? GQA_OK

@@ -97,6 +97,10 @@ struct DecodeParams {
     // frequencies theta^(-2i/D) of the rotated pairs, in fp64
     const __nv_bfloat16* w_k;
     double rope_freq[64];
+    // the tensor-core single K=V path: the scores' B operand of every segment,
+    // [B, KVH, 2 G, D] bf16 in the workspace (rows [0, G): q * w hi, rows [G, 2 G): lo,
+    // with the raw q and zeros on the rotated dims)
+    __nv_bfloat16* keqv_operand;
 };
 
 // Unpack 2 x bf16 (low half first) to fp32.
@@ -482,8 +486,9 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
     static_assert(TP % kBoxRows == 0, "tile must be whole boxes");
 
     extern __shared__ uint8_t smem_raw[];
-    KernelSmem<Pol>& sm = *reinterpret_cast<KernelSmem<Pol>*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // aligned to 1024 B by pointer arithmetic on smem_raw, so that the compiler still
+    // sees shared-memory accesses through sm
+    KernelSmem<Pol>& sm = *reinterpret_cast<KernelSmem<Pol>*>(smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u));
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;

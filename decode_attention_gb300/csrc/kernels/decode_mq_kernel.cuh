@@ -55,6 +55,8 @@
 // released before the CTA exits.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_kernel.cuh"
 
 namespace gqa {
@@ -75,11 +77,16 @@ constexpr int tmem_cols_for(int cols) {
     return c;
 }
 
-template <int kD, int kG, int kMaxT, int kKStages, int kVStages, int kObufs>
+template <int kD, int kG, int kMaxT, int kKStages, int kVStages, int kObufs, bool kKeqV = false,
+          int kRStages = 0>
 struct MqCfg {
     static constexpr int D = kD, G = kG, MAXT = kMaxT, OBUFS = kObufs;
-    // two stage rings, each consumed in order by one warp: K (scores warp) and V (P.V warp)
-    static constexpr int KST = kKStages, VST = kVStages, STAGES = kKStages + kVStages;
+    // stage rings, each consumed in order by one warp: K (scores warp), V (P.V warp) and,
+    // over a single K=V cache, R (the rotated dims, read by the softmax warps to
+    // derive the rotated keys)
+    static constexpr bool KEQV = kKeqV;
+    static constexpr int KST = kKStages, VST = kVStages, RST = kRStages;
+    static constexpr int STAGES = kKStages + kVStages + kRStages;
     static constexpr int NSUB = D / 64;                 // stages per tile of one tensor
     static constexpr int NB = D / 128;                  // 128-wide head-dim blocks of O^T
     static constexpr int RMAX = G * MAXT;               // query rows of a segment
@@ -90,17 +97,40 @@ struct MqCfg {
     static constexpr int TMEM_S = 0;                    // S^T buffers: columns [0, 2 NMAX)
     static constexpr int TMEM_O = 2 * NMAX;             // O^T: OBUFS piece buffers of NB blocks
     static constexpr int OBUF = NB * 2 * NMAX;          // of 2 NMAX columns (hi part, lo part)
-    static constexpr int TMEM_COLS = tmem_cols_for(TMEM_O + OBUFS * OBUF);
-    static_assert(TMEM_O + OBUFS * OBUF <= 512, "TMEM holds 512 columns");
+    // K=V: the derived rotated keys of a tile, the A operand of the rotated k-steps:
+    // 128 rows x 128 bf16 (rotated dims i and D/2 + i, i < 64), hi then lo
+    static constexpr int TMEM_KROT = TMEM_O + OBUFS * OBUF;
+    static constexpr int KROT_COLS = KEQV ? 128 : 0;
+    static constexpr int NK = KEQV ? NSUB - 2 : NSUB;   // stages of a K block
+    static constexpr int TMEM_COLS = tmem_cols_for(TMEM_KROT + KROT_COLS);
+    static_assert(TMEM_KROT + KROT_COLS <= 512, "TMEM holds 512 columns");
     static_assert(OBUFS == 1 || OBUFS == 2, "one or two O^T buffers");
+    static_assert(!KEQV || (D == 512 && G == 8 && MAXT == 1 && RST == 2), "K=V: decodeGQA, one query");
     static_assert(VST % 2 == 0, "a P.V block reads two adjacent stages");
     static_assert(NSUB % 2 == 0 && RMAX <= 32, "geometry");
-    static_assert(RMAX == NMAX, "query rows fill the mma N bound");
+    // query rows fill the mma N bound; over a K=V cache the scores' B operand holds
+    // the hi and the lo parts of q * w as 2 RMAX rows
+    static_assert(RMAX == NMAX || (KEQV && 2 * RMAX == NMAX), "query rows fill the mma N bound");
 };
 
 using MqGlobal = MqCfg<512, 8, 4, 4, 4, 1>;     // decodeGQA, T <= 4
 using MqGlobal2 = MqCfg<512, 8, 2, 4, 6, 2>;   // decodeGQA, T <= 2: smaller Q and P, more stages
 using MqSliding = MqCfg<256, 2, 8, 4, 6, 2>;   // slidingDecodeGQA, T <= 8
+using MqKeqV = MqCfg<512, 8, 1, 4, 4, 2, true, 2>;   // decodeGQA over a single K=V cache
+
+// Rotation tables of the K=V key derivation (rotated pair i < 64, angle of position
+// t + j for tile row j = 16 a + b): cos and sin of 16 a f_i and of b f_i, once per CTA;
+// per tile, cos and sin of t f_i and of (t + 16 a) f_i.  Indexed pair-major, so the
+// lanes of a warp (consecutive rows) read consecutive words.
+struct MqRopeTables {
+    float2 coarse[64][8];
+    float2 fine[64][16];
+    float2 base[64];
+    float2 tile[64][8];
+    float w[128];        // k_norm weight of the rotated dims: w[i], then w[D/2 + i]
+    double freq[64];     // f_i = theta^(-2i/D)
+};
+struct MqNoTables {};
 
 struct MqTile {
     int b, kvh;
@@ -112,7 +142,7 @@ struct MqTile {
     int ob;         // O^T buffer of the piece (pieces alternate)
 };
 
-constexpr int kMqKindK = 0, kMqKindV = 1, kMqKindDone = 2;
+constexpr int kMqKindK = 0, kMqKindV = 1, kMqKindDone = 2, kMqKindR = 3, kMqKindDoneR = 4;
 
 template <class Cfg>
 struct alignas(1024) MqSmem {
@@ -130,6 +160,10 @@ struct alignas(1024) MqSmem {
     alignas(8) uint64_t drain[2];     // the two mma warps' final commits
     int kind[Cfg::KST];               // K ring: a K block or the end-of-work marker
     MqTile desc[Cfg::KST];            // tile of a K block (its first stage)
+    int rkind[Cfg::KEQV ? Cfg::RST : 1];       // R ring: an R block or the end-of-work marker
+    MqTile rdesc[Cfg::KEQV ? Cfg::RST : 1];    // tile of an R block (its first stage)
+    alignas(8) uint64_t krot_full;             // K=V: the derived keys of the next tile are in TMEM
+    alignas(16) std::conditional_t<Cfg::KEQV, MqRopeTables, MqNoTables> rope;
     MqTile s_desc[2];                 // tile whose scores are in S buffer j
     MqTile p_desc[2];                 // tile whose P is in P buffer j
     int pv_stop;                      // index of the first tile that does not exist (set
@@ -158,8 +192,9 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     constexpr int NMAX = Cfg::NMAX;
 
     extern __shared__ uint8_t smem_raw[];
-    MqSmem<Cfg>& sm = *reinterpret_cast<MqSmem<Cfg>*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // aligned to 1024 B by pointer arithmetic on smem_raw, so that the compiler still
+    // sees shared-memory accesses through sm
+    MqSmem<Cfg>& sm = *reinterpret_cast<MqSmem<Cfg>*>(smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u));
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -184,6 +219,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             ptx::mbar_init(ptx::smem_addr(&sm.s_empty[j]), 8);   // one arrival per softmax warp
             ptx::mbar_init(ptx::smem_addr(&sm.drain[j]), 1);
         }
+        ptx::mbar_init(ptx::smem_addr(&sm.krot_full), 8);   // one arrival per softmax warp
         sm.pv_stop = 0x7fffffff;
         ptx::fence_mbar_init();
         sm.abort_flag = 0;
@@ -229,8 +265,10 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     const uint32_t tmem = sm.tmem_base;
     const uint32_t stage0 = ptx::smem_addr(&sm.stage[0][0]);
     // Stage q of the K ring is stage[q % KST]; stage q of the V ring is stage[KST + q % VST].
+    constexpr int RST1 = Cfg::RST > 0 ? Cfg::RST : 1;
     auto kst = [&](uint32_t q) { return static_cast<int>(q % KST); };
     auto vst = [&](uint32_t q) { return KST + static_cast<int>(q % VST); };
+    auto rstg = [&](uint32_t q) { return KST + VST + static_cast<int>(q % RST1); };
     // bounded wait (whole warp) for K-ring (v = false) or V-ring stage q to be full
     auto wait_full = [&](bool v, uint32_t q) -> bool {
         const int s = v ? vst(q) : kst(q);
@@ -243,9 +281,11 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         // ============================ producer ============================
         if (lane == 0) {
             const uint64_t policy = ptx::policy_evict_first();
-            const uint32_t q_bytes = static_cast<uint32_t>(NSUB * R * 128);
+            // Q rows: the query rows, or over a K=V cache the hi and lo rows of q * w
+            const uint32_t q_bytes = static_cast<uint32_t>(NSUB * (Cfg::KEQV ? 2 * R : R) * 128);
             constexpr uint32_t kPageBytes = kPageRows * 128;
-            uint32_t kseq = 0, vseq = 0;   // stages issued on the K and V rings
+            uint32_t kseq = 0, vseq = 0, rseq = 0;   // stages issued on the K, V and R rings
+            const uint64_t policy_keep = ptx::policy_evict_normal();
             uint32_t n_piece = 0;    // pieces started (O^T buffer n_piece & 1)
             bool ok = true;
             // Q of the newest piece, when its load still waits for the previous piece's
@@ -261,9 +301,15 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 // piece n (= q_issued) may overwrite Q once the last scores of piece n - 1 are done
                 if (q_pend && ptx::mbar_try_wait(q_empty_bar, (q_issued & 1u) ^ 1u)) {
                     const uint32_t qdst = ptx::smem_addr(&sm.q[0]);
-                    for (int c = 0; c < NSUB; ++c)
-                        ptx::tma_load_4d(qdst + c * Cfg::QATOM, &tm_q, q_bar, 64 * c, q_kvh * G, 0, q_b,
-                                         policy);
+                    for (int c = 0; c < NSUB; ++c) {
+                        // (elements, rows, ...): the q rows of the KV head's group, or the
+                        // K=V scores operand [B, KVH, 2 G, D] of the segment
+                        if (Cfg::KEQV)
+                            ptx::tma_load_4d(qdst + c * Cfg::QATOM, &tm_q, q_bar, 64 * c, 0, q_kvh, q_b, policy);
+                        else
+                            ptx::tma_load_4d(qdst + c * Cfg::QATOM, &tm_q, q_bar, 64 * c, q_kvh * G, 0, q_b,
+                                             policy);
+                    }
                     q_pend = false;
                     ++q_issued;
                 }
@@ -292,33 +338,42 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             MqTile prev;
             bool have_prev = false;
 
-            // One block (NSUB stages) of tile d: its K or V rows, or (kind Done) empty stages.
+            // One block of tile d: its K rows (NK stages), V rows (NSUB stages) or, on a K=V
+            // cache, the rotated dims (R, 2 stages); or an end-of-work marker on the K or
+            // the R ring.  Over a K=V cache, the K and R blocks are the first read of the
+            // value tile (kept in L2 for the V block's second read); the R block holds the
+            // column blocks of dims [0, 64) and [D/2, D/2 + 64), the K block the others.
             auto emit_block = [&](const MqTile& d, int kind) -> bool {
                 const int32_t* bt_row =
                     kPaged ? p.block_table + static_cast<size_t>(d.b) * p.max_pages : nullptr;
                 // paged: load the pages that hold attended positions of the sequence
                 const int npage = kPaged ? (d.zhi + kPageRows - 1) / kPageRows : 0;
-                const bool on_v = kind == kMqKindV;
-                for (int sub = 0; sub < NSUB; ++sub) {
-                    uint32_t& seq = on_v ? vseq : kseq;
-                    const int s = on_v ? vst(seq) : kst(seq);
-                    const uint32_t ph = (seq / (on_v ? VST : KST)) & 1u;
+                const int ring = (kind == kMqKindV) ? 1 : (kind == kMqKindR || kind == kMqKindDoneR) ? 2 : 0;
+                const int nst = ring == 1 ? NSUB : ring == 2 ? 2 : Cfg::NK;
+                const uint64_t pol = (Cfg::KEQV && ring != 1) ? policy_keep : policy;
+                for (int sub = 0; sub < nst; ++sub) {
+                    uint32_t& seq = ring == 1 ? vseq : ring == 2 ? rseq : kseq;
+                    const int s = ring == 1 ? vst(seq) : ring == 2 ? rstg(seq) : kst(seq);
+                    const uint32_t ph = (seq / (ring == 1 ? VST : ring == 2 ? RST1 : KST)) & 1u;
                     if (!wait_servicing(ptx::smem_addr(&sm.empty[s]), ph ^ 1u)) return false;
-                    if (!on_v) sm.kind[s] = kind;
+                    if (ring == 0) sm.kind[s] = kind;
+                    if (ring == 2) sm.rkind[s - KST - VST] = kind;
                     const uint32_t full_bar = ptx::smem_addr(&sm.full[s]);
-                    if (kind == kMqKindDone) {
+                    if (kind == kMqKindDone || kind == kMqKindDoneR) {
                         ptx::mbar_arrive(full_bar);
                         ++seq;
                         continue;
                     }
                     const bool with_q = kind == kMqKindK && sub == 0 && (d.flags & kDescFirst);
-                    if (kind == kMqKindK && sub == 0) sm.desc[s] = d;
+                    // at most one Q load pending: the previous piece's goes out first
+                    if (with_q && !wait_servicing(0u, 0u)) return false;
+                    if (sub == 0 && ring == 0) sm.desc[s] = d;
+                    if (sub == 0 && ring == 2) sm.rdesc[s - KST - VST] = d;
                     const uint32_t bytes =
                         (kPaged ? static_cast<uint32_t>(npage) * kPageBytes : kMqStageBytes) +
                         (with_q ? q_bytes : 0u);
                     ptx::mbar_arrive_expect_tx(full_bar, bytes);
                     if (with_q) {
-                        // (emit_piece made sure no other Q is pending)
                         q_pend = true;
                         q_b = d.b;
                         q_kvh = d.kvh;
@@ -326,33 +381,51 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                     }
                     const CUtensorMap* map = kind == kMqKindK ? &tm_k : &tm_v;
                     const uint32_t dst = stage0 + s * kMqStageBytes;
-                    const int chunk = d.kvh * NSUB + sub;
+                    // column block of the stage: K=V K blocks skip blocks 0 and NSUB/2
+                    int cb = sub;
+                    if (Cfg::KEQV && ring == 0) cb = sub + 1 + (sub >= NSUB / 2 - 1 ? 1 : 0);
+                    if (ring == 2) cb = sub * (NSUB / 2);
+                    const int chunk = d.kvh * NSUB + cb;
                     if (kPaged) {
                         for (int j = 0; j < npage; ++j) {
                             int page = bt_row[(d.t >> 4) + j];
                             if (page < 0 || page >= p.num_pages) page = 0;   // flagged by the softmax warps
-                            ptx::tma_load_4d(dst + j * kPageBytes, map, full_bar, 0, 0, chunk, page, policy);
+                            ptx::tma_load_4d(dst + j * kPageBytes, map, full_bar, 0, 0, chunk, page, pol);
                         }
                     } else {
                         // rows past the end of the cache read as zeros
-                        ptx::tma_load_4d(dst, map, full_bar, 0, d.t, chunk, d.b, policy);
+                        ptx::tma_load_4d(dst, map, full_bar, 0, d.t, chunk, d.b, pol);
                     }
                     ++seq;
                     service_q();
                 }
                 return true;
             };
-            auto emit_tile = [&](MqTile cur) -> bool {
-                if (!emit_block(cur, kMqKindK)) return false;
-                if (have_prev && !emit_block(prev, kMqKindV)) return false;
-                prev = cur;
-                have_prev = true;
+            // Tiles arrive in order.  Multi-query: K(i), then V(i - 1).  K=V: K(i - 1), then
+            // R(i) one tile ahead (the softmax warps derive tile i's rotated keys while
+            // tile i - 1's scores are read), then V(i - 2).  K goes first: R(i) waits for
+            // the derivation of tile i - 1 to free the R ring, and K(i - 1) must not.
+            MqTile cur;
+            bool have_cur = false;
+            auto emit_tile = [&](MqTile nxt) -> bool {
+                if constexpr (Cfg::KEQV) {
+                    if (have_cur && !emit_block(cur, kMqKindK)) return false;
+                    if (!emit_block(nxt, kMqKindR)) return false;
+                    if (have_prev && !emit_block(prev, kMqKindV)) return false;
+                    prev = cur;
+                    have_prev = have_cur;
+                    cur = nxt;
+                    have_cur = true;
+                } else {
+                    if (!emit_block(nxt, kMqKindK)) return false;
+                    if (have_prev && !emit_block(prev, kMqKindV)) return false;
+                    prev = nxt;
+                    have_prev = true;
+                }
                 return true;
             };
             // The tiles of positions [p0, p1) of segment (b, kvh).
             auto emit_piece = [&](int b, int kvh, int p0, int p1, int slot, bool unit_end) -> bool {
-                // at most one Q load pending: the previous piece's goes out first
-                if (!wait_servicing(0u, 0u)) return false;
                 const uint32_t ob = n_piece & 1u;
                 ++n_piece;
                 const int lo = pl.lo[b], L = lo + pl.n[b];
@@ -411,15 +484,23 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                                  kvh * (pl.dn[b] + pl.dn1[b]) + local;
                 ok = emit_piece(b, kvh, p0, p0 + len, slot, true);
             }
-            // end of work: a Done block where the next K block would be, then the
-            // last tile's V block
+            // end of work: end-of-work markers where the next K (and R) block would be,
+            // then the blocks still owed
             if (ok) {
                 MqTile none;
                 none.b = none.kvh = none.t = none.vlo = none.vhi = none.zlo = none.zhi = 0;
                 none.slot = none.ob = 0;
                 none.flags = kDescDone;
-                ok = emit_block(none, kMqKindDone);
-                if (ok && have_prev) ok = emit_block(prev, kMqKindV);
+                if constexpr (Cfg::KEQV) {
+                    if (have_cur) ok = emit_block(cur, kMqKindK);
+                    if (ok) ok = emit_block(none, kMqKindDoneR);
+                    if (ok && have_prev) ok = emit_block(prev, kMqKindV);
+                    if (ok) ok = emit_block(none, kMqKindDone);
+                    if (ok && have_cur) ok = emit_block(cur, kMqKindV);
+                } else {
+                    ok = emit_block(none, kMqKindDone);
+                    if (ok && have_prev) ok = emit_block(prev, kMqKindV);
+                }
             }
             if (!ok) {
                 // let every copy already issued land before the CTA exits
@@ -427,6 +508,8 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                     wait_drain(ptx::smem_addr(&sm.full[kst(tt)]), (tt / KST) & 1u);
                 for (uint32_t tt = vseq > static_cast<uint32_t>(VST) ? vseq - VST : 0u; tt < vseq; ++tt)
                     wait_drain(ptx::smem_addr(&sm.full[vst(tt)]), (tt / VST) & 1u);
+                for (uint32_t tt = rseq > static_cast<uint32_t>(RST1) ? rseq - RST1 : 0u; tt < rseq; ++tt)
+                    wait_drain(ptx::smem_addr(&sm.full[rstg(tt)]), (tt / RST1) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -434,7 +517,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         const uint32_t idesc_s = ptx::idesc_bf16_f32(kMqTile, N, 0, 0);
         for (uint32_t i = 0;; ++i) {
             // tile i's K block (or the end-of-work marker) on the K ring
-            uint32_t seq = i * NSUB;
+            uint32_t seq = i * Cfg::NK;
             if (!wait_full(false, seq)) break;
             ptx::tc_fence_after();
             const bool done = sm.kind[kst(seq)] == kMqKindDone;
@@ -447,7 +530,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             if (done) {
                 // release the end-of-work stages; the softmax warps learn there is no tile i
                 bool ok = true;
-                for (int sub = 0; sub < NSUB && ok; ++sub) {
+                for (int sub = 0; sub < Cfg::NK && ok; ++sub) {
                     if (sub > 0) ok = wait_full(false, seq);
                     if (ok && lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.empty[kst(seq)]));
                     ++seq;
@@ -462,19 +545,21 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             const uint32_t s_col = tmem + Cfg::TMEM_S + (i & 1u) * NMAX;
             const uint32_t qbase = ptx::smem_addr(&sm.q[0]);
             bool ok = true;
-            for (int sub = 0; sub < NSUB; ++sub) {
+            for (int sub = 0; sub < Cfg::NK; ++sub) {
                 if (sub > 0) {
                     ok = wait_full(false, seq);
                     if (!ok) break;
                     ptx::tc_fence_after();
                 }
                 const int s = kst(seq);
+                // column block of the stage (K=V: blocks 0 and NSUB/2 are the rotated dims)
+                const int cb = Cfg::KEQV ? sub + 1 + (sub >= NSUB / 2 - 1 ? 1 : 0) : sub;
                 if (lane == 0) {
                     const uint32_t a0 = stage0 + s * kMqStageBytes;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t a = ptx::smem_desc(a0 + kk * 32, 16, 1024, ptx::kSwizzle128B);
-                        const uint64_t bq = ptx::smem_desc(qbase + sub * Cfg::QATOM + kk * 32, 16, 1024,
+                        const uint64_t bq = ptx::smem_desc(qbase + cb * Cfg::QATOM + kk * 32, 16, 1024,
                                                            ptx::kSwizzle128B);
                         ptx::umma_ss(s_col, a, bq, idesc_s, (sub | kk) != 0 ? 1u : 0u);
                     }
@@ -484,6 +569,27 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 ++seq;
             }
             if (!ok) break;
+            if constexpr (Cfg::KEQV) {
+                // rotated dims: A = the keys derived into TMEM (hi, then lo), B = the raw q in
+                // rows [0, G) of column blocks 0 and NSUB/2 (rows [G, 2 G) are zero there)
+                if (!__all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&sm.krot_full), i & 1u,
+                                                          &sm.abort_flag, p.ws_flags)))
+                    break;
+                ptx::tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t a_t = tmem + Cfg::TMEM_KROT + part * 64 + kk * 8;
+                            const uint64_t bq = ptx::smem_desc(
+                                qbase + (kk < 4 ? 0 : NSUB / 2) * Cfg::QATOM + (kk & 3) * 32, 16, 1024,
+                                ptx::kSwizzle128B);
+                            ptx::umma_ts(s_col, a_t, bq, idesc_s, 1u);
+                        }
+                }
+                __syncwarp();
+            }
             if (lane == 0) {
                 if (d.flags & kDescLast) ptx::umma_commit(ptx::smem_addr(&sm.q_empty));
                 ptx::umma_commit(ptx::smem_addr(&sm.s_full[i & 1u]));
@@ -570,7 +676,9 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         // Thread j of lane quarter q (warp % 4) owns TMEM lane j: position j of the
         // tile's scores and head-dim element j of each O^T block.  The two warps of a
         // quarter split the query rows: warps 2..5 rows [0, RH), warps 6..9 [RH, 2 RH).
-        constexpr int RH = NMAX / 2;
+        // rows per warp; over a K=V cache the G query rows' scores are the sum of a hi
+        // column r and a lo column G + r
+        constexpr int RH = Cfg::KEQV ? Cfg::RMAX / 2 : NMAX / 2;
         const int q4 = warp & 3;
         const int r0 = ((warp - 2) >> 2) * RH;      // first row of this warp
         const int j = 32 * q4 + lane;
@@ -588,6 +696,123 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         for (int i = sid; i < 2 * Cfg::PBYTES / 16; i += kMqSoftmaxThreads)
             ptx::sts128(ptx::smem_addr(&sm.pm[0][0]) + i * 16, 0u, 0u, 0u, 0u);
         ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+        // K=V: derives tile ti's rotated keys rope(w * v, t + j) into TMEM (the A operand of
+        // the scores' rotated k-steps) from the R ring; 1 when done, 0 when there is no
+        // tile ti, -1 when the CTA is aborting.  Thread j (two per row, halves h of the
+        // 64 rotated pairs) takes the pairs [32 h, 32 h + 32) of row j.
+        auto derive = [&](uint32_t ti) -> int {
+            if constexpr (Cfg::KEQV) {
+                const uint32_t q0 = 2u * ti;
+                const bool okd =
+                    wait_bounded(ptx::smem_addr(&sm.full[rstg(q0)]), (q0 / RST1) & 1u, &sm.abort_flag,
+                                 p.ws_flags) &&
+                    wait_bounded(ptx::smem_addr(&sm.full[rstg(q0 + 1)]), ((q0 + 1) / RST1) & 1u,
+                                 &sm.abort_flag, p.ws_flags);
+                if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !okd)) return -1;
+                const int rs = rstg(q0) - KST - VST;
+                if (sm.rkind[rs] == kMqKindDoneR) return 0;
+                const int t0 = sm.rdesc[rs].t;
+                // cos, sin of t0 f_i: the angle reaches 2.6e5 rad, so it is reduced mod
+                // 2 pi in fp64 before sincosf; then (t0 + 16 a) f_i by the angle sum
+                if (sid < 64) {
+                    const double ang = static_cast<double>(t0) * sm.rope.freq[sid];
+                    const double turns = rint(ang * 0.15915494309189535);   // 1 / (2 pi)
+                    const double rr = fma(-turns, 6.283185307179586, ang);
+                    float sn, cs;
+                    sincosf(static_cast<float>(rr), &sn, &cs);
+                    sm.rope.base[sid] = make_float2(cs, sn);
+                }
+                ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+                for (int e = sid; e < 8 * 64; e += kMqSoftmaxThreads) {
+                    const int ii = e >> 3, a = e & 7;
+                    const float2 b0 = sm.rope.base[ii], c0 = sm.rope.coarse[ii][a];
+                    sm.rope.tile[ii][a] = make_float2(b0.x * c0.x - b0.y * c0.y, b0.y * c0.x + b0.x * c0.y);
+                }
+                ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+                const int h = (warp - 2) >> 2;
+                const uint32_t sx = stage0 + rstg(q0) * kMqStageBytes;       // dims [0, 64)
+                const uint32_t sy = stage0 + rstg(q0 + 1) * kMqStageBytes;   // dims [D/2, D/2 + 64)
+                const uint32_t rowoff = (j >> 3) * 1024 + (j & 7) * 128;
+                const int ja = j >> 4, jb = j & 15;
+                uint32_t hx[16], hy[16], lx[16], ly[16];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t unit = static_cast<uint32_t>(((4 * h + u) ^ (j & 7)) << 4);
+                    const uint4 vx4 = ptx::lds128(sx + rowoff + unit);
+                    const uint4 vy4 = ptx::lds128(sy + rowoff + unit);
+                    const uint32_t vx[4] = {vx4.x, vx4.y, vx4.z, vx4.w};
+                    const uint32_t vy[4] = {vy4.x, vy4.y, vy4.z, vy4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float k0[2], k1[2];
+#pragma unroll
+                        for (int tt = 0; tt < 2; ++tt) {
+                            const int ii = 32 * h + 8 * u + 2 * e + tt;
+                            const float2 tb = sm.rope.tile[ii][ja], fb = sm.rope.fine[ii][jb];
+                            const float c = tb.x * fb.x - tb.y * fb.y;    // cos((t0 + j) f_i)
+                            const float sn = tb.y * fb.x + tb.x * fb.y;   // sin((t0 + j) f_i)
+                            const float x = sm.rope.w[ii] * (tt ? bf16hi(vx[e]) : bf16lo(vx[e]));
+                            const float y = sm.rope.w[64 + ii] * (tt ? bf16hi(vy[e]) : bf16lo(vy[e]));
+                            k0[tt] = x * c - y * sn;
+                            k1[tt] = y * c + x * sn;
+                        }
+                        const __nv_bfloat162 h0 = __floats2bfloat162_rn(k0[0], k0[1]);
+                        const __nv_bfloat162 h1 = __floats2bfloat162_rn(k1[0], k1[1]);
+                        const __nv_bfloat162 l0 =
+                            __floats2bfloat162_rn(k0[0] - __low2float(h0), k0[1] - __high2float(h0));
+                        const __nv_bfloat162 l1 =
+                            __floats2bfloat162_rn(k1[0] - __low2float(h1), k1[1] - __high2float(h1));
+                        hx[4 * u + e] = *reinterpret_cast<const uint32_t*>(&h0);
+                        hy[4 * u + e] = *reinterpret_cast<const uint32_t*>(&h1);
+                        lx[4 * u + e] = *reinterpret_cast<const uint32_t*>(&l0);
+                        ly[4 * u + e] = *reinterpret_cast<const uint32_t*>(&l1);
+                    }
+                }
+                // columns: dims i (x) at i / 2, dims D/2 + i (y) at 32 + i / 2; lo parts 64 later
+                const uint32_t kb = lane_addr + Cfg::TMEM_KROT + 16 * h;
+                ptx::tmem_st16(kb, hx);
+                ptx::tmem_st16(kb + 32, hy);
+                ptx::tmem_st16(kb + 64, lx);
+                ptx::tmem_st16(kb + 96, ly);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                // every thread is done with the R stages and has stored its keys
+                ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+                if (sid == 0) {
+                    ptx::mbar_arrive(ptx::smem_addr(&sm.empty[rstg(q0)]));
+                    ptx::mbar_arrive(ptx::smem_addr(&sm.empty[rstg(q0 + 1)]));
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.krot_full));
+                return 1;
+            } else {
+                (void)ti;
+                return 0;
+            }
+        };
+        bool derive_more = Cfg::KEQV;   // K=V: tiles still to derive
+        if constexpr (Cfg::KEQV) {
+            // rotation tables: f_i, the weights of the rotated dims, cos and sin of b f_i
+            for (int e = sid; e < 64; e += kMqSoftmaxThreads) sm.rope.freq[e] = p.rope_freq[e];
+            for (int e = sid; e < 128; e += kMqSoftmaxThreads)
+                sm.rope.w[e] = __bfloat162float(p.w_k[(e >> 6) * (D / 2) + (e & 63)]);
+            for (int e = sid; e < 64 * 16; e += kMqSoftmaxThreads) {
+                const int ii = e >> 4, b = e & 15;
+                float sn, cs;
+                sincosf(static_cast<float>(static_cast<double>(b) * p.rope_freq[ii]), &sn, &cs);
+                sm.rope.fine[ii][b] = make_float2(cs, sn);
+            }
+            for (int e = sid; e < 64 * 8; e += kMqSoftmaxThreads) {
+                const int ii = e >> 3, a = e & 7;
+                float sn, cs;   // |16 a f_i| < 128
+                sincosf(static_cast<float>(static_cast<double>(16 * a) * p.rope_freq[ii]), &sn, &cs);
+                sm.rope.coarse[ii][a] = make_float2(cs, sn);
+            }
+            ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+            const int dr = derive(0u);
+            derive_more = dr == 1;
+            if (dr < 0) derive_more = false;
+        }
         // A finished piece whose output is still to be written: its last tile and
         // that tile's index; its reference max, normaliser and bad bits are in smem.
         bool epi_pending = false;
@@ -678,12 +903,27 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             }
             // scores of position j for this warp's rows, log2 units, masked per query
             uint32_t sr[RH];
-            ptx::tmem_ld<RH>(lane_addr + Cfg::TMEM_S + (i & 1u) * NMAX + r0, sr);
-            ptx::tmem_wait_ld();
+            if constexpr (Cfg::KEQV) {
+                uint32_t sa[NMAX];
+                ptx::tmem_ld<NMAX>(lane_addr + Cfg::TMEM_S + (i & 1u) * NMAX, sa);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < RH; ++k)
+                    sr[k] = __float_as_uint(__uint_as_float(sa[r0 + k]) + __uint_as_float(sa[Cfg::RMAX + r0 + k]));
+            } else {
+                ptx::tmem_ld<RH>(lane_addr + Cfg::TMEM_S + (i & 1u) * NMAX + r0, sr);
+                ptx::tmem_wait_ld();
+            }
             // S buffer i % 2 may take the scores of tile i + 2
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.s_empty[i & 1u]));
+            // K=V: the next tile's rotated keys (its scores can run during this softmax)
+            if (derive_more) {
+                const int dr = derive(i + 1);
+                if (dr < 0) break;
+                derive_more = dr == 1;
+            }
             float s[RH];
             bool need = false;
 #pragma unroll

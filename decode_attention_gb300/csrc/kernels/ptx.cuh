@@ -77,6 +77,13 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// L2 policy for data read again soon from L2 (a first read of a tile that is re-read).
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // L2 policy for data read exactly once (the KV stream).
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t pol;
@@ -232,6 +239,17 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M x 16 bf16, K-major) read from TMEM, lane = row,
+// two elements per 32-bit column.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile(
@@ -269,11 +287,19 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                  : "r"(taddr));
 }
 
-// n (8 or 16) consecutive columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+
+// n (4, 8 or 16) consecutive columns of this thread's lane.
 template <int n>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[n]) {
-    static_assert(n == 8 || n == 16, "8 or 16 columns");
-    if constexpr (n == 16) tmem_ld16(taddr, r); else tmem_ld8(taddr, r);
+    static_assert(n == 4 || n == 8 || n == 16, "4, 8 or 16 columns");
+    if constexpr (n == 16) tmem_ld16(taddr, r);
+    else if constexpr (n == 8) tmem_ld8(taddr, r);
+    else tmem_ld4(taddr, r);
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {
@@ -296,10 +322,18 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                  : "memory");
 }
 
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 template <int n>
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[n]) {
-    static_assert(n == 8 || n == 16, "8 or 16 columns");
-    if constexpr (n == 16) tmem_st16(taddr, r); else tmem_st8(taddr, r);
+    static_assert(n == 4 || n == 8 || n == 16, "4, 8 or 16 columns");
+    if constexpr (n == 16) tmem_st16(taddr, r);
+    else if constexpr (n == 8) tmem_st8(taddr, r);
+    else tmem_st4(taddr, r);
 }
 
 __device__ __forceinline__ void tmem_wait_st() {

@@ -37,6 +37,9 @@ cudaError_t launch_global_keqv(const LaunchArgs& a, bool paged);
 // out [B, T, H, D]; at most mq_max_queries(sliding) tokens.
 cudaError_t launch_mq(const LaunchArgs& a, bool sliding, bool paged);
 int mq_max_queries(bool sliding);
+// decodeGQA over a single K=V cache on the tcgen05 kernel (a.k == a.v: the value
+// cache; a.p.keqv_operand: workspace room for the scores' operand).
+cudaError_t launch_keqv_tc(const LaunchArgs& a, bool paged);
 size_t smem_bytes_mq(bool sliding);
 
 // Bytes of dynamic shared memory each geometry's kernel requests.
