@@ -125,10 +125,12 @@ struct PlanSmem {
     int sn[kMaxBatch];               // static head length of each segment of sequence b
     int dn[kMaxBatch];               // long dynamic chunks of each segment of sequence b
     int dn1[kMaxBatch];              // short dynamic chunks of each segment of sequence b
-    long long spref[kMaxBatch + 1];  // KVH * sum_{b' < b} sn_b'
+    long long spref[kMaxBatch + 1];  // KVH * sum_{b' < b} st_b' (static tiles, below)
     int dpref[kMaxBatch + 1];        // KVH * sum_{b' < b} dn_b'
     int dpref1[kMaxBatch + 1];       // KVH * sum_{b' < b} dn1_b'
-    long long n_static;              // Ns
+    long long n_static;              // Ns: static tiles in total
+    int unit;                        // positions per tile: the static head of a segment is
+                                     // st_b = ceil(sn_b / unit) tiles, all whole but the last
     int n_dyn;                       // dynamic chunks in total (long, then short)
     int n_dyn0;                      // long dynamic chunks
     int c_dyn;                       // positions per long dynamic chunk
@@ -150,10 +152,17 @@ __device__ __forceinline__ int upper_seq(const T* pref, int B, long long x) {
     return lo;
 }
 
+// Static tiles of each segment of sequence b.
+__device__ __forceinline__ int static_tiles(const PlanSmem& pl, int b) {
+    return (pl.sn[b] + pl.unit - 1) / pl.unit;
+}
+// First static tile of unit j.  The static heads of all segments, concatenated in
+// (b, kvh) order and counted in tiles, are split evenly over the units: a unit
+// boundary never falls inside a tile, so no tile is read by two CTAs.
 __device__ __forceinline__ long long static_unit_begin(const PlanSmem& pl, int j) {
     return static_cast<long long>(j) * pl.n_static / pl.g_eff;
 }
-// static unit containing static index x (units are floor(j Ns / Ge))
+// static unit containing static tile x (units are floor(j Ns / Ge))
 __device__ __forceinline__ int static_unit_of(const PlanSmem& pl, long long x) {
     return static_cast<int>(((x + 1) * pl.g_eff - 1) / pl.n_static);
 }
@@ -164,9 +173,10 @@ struct SegmentParts {
     int first_s, ns_parts, dk0, nd_parts, dyn_base;
     __device__ __forceinline__ SegmentParts(const PlanSmem& pl, int b, int kvh, int dyn_slot_base)
         : dyn_base(dyn_slot_base) {
-        const long long ss = pl.spref[b] + static_cast<long long>(kvh) * pl.sn[b];
+        const int st = static_tiles(pl, b);
+        const long long ss = pl.spref[b] + static_cast<long long>(kvh) * st;
         first_s = static_unit_of(pl, ss);
-        ns_parts = static_unit_of(pl, ss + pl.sn[b] - 1) - first_s + 1;
+        ns_parts = static_unit_of(pl, ss + st - 1) - first_s + 1;
         // the dynamic slots of a segment are contiguous: its long chunks, then its
         // short ones (whatever order they are claimed in)
         nd_parts = pl.dn[b] + pl.dn1[b];
@@ -425,7 +435,7 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
         sloc[j] = srun;
         dloc[j] = drun;
         d1loc[j] = d1run;
-        srun += static_cast<uint32_t>(sn) * static_cast<uint32_t>(KVH);
+        srun += static_cast<uint32_t>((sn + unit - 1) / unit) * static_cast<uint32_t>(KVH);
         drun += d * KVH;
         d1run += d1 * KVH;
     }
@@ -460,6 +470,7 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
             pl.dpref1[kMaxBatch] = d1incl;
         }
         pl.n_static = static_cast<long long>(sincl);
+        pl.unit = unit;
         pl.n_dyn0 = dincl;
         pl.n_dyn = dincl + d1incl;
         pl.c_dyn = c;
@@ -645,18 +656,18 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
         };
 
         // ---- the static unit of this CTA: pieces of consecutive static heads ----
-        long long pos = static_unit_begin(pl, cta);
+        long long x = static_unit_begin(pl, cta);
         const long long stop = static_unit_begin(pl, cta + 1);
-        while (ok && pos < stop) {
-            const int b = upper_seq(pl.spref, B, pos);
-            const int sn = pl.sn[b];
-            const long long rel = pos - pl.spref[b];
-            const int kvh = static_cast<int>(rel / sn);
-            const int off = static_cast<int>(rel - static_cast<long long>(kvh) * sn);
-            const int take = static_cast<int>(stop - pos < sn - off ? stop - pos : sn - off);
-            pos += take;
-            const int p0 = pl.lo[b] + off;
-            ok = emit_piece(b, kvh, p0, p0 + take, cta + b * KVH + kvh, pos >= stop);
+        while (ok && x < stop) {
+            const int b = upper_seq(pl.spref, B, x);
+            const int st = static_tiles(pl, b);
+            const long long rel = x - pl.spref[b];
+            const int kvh = static_cast<int>(rel / st);
+            const int k0 = static_cast<int>(rel - static_cast<long long>(kvh) * st);
+            const int take = static_cast<int>(stop - x < st - k0 ? stop - x : st - k0);
+            x += take;
+            const int e = k0 + take == st ? pl.sn[b] : (k0 + take) * TP;
+            ok = emit_piece(b, kvh, pl.lo[b] + k0 * TP, pl.lo[b] + e, cta + b * KVH + kvh, x >= stop);
         }
         // ---- dynamic chunks ----
         while (ok && dynamic) {

@@ -451,18 +451,19 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             };
 
             // the static unit of this CTA, then dynamic chunks (as in the single-query kernel)
-            long long pos = static_unit_begin(pl, cta);
+            long long x = static_unit_begin(pl, cta);
             const long long stop = static_unit_begin(pl, cta + 1);
-            while (ok && pos < stop) {
-                const int b = upper_seq(pl.spref, B, pos);
-                const int sn = pl.sn[b];
-                const long long rel = pos - pl.spref[b];
-                const int kvh = static_cast<int>(rel / sn);
-                const int off = static_cast<int>(rel - static_cast<long long>(kvh) * sn);
-                const int take = static_cast<int>(stop - pos < sn - off ? stop - pos : sn - off);
-                pos += take;
-                const int p0 = pl.lo[b] + off;
-                ok = emit_piece(b, kvh, p0, p0 + take, cta + b * KVH + kvh, pos >= stop);
+            while (ok && x < stop) {
+                const int b = upper_seq(pl.spref, B, x);
+                const int st = static_tiles(pl, b);
+                const long long rel = x - pl.spref[b];
+                const int kvh = static_cast<int>(rel / st);
+                const int k0 = static_cast<int>(rel - static_cast<long long>(kvh) * st);
+                const int take = static_cast<int>(stop - x < st - k0 ? stop - x : st - k0);
+                x += take;
+                const int e = k0 + take == st ? pl.sn[b] : (k0 + take) * kMqTile;
+                ok = emit_piece(b, kvh, pl.lo[b] + k0 * kMqTile, pl.lo[b] + e, cta + b * KVH + kvh,
+                                x >= stop);
             }
             while (ok && dynamic) {
                 if (claimed < 0) claimed = static_cast<int>(atomicAdd(p.ws_claim, 1u));
