@@ -15,6 +15,7 @@ from ._native import (  # noqa: F401
     GQA_DEVICE_WAIT_TIMEOUT,
     GQA_MAX_QUERIES_GLOBAL,
     GQA_MAX_QUERIES_SLIDING,
+    GQA_MAX_SEQ,
     GQA_ERR_CUDA,
     GQA_ERR_INVALID_ARGUMENT,
     GQA_ERR_UNSUPPORTED,

@@ -30,6 +30,7 @@ GQA_DEVICE_BAD_PAGE = 2
 GQA_DEVICE_BAD_LENGTH = 4
 
 PAGE_SIZE = 16
+GQA_MAX_SEQ = 262144   # longest cache (positions) a call accepts
 
 EXPORTED_SYMBOLS = ("gqa_workspace_size", "gqa_workspace_init", "gqa_decode", "gqa_decode_paged",
                     "gqa_device_status", "gqa_decode_noalloc", "gqa_decode_ring",

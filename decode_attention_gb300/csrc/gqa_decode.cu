@@ -33,6 +33,10 @@ int heads_per_kv(Geometry g) { return g == Geometry::kSliding ? 2 : 8; }
 
 // RoPE base of the global layers (Model Spec, `attn.rope` row for layers 5, 11, ..., 59).
 constexpr double kGlobalRopeTheta = 1.0e6;
+// K=V calls whose cache holds at least this many 128-position tiles per CTA take the
+// tcgen05 kernel (measured: ~13 tiles per CTA ran 40% faster on the mma.sync kernel,
+// ~430 tiles per CTA 16% faster on the tcgen05 kernel)
+constexpr int kKeqvTcTilesPerCta = 64;
 
 // ---- workspace layout --------------------------------------------------------
 // [0, 4)              status word (uint32)
@@ -219,7 +223,14 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
         for (int i = 0; i < 64; ++i)
             a.p.rope_freq[i] = std::pow(kGlobalRopeTheta, -2.0 * i / static_cast<double>(c.D));
         a.p.keqv_operand = reinterpret_cast<__nv_bfloat16*>(w + lay.operand_off);
-        return gqa::launch_keqv_tc(a, paged) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+        // Long histories run on the tcgen05 kernel (derived keys in TMEM).  Short ones
+        // are latency-bound: its pipeline fill and per-piece steps cost more than they
+        // save there, and the mma.sync streaming kernel finishes first.  The host knows
+        // only the cache capacity, so the split is on capacity tiles per CTA.
+        const long long cap_tiles = static_cast<long long>(c.B) * capacity * c.KVH / 128;
+        const bool long_history = cap_tiles >= static_cast<long long>(kKeqvTcTilesPerCta) * grid;
+        const cudaError_t e = long_history ? gqa::launch_keqv_tc(a, paged) : gqa::launch_global_keqv(a, paged);
+        return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
     }
     if (multi_query)
         return gqa::launch_mq(a, c.geo == Geometry::kSliding, paged) == cudaSuccess ? GQA_OK

@@ -35,6 +35,17 @@ def test_header_declares_the_exported_api():
     assert declared_functions() == sorted(_native.EXPORTED_SYMBOLS)
 
 
+def test_binding_constants_match_the_header():
+    defines = dict(re.findall(r"#define (GQA_[A-Z_]+) (\d+)u?\b", open(HEADER).read()))
+    for name, value in [("GQA_MAX_SEQ", gqa.GQA_MAX_SEQ), ("GQA_PAGE_SIZE", gqa.PAGE_SIZE),
+                        ("GQA_MAX_QUERIES_SLIDING", gqa.GQA_MAX_QUERIES_SLIDING),
+                        ("GQA_MAX_QUERIES_GLOBAL", gqa.GQA_MAX_QUERIES_GLOBAL),
+                        ("GQA_DEVICE_WAIT_TIMEOUT", gqa.GQA_DEVICE_WAIT_TIMEOUT),
+                        ("GQA_DEVICE_BAD_PAGE", gqa.GQA_DEVICE_BAD_PAGE),
+                        ("GQA_DEVICE_BAD_LENGTH", gqa.GQA_DEVICE_BAD_LENGTH)]:
+        assert int(defines[name]) == value, name
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name

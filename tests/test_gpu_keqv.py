@@ -5,6 +5,12 @@ Covers ragged lengths that span many 32-position tiles and several CTAs per
 segment, a sequence reaching position 131074 (where the rotation angle of the
 fastest pair is ~1.3e5 rad, so the kernel's fp64 angle reduction matters), the
 paged form, NaN in every cache row past the sequence end, and the bf16 output.
+
+The library runs a K=V call on one of two kernels, chosen by the cache capacity
+(tiles of 128 positions per CTA): the mma.sync streaming kernel for small caches,
+the tcgen05 kernel for large ones.  Every test runs twice with the same lengths: in
+a cache sized to them ("tight") and in one large enough for the tcgen05 kernel
+("roomy").
 """
 import numpy as np
 import pytest
@@ -22,6 +28,22 @@ if not torch.cuda.is_available():
 
 H, KVH, D = GLOBAL["H"], GLOBAL["KVH"], GLOBAL["D"]
 
+# the capacity (in 128-position tiles per CTA, one CTA per SM) from which the
+# library takes the tcgen05 kernel
+_TC_TILES_PER_CTA = 64
+
+
+def capacity(B, S, roomy):
+    """S, or a roomy capacity: 1.5x the tcgen05 threshold, within the longest cache
+    the library accepts."""
+    if not roomy:
+        return S
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    need = -(-_TC_TILES_PER_CTA * sms * 128 // (B * KVH))
+    cap = min(max(S, need * 3 // 2), gqa.GQA_MAX_SEQ)
+    assert cap >= need, "the roomy cache must take the tcgen05 kernel"
+    return cap
+
 
 def case(lens, S, seed):
     c = inputs.contiguous_case(len(lens), S, H, KVH, D, lens, seed, device="cuda")
@@ -30,7 +52,9 @@ def case(lens, S, seed):
 
 
 def oracle_keqv(c, lens):
-    return oracle.gqa_decode_keqv_f64(inputs.bf16_bits(c["q"]), inputs.bf16_bits(c["v"]),
+    # the oracle reads rows below each length only: pass the rows up to the longest
+    v = c["v"][:, :max(1, max(lens))].contiguous()
+    return oracle.gqa_decode_keqv_f64(inputs.bf16_bits(c["q"]), inputs.bf16_bits(v),
                                       inputs.bf16_bits(c["w_k"]), np.asarray(lens), 0)
 
 
@@ -43,26 +67,34 @@ def check(out, ref, lens, what):
     assert gqa.gqa_device_status() == 0
 
 
-def test_keqv_contiguous_ragged():
+ROOMY = pytest.mark.parametrize("roomy", [False, True], ids=["tight", "roomy"])
+
+
+@ROOMY
+def test_keqv_contiguous_ragged(roomy):
     lens = [0, 1, 17, 31, 32, 33, 1023, 2500, 3000]
-    c = case(lens, 3000, seed=400)
+    c = case(lens, capacity(len(lens), 3000, roomy), seed=400)
     out = gqa.gqa_decode_keqv(c["q"], c["v"], c["w_k"], c["seq_lens"], out_dtype=torch.float32)
     torch.cuda.synchronize()
     check(out, oracle_keqv(c, lens), lens, "keqv contiguous")
 
 
-def test_keqv_long_positions():
-    """One sequence of 131075 positions: keys at rotation angles up to ~1.3e5 rad."""
-    lens = [131075]
-    c = case(lens, 131080, seed=401)
+@ROOMY
+def test_keqv_long_positions(roomy):
+    """A sequence of 131075 positions: keys at rotation angles up to ~1.3e5 rad.  (One
+    sequence alone never fills enough tiles per CTA for the tcgen05 kernel: the roomy
+    form adds a short second one.)"""
+    lens = [131075, 3] if roomy else [131075]
+    c = case(lens, capacity(len(lens), 131080, roomy), seed=401)
     out = gqa.gqa_decode_keqv(c["q"], c["v"], c["w_k"], c["seq_lens"], out_dtype=torch.float32)
     torch.cuda.synchronize()
     check(out, oracle_keqv(c, lens), lens, "keqv long")
 
 
-def test_keqv_rows_past_the_end_are_never_read():
+@ROOMY
+def test_keqv_rows_past_the_end_are_never_read(roomy):
     lens = [5, 700, 1601]
-    c = case(lens, 1700, seed=402)
+    c = case(lens, capacity(len(lens), 1700, roomy), seed=402)
     nan = torch.tensor(BF16_NAN, dtype=torch.int16).view(torch.bfloat16).item()
     for b, L in enumerate(lens):
         c["v"][b, L:] = nan
@@ -71,11 +103,14 @@ def test_keqv_rows_past_the_end_are_never_read():
     check(out, oracle_keqv(c, lens), lens, "keqv poisoned")
 
 
-def test_keqv_paged():
+@ROOMY
+def test_keqv_paged(roomy):
     lens = [1, 16, 17, 900, 2049]
     S = max(lens)
     c = case(lens, S, seed=403)
-    bt, P = inputs.page_table(lens, 403, max_pages=(S + 15) // 16, spare_pages=5)
+    # the capacity of a paged call is max_pages * 16 positions
+    bt, P = inputs.page_table(lens, 403, max_pages=(capacity(len(lens), S, roomy) + 15) // 16,
+                              spare_pages=5)
     pool = torch.full((P, 16, KVH, D), float("nan"), dtype=torch.bfloat16, device="cuda")
     for b, L in enumerate(lens):
         for j in range((L + 15) // 16):
@@ -87,9 +122,10 @@ def test_keqv_paged():
     check(out, oracle_keqv(c, lens), lens, "keqv paged")
 
 
-def test_keqv_bf16_output_is_the_rounded_fp32_output():
+@ROOMY
+def test_keqv_bf16_output_is_the_rounded_fp32_output(roomy):
     lens = [40, 1500]
-    c = case(lens, 1500, seed=404)
+    c = case(lens, capacity(len(lens), 1500, roomy), seed=404)
     out32 = gqa.gqa_decode_keqv(c["q"], c["v"], c["w_k"], c["seq_lens"], out_dtype=torch.float32)
     out16 = gqa.gqa_decode_keqv(c["q"], c["v"], c["w_k"], c["seq_lens"], out_dtype=torch.bfloat16)
     torch.cuda.synchronize()

@@ -19,7 +19,8 @@ import decode_attention_gb300 as gqa  # noqa: E402
 
 WORKLOADS = ["sliding_b1_s2048", "global_b8_s8192", "sliding_b64_s32768",
              "global_b16_s131072", "paged_mixed_b256", "retrofit_block_b64",
-             "global_keqv_b16_s131072", "global_mq4_b16_s131072", "sliding_mq8_b64_s32768",
+             "global_keqv_b16_s131072", "global_keqv_b8_s8192", "global_mq4_b16_s131072",
+             "sliding_mq8_b64_s32768",
              "global_mq4_b8_s8192"]
 
 
