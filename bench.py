@@ -43,12 +43,25 @@ from decode_attention_gb300 import inputs  # noqa: E402
 DEFAULT_WORKLOAD = "global_b8_s8192"
 HBM_FALLBACK_GBS = 6800.0
 PROFILES = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = [
-    "decode_attention_gb300/csrc/kernels/decode_kernel.cuh",
-    "decode_attention_gb300/csrc/kernels/policy_sliding_core.cuh",
-    "decode_attention_gb300/csrc/kernels/policy_mma.cuh",
-    "decode_attention_gb300/csrc/kernels/ptx.cuh",
-]
+# the sources each main kernel is compiled from: a recorded DRAM traffic figure holds
+# only while they hash to the value stored beside it
+KERNEL_SOURCES = {
+    "gqa_decode_kernel": [
+        "decode_attention_gb300/csrc/kernels/decode_kernel.cuh",
+        "decode_attention_gb300/csrc/kernels/policy_sliding_core.cuh",
+        "decode_attention_gb300/csrc/kernels/policy_mma.cuh",
+        "decode_attention_gb300/csrc/kernels/policy_mma_keqv.cuh",
+        "decode_attention_gb300/csrc/kernels/ptx.cuh",
+    ],
+    "gqa_mq_kernel": [
+        "decode_attention_gb300/csrc/kernels/decode_mq_kernel.cuh",
+        "decode_attention_gb300/csrc/kernels/decode_kernel.cuh",
+        "decode_attention_gb300/csrc/kernels/ptx.cuh",
+    ],
+}
+# K=V calls whose cache holds at least this many 128-position tiles per CTA (one CTA
+# per SM) run on the tcgen05 kernel (gqa_mq_kernel), smaller ones on gqa_decode_kernel
+KEQV_TC_TILES_PER_CTA = 64
 
 
 # ---------------------------------------------------------------------------
@@ -283,15 +296,28 @@ def hbm_peak():
         return HBM_FALLBACK_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, layer: str):
+def main_kernel(call) -> str:
+    """The kernel a call's positions stream through."""
+    if call.queries:
+        return "gqa_mq_kernel"
+    if call.keqv:
+        cap = call.case["v"].shape[1]   # K=V calls here are contiguous
+        B = len(call.seq_lens)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        if B * cap * call.geo["KVH"] // 128 >= KEQV_TC_TILES_PER_CTA * sms:
+            return "gqa_mq_kernel"
+    return "gqa_decode_kernel"
+
+
+def recorded_traffic(workload: str, layer: str, kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
     path = os.path.join(PROFILES, "traffic.json")
     try:
@@ -300,7 +326,8 @@ def recorded_traffic(workload: str, layer: str):
     except Exception:
         return None
     entry = rec.get(workload, {}).get(layer)
-    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+    if not entry or entry.get("kernel") != kernel or \
+            entry.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -569,11 +596,11 @@ def run_ours(args, wl):
     dom_ms = statistics.mean(dom.times_ms)
     achieved = dom.bytes / (dom_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
-    kernel = "gqa_mq_kernel" if dom.queries else "gqa_decode_kernel"
+    kernel = main_kernel(dom)
     roofline = {"bound": "hbm", "kernel": f"{kernel}<{dom.name}>",
                 "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": recorded_traffic(wl.name, dom.layer),
+                "traffic": recorded_traffic(wl.name, dom.layer, kernel),
                 "algorithmic_bytes_per_launch": dom.bytes}
 
     us_per_layer = {c.name: round(statistics.median(c.times_ms) * 1e3, 2) for c in calls}

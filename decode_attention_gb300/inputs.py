@@ -156,6 +156,11 @@ WORKLOADS = {
         Workload("global_keqv_b16_s131072", "decodeGQA long context over a single K=V cache, "
                  "B=16, seq_lens uniform on [65536, 131072]", B=16, S=131072, seed=7,
                  lengths=lengths_uniform(65536, 131072, 16), layers=("global",), keqv=True),
+        # mid-size: a cache large enough for the tcgen05 K=V kernel, small enough for a
+        # full profiler capture
+        Workload("global_keqv_b16_s24576", "decodeGQA over a single K=V cache, B=16, seq_lens "
+                 "uniform on [12288, 24576]", B=16, S=24576, seed=13,
+                 lengths=lengths_uniform(12288, 24576, 16), layers=("global",), keqv=True),
         Workload("global_keqv_b8_s8192", "decodeGQA over a single K=V cache, B=8, seq_lens "
                  "uniform on [1, 8192]", B=8, S=8192, seed=8, lengths=lengths_uniform(1, 8192, 8),
                  layers=("global",), keqv=True),
