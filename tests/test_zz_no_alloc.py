@@ -99,3 +99,25 @@ def test_decode_global_with_fewer_dynamic_slots():
         gqa.gqa_decode_noalloc(case["q"], case["k"], case["v"], case["seq_lens"], 0, out)
         torch.cuda.synchronize()
         close(out, ref)
+
+
+@pytest.mark.gpu
+@needs_gpu
+def test_larger_call_after_a_smaller_one():
+    # The scratch layout depends on the call's shape.  A small call leaves split-softmax
+    # partials in the scratch; a larger call after it must still start from clean
+    # per-segment arrival counters (they sit where no call's partials ever go).
+    geo = inputs.geometry("global")
+    small = [3000, 4097, 5000]
+    c1 = inputs.contiguous_case(len(small), max(small), geo["H"], geo["KVH"], geo["D"], small,
+                                seed=79, device="cuda")
+    out1 = torch.empty(len(small), geo["H"], geo["D"], dtype=torch.float32, device="cuda")
+    gqa.gqa_decode_noalloc(c1["q"], c1["k"], c1["v"], c1["seq_lens"], 0, out1)
+    B, S = 48, 4096
+    lens = np.random.default_rng(6).integers(1, S + 1, B).tolist()
+    c2 = inputs.contiguous_case(B, S, geo["H"], geo["KVH"], geo["D"], lens, seed=80, device="cuda")
+    ref = gqa.gqa_decode(c2["q"], c2["k"], c2["v"], c2["seq_lens"], 0, out_dtype=torch.float32)
+    out = torch.full_like(ref, float("nan"))
+    gqa.gqa_decode_noalloc(c2["q"], c2["k"], c2["v"], c2["seq_lens"], 0, out)
+    torch.cuda.synchronize()
+    close(out, ref)
