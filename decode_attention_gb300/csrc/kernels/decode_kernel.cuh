@@ -61,7 +61,8 @@ constexpr int kDynTailPerCta = 2;     // short chunks (claimed last) per CTA
 constexpr int kDynTailRatio = 4;      // long / short chunk length
 constexpr int kDynFraction = 7;       // about 1/7 of the work is dynamic: covers the spread
                                       // of per-SM memory throughput (~13% between SMs)
-constexpr int kDynMinChunk = 128;     // positions: keeps the per-piece epilogue small
+constexpr int kDynMinChunk = 256;     // positions: fewer pieces to merge per segment (global
+                                      // B=8, S=8192: 1.5% faster than 128; 512 is 5% slower)
 constexpr int kDynMinShare = 256;     // positions per CTA below which all work is static
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // a wait gives up after 2 s
