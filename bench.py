@@ -306,7 +306,7 @@ def kernel_source_hash(kernel: str) -> str:
 
 def main_kernel(call) -> str:
     """The kernel a call's positions stream through."""
-    if call.queries:
+    if call.queries > 1:
         return "gqa_mq_kernel"
     if call.keqv:
         cap = call.case["v"].shape[1]   # K=V calls here are contiguous

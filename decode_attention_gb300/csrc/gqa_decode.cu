@@ -232,7 +232,9 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
         const cudaError_t e = long_history ? gqa::launch_keqv_tc(a, paged) : gqa::launch_global_keqv(a, paged);
         return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
     }
-    if (multi_query)
+    // One new token per sequence is a single-token decode: the mma.sync kernel streams
+    // it faster than the tcgen05 multi-query kernel (N = 16 mma for g <= 8 rows).
+    if (multi_query && c.T > 1)
         return gqa::launch_mq(a, c.geo == Geometry::kSliding, paged) == cudaSuccess ? GQA_OK
                                                                                    : GQA_ERR_CUDA;
     const cudaError_t e = c.geo == Geometry::kSliding ? gqa::launch_sliding(a, paged)

@@ -326,8 +326,9 @@ gqa_status_t gqa_prepare_decode_paged(const void *q_raw, const void *k_raw, cons
  * queries whose attended range covers that page.  Rows outside a sequence's
  * attended range are never used; a non-finite value inside it may reach every
  * query of that sequence (the P.V product multiplies it by a zero weight).
- * Runs on the tcgen05 tensor cores: scores and P.V as 128-position mma with
- * TMEM accumulators.
+ * T >= 2 runs on the tcgen05 tensor cores: scores and P.V as 128-position mma
+ * with TMEM accumulators.  T = 1 is a single-token decode and runs on gqa_decode's
+ * kernel.
  */
 #define GQA_MAX_QUERIES_SLIDING 8
 #define GQA_MAX_QUERIES_GLOBAL 4
