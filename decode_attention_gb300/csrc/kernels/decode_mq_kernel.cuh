@@ -19,7 +19,7 @@
 // elements (16 KB, 128-byte swizzled, exactly what TMA writes); the P.V mma of a
 // 128-wide head-dim block reads two adjacent stages.
 //
-// Warp roles (352 threads).  Warp 0, lane 0: the producer.  It walks the same
+// Warp roles (352 threads; 384 over a K=V cache).  Warp 0, lane 0: the producer.  It walks the same
 // schedule as the single-query kernel (static units, then claimed dynamic chunks)
 // and streams the tiles in the order K(0), K(1), V(0), K(2), V(1), ...: the scores
 // of tile i+1 are computed while the softmax of tile i runs.  K blocks go to one
@@ -35,7 +35,9 @@
 // Warps 2..9: thread j of lane quarter warp % 4 owns TMEM lane j, i.e. position j
 // of the tile's scores and head-dim element j of each O^T block; they run the
 // softmax and the epilogue, the two warps of a quarter splitting the query rows
-// (two warps per scheduler hide each other's latencies).
+// (two warps per scheduler hide each other's latencies).  Over a K=V cache, warp 11
+// (lane 0) streams the V blocks from tile descriptors the producer hands it, and the
+// softmax warps also derive the next tile's rotated keys into TMEM.
 //
 // Pieces alternate between two O^T buffers in TMEM: a piece's output is written
 // after the next tile's P has been published, so the softmax warps never wait
@@ -70,6 +72,8 @@ constexpr int kMqPSbo = (kMqTile / 8) * kMqPLbo;   // P 8-row groups: 2304 B
 constexpr int kMqThreads = 352;         // producer, scores, 8 softmax warps, P.V
 constexpr int kMqSoftmaxThreads = 256;
 constexpr int kMqPvWarp = 10;
+constexpr int kMqVWarp = 11;            // K=V: the V producer (a 12th warp)
+constexpr int kMqVq = 8;                // tile descriptors in flight to the V producer
 
 constexpr int tmem_cols_for(int cols) {
     int c = 32;
@@ -101,9 +105,17 @@ struct MqCfg {
     // 128 rows x 128 bf16 (rotated dims i and D/2 + i, i < 64), hi then lo
     static constexpr int TMEM_KROT = TMEM_O + OBUFS * OBUF;
     static constexpr int KROT_COLS = KEQV ? 128 : 0;
+    // K=V: cos and sin of j f_i for tile row j (the TMEM lane) and rotated pair i, fp32:
+    // pair 32 h + k of the thread half h at columns 64 h + 2 k (cos) and 64 h + 2 k + 1
+    static constexpr int TMEM_TRIG = TMEM_KROT + KROT_COLS;
+    static constexpr int TRIG_COLS = KEQV ? 128 : 0;
     static constexpr int NK = KEQV ? NSUB - 2 : NSUB;   // stages of a K block
-    static constexpr int TMEM_COLS = tmem_cols_for(TMEM_KROT + KROT_COLS);
-    static_assert(TMEM_KROT + KROT_COLS <= 512, "TMEM holds 512 columns");
+    // Over a K=V cache a second producer warp streams the V blocks, so that waits on the
+    // V ring (paced by the P.V warp) never hold up the K and R rings.
+    static constexpr bool SPLIT_V = KEQV;
+    static constexpr int THREADS = SPLIT_V ? kMqThreads + 32 : kMqThreads;
+    static constexpr int TMEM_COLS = tmem_cols_for(TMEM_TRIG + TRIG_COLS);
+    static_assert(TMEM_TRIG + TRIG_COLS <= 512, "TMEM holds 512 columns");
     static_assert(OBUFS == 1 || OBUFS == 2, "one or two O^T buffers");
     static_assert(!KEQV || (D == 512 && G == 8 && MAXT == 1 && RST == 2), "K=V: decodeGQA, one query");
     static_assert(VST % 2 == 0, "a P.V block reads two adjacent stages");
@@ -116,17 +128,13 @@ struct MqCfg {
 using MqGlobal = MqCfg<512, 8, 4, 4, 4, 1>;     // decodeGQA, T <= 4
 using MqGlobal2 = MqCfg<512, 8, 2, 4, 6, 2>;   // decodeGQA, T <= 2: smaller Q and P, more stages
 using MqSliding = MqCfg<256, 2, 8, 4, 6, 2>;   // slidingDecodeGQA, T <= 8
-using MqKeqV = MqCfg<512, 8, 1, 4, 4, 2, true, 2>;   // decodeGQA over a single K=V cache
+using MqKeqV = MqCfg<512, 8, 1, 4, 4, 1, true, 2>;   // decodeGQA over a single K=V cache (one
+                                                     // O^T buffer: TMEM holds the rotation factors)
 
-// Rotation tables of the K=V key derivation (rotated pair i < 64, angle of position
-// t + j for tile row j = 16 a + b): cos and sin of 16 a f_i and of b f_i, once per CTA;
-// per tile, cos and sin of t f_i and of (t + 16 a) f_i.  Indexed pair-major, so the
-// lanes of a warp (consecutive rows) read consecutive words.
+// Rotation data of the K=V key derivation in shared memory (the per-row factors cos and
+// sin of j f_i live in TMEM): per tile, cos and sin of t f_i for the tile's first position t.
 struct MqRopeTables {
-    float2 coarse[64][8];
-    float2 fine[64][16];
     float2 base[64];
-    float2 tile[64][8];
     float w[128];        // k_norm weight of the rotated dims: w[i], then w[D/2 + i]
     double freq[64];     // f_i = theta^(-2i/D)
 };
@@ -163,6 +171,10 @@ struct alignas(1024) MqSmem {
     int rkind[Cfg::KEQV ? Cfg::RST : 1];       // R ring: an R block or the end-of-work marker
     MqTile rdesc[Cfg::KEQV ? Cfg::RST : 1];    // tile of an R block (its first stage)
     alignas(8) uint64_t krot_full;             // K=V: the derived keys of the next tile are in TMEM
+    // K=V: tiles whose V blocks the V producer issues, in order (FIFO from the producer)
+    MqTile vq[Cfg::SPLIT_V ? kMqVq : 1];
+    alignas(8) uint64_t vq_full[Cfg::SPLIT_V ? kMqVq : 1];
+    alignas(8) uint64_t vq_empty[Cfg::SPLIT_V ? kMqVq : 1];
     alignas(16) std::conditional_t<Cfg::KEQV, MqRopeTables, MqNoTables> rope;
     MqTile s_desc[2];                 // tile whose scores are in S buffer j
     MqTile p_desc[2];                 // tile whose P is in P buffer j
@@ -184,7 +196,7 @@ __device__ __forceinline__ uint32_t mq_p_off(int r, int j) {
 }
 
 template <class Cfg, bool kPaged>
-__global__ void __launch_bounds__(kMqThreads, 1)
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
     gqa_mq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
     constexpr int D = Cfg::D, G = Cfg::G, NSUB = Cfg::NSUB, NB = Cfg::NB, STAGES = Cfg::STAGES;
@@ -220,6 +232,10 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             ptx::mbar_init(ptx::smem_addr(&sm.drain[j]), 1);
         }
         ptx::mbar_init(ptx::smem_addr(&sm.krot_full), 8);   // one arrival per softmax warp
+        for (int k = 0; k < (Cfg::SPLIT_V ? kMqVq : 0); ++k) {
+            ptx::mbar_init(ptx::smem_addr(&sm.vq_full[k]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sm.vq_empty[k]), 1);
+        }
         sm.pv_stop = 0x7fffffff;
         ptx::fence_mbar_init();
         sm.abort_flag = 0;
@@ -285,6 +301,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             const uint32_t q_bytes = static_cast<uint32_t>(NSUB * (Cfg::KEQV ? 2 * R : R) * 128);
             constexpr uint32_t kPageBytes = kPageRows * 128;
             uint32_t kseq = 0, vseq = 0, rseq = 0;   // stages issued on the K, V and R rings
+            uint32_t vpush = 0;                      // K=V: tiles handed to the V producer
             const uint64_t policy_keep = ptx::policy_evict_normal();
             uint32_t n_piece = 0;    // pieces started (O^T buffer n_piece & 1)
             bool ok = true;
@@ -401,19 +418,27 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 }
                 return true;
             };
-            // Tiles arrive in order.  Multi-query: K(i), then V(i - 1).  K=V: K(i - 1), then
-            // R(i) one tile ahead (the softmax warps derive tile i's rotated keys while
-            // tile i - 1's scores are read), then V(i - 2).  K goes first: R(i) waits for
-            // the derivation of tile i - 1 to free the R ring, and K(i - 1) must not.
+            // K=V: hands tile d (or, flagged kDescDone, the end of work) to the V producer.
+            auto push_v = [&](const MqTile& d) -> bool {
+                const uint32_t k = vpush % kMqVq;
+                if (!wait_servicing(ptx::smem_addr(&sm.vq_empty[k]), ((vpush / kMqVq) & 1u) ^ 1u))
+                    return false;
+                sm.vq[k] = d;
+                ptx::mbar_arrive(ptx::smem_addr(&sm.vq_full[k]));   // releases the descriptor
+                ++vpush;
+                return true;
+            };
+            // Tiles arrive in order.  Multi-query: K(i), then V(i - 1).  K=V: K(i - 1) and
+            // tile i - 1 to the V producer, then R(i) one tile ahead (the softmax warps
+            // derive tile i's rotated keys while tile i - 1's scores are read).  K goes
+            // first: R(i) waits for the derivation of tile i - 1 to free the R ring, and
+            // K(i - 1) must not.
             MqTile cur;
             bool have_cur = false;
             auto emit_tile = [&](MqTile nxt) -> bool {
                 if constexpr (Cfg::KEQV) {
-                    if (have_cur && !emit_block(cur, kMqKindK)) return false;
+                    if (have_cur && !(emit_block(cur, kMqKindK) && push_v(cur))) return false;
                     if (!emit_block(nxt, kMqKindR)) return false;
-                    if (have_prev && !emit_block(prev, kMqKindV)) return false;
-                    prev = cur;
-                    have_prev = have_cur;
                     cur = nxt;
                     have_cur = true;
                 } else {
@@ -493,11 +518,10 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 none.slot = none.ob = 0;
                 none.flags = kDescDone;
                 if constexpr (Cfg::KEQV) {
-                    if (have_cur) ok = emit_block(cur, kMqKindK);
+                    if (have_cur) ok = emit_block(cur, kMqKindK) && push_v(cur);
                     if (ok) ok = emit_block(none, kMqKindDoneR);
-                    if (ok && have_prev) ok = emit_block(prev, kMqKindV);
                     if (ok) ok = emit_block(none, kMqKindDone);
-                    if (ok && have_cur) ok = emit_block(cur, kMqKindV);
+                    if (ok) ok = push_v(none);
                 } else {
                     ok = emit_block(none, kMqKindDone);
                     if (ok && have_prev) ok = emit_block(prev, kMqKindV);
@@ -672,6 +696,55 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             wait_drain(ptx::smem_addr(&sm.drain[1]), 0u);
         }
         __syncwarp();
+    } else if (Cfg::SPLIT_V && warp == kMqVWarp) {
+        // ========== K=V: V producer, tile i's V blocks in tile order (lane 0) ==========
+        // The tiles come from the producer through the descriptor FIFO.
+        if (lane == 0) {
+            const uint64_t policy = ptx::policy_evict_first();
+            constexpr uint32_t kPageBytes = kPageRows * 128;
+            uint32_t vseq = 0;   // stages issued on the V ring
+            bool ok = true;
+            for (uint32_t n = 0; ok; ++n) {
+                const uint32_t k = n % kMqVq;
+                ok = wait_bounded(ptx::smem_addr(&sm.vq_full[k]), (n / kMqVq) & 1u, &sm.abort_flag,
+                                  p.ws_flags);
+                if (!ok) break;
+                const MqTile d = sm.vq[k];
+                ptx::mbar_arrive(ptx::smem_addr(&sm.vq_empty[k]));
+                if (d.flags & kDescDone) break;
+                const int32_t* bt_row =
+                    kPaged ? p.block_table + static_cast<size_t>(d.b) * p.max_pages : nullptr;
+                // paged: the pages that hold attended positions of the sequence
+                const int npage = kPaged ? (d.zhi + kPageRows - 1) / kPageRows : 0;
+                for (int sub = 0; sub < NSUB; ++sub) {
+                    const int s = vst(vseq);
+                    ok = wait_bounded(ptx::smem_addr(&sm.empty[s]), ((vseq / VST) & 1u) ^ 1u,
+                                      &sm.abort_flag, p.ws_flags);
+                    if (!ok) break;
+                    const uint32_t vfull = ptx::smem_addr(&sm.full[s]);
+                    ptx::mbar_arrive_expect_tx(vfull, kPaged ? static_cast<uint32_t>(npage) * kPageBytes : kMqStageBytes);
+                    const uint32_t dst = stage0 + s * kMqStageBytes;
+                    const int chunk = d.kvh * NSUB + sub;
+                    if (kPaged) {
+                        for (int j = 0; j < npage; ++j) {
+                            int page = bt_row[(d.t >> 4) + j];
+                            if (page < 0 || page >= p.num_pages) page = 0;   // flagged by the softmax warps
+                            ptx::tma_load_4d(dst + j * kPageBytes, &tm_v, vfull, 0, 0, chunk, page, policy);
+                        }
+                    } else {
+                        // rows past the end of the cache read as zeros
+                        ptx::tma_load_4d(dst, &tm_v, vfull, 0, d.t, chunk, d.b, policy);
+                    }
+                    ++vseq;
+                }
+            }
+            if (!ok) {
+                // let every copy already issued land before the CTA exits
+                for (uint32_t tt = vseq > static_cast<uint32_t>(VST) ? vseq - VST : 0u; tt < vseq; ++tt)
+                    wait_drain(ptx::smem_addr(&sm.full[vst(tt)]), (tt / VST) & 1u);
+            }
+        }
+        __syncwarp();
     } else {
         // ================ softmax and epilogue (warps 2..9, two per TMEM lane quarter) ================
         // Thread j of lane quarter q (warp % 4) owns TMEM lane j: position j of the
@@ -714,7 +787,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 if (sm.rkind[rs] == kMqKindDoneR) return 0;
                 const int t0 = sm.rdesc[rs].t;
                 // cos, sin of t0 f_i: the angle reaches 2.6e5 rad, so it is reduced mod
-                // 2 pi in fp64 before sincosf; then (t0 + 16 a) f_i by the angle sum
+                // 2 pi in fp64 before sincosf; (t0 + j) f_i by the angle sum below
                 if (sid < 64) {
                     const double ang = static_cast<double>(t0) * sm.rope.freq[sid];
                     const double turns = rint(ang * 0.15915494309189535);   // 1 / (2 pi)
@@ -724,20 +797,17 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                     sm.rope.base[sid] = make_float2(cs, sn);
                 }
                 ptx::named_barrier_sync(3, kMqSoftmaxThreads);
-                for (int e = sid; e < 8 * 64; e += kMqSoftmaxThreads) {
-                    const int ii = e >> 3, a = e & 7;
-                    const float2 b0 = sm.rope.base[ii], c0 = sm.rope.coarse[ii][a];
-                    sm.rope.tile[ii][a] = make_float2(b0.x * c0.x - b0.y * c0.y, b0.y * c0.x + b0.x * c0.y);
-                }
-                ptx::named_barrier_sync(3, kMqSoftmaxThreads);
                 const int h = (warp - 2) >> 2;
                 const uint32_t sx = stage0 + rstg(q0) * kMqStageBytes;       // dims [0, 64)
                 const uint32_t sy = stage0 + rstg(q0 + 1) * kMqStageBytes;   // dims [D/2, D/2 + 64)
                 const uint32_t rowoff = (j >> 3) * 1024 + (j & 7) * 128;
-                const int ja = j >> 4, jb = j & 15;
                 uint32_t hx[16], hy[16], lx[16], ly[16];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
+                    // cos, sin of j f_i for this row's pairs 32 h + 8 u .. + 8
+                    uint32_t cj[16];
+                    ptx::tmem_ld16(lane_addr + Cfg::TMEM_TRIG + 64 * h + 16 * u, cj);
+                    ptx::tmem_wait_ld();
                     const uint32_t unit = static_cast<uint32_t>(((4 * h + u) ^ (j & 7)) << 4);
                     const uint4 vx4 = ptx::lds128(sx + rowoff + unit);
                     const uint4 vy4 = ptx::lds128(sy + rowoff + unit);
@@ -749,9 +819,11 @@ __global__ void __launch_bounds__(kMqThreads, 1)
 #pragma unroll
                         for (int tt = 0; tt < 2; ++tt) {
                             const int ii = 32 * h + 8 * u + 2 * e + tt;
-                            const float2 tb = sm.rope.tile[ii][ja], fb = sm.rope.fine[ii][jb];
-                            const float c = tb.x * fb.x - tb.y * fb.y;    // cos((t0 + j) f_i)
-                            const float sn = tb.y * fb.x + tb.x * fb.y;   // sin((t0 + j) f_i)
+                            const float2 tb = sm.rope.base[ii];
+                            const float fc = __uint_as_float(cj[2 * (2 * e + tt)]);
+                            const float fs = __uint_as_float(cj[2 * (2 * e + tt) + 1]);
+                            const float c = tb.x * fc - tb.y * fs;    // cos((t0 + j) f_i)
+                            const float sn = tb.y * fc + tb.x * fs;   // sin((t0 + j) f_i)
                             const float x = sm.rope.w[ii] * (tt ? bf16hi(vx[e]) : bf16lo(vx[e]));
                             const float y = sm.rope.w[64 + ii] * (tt ? bf16hi(vy[e]) : bf16lo(vy[e]));
                             k0[tt] = x * c - y * sn;
@@ -793,21 +865,27 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         };
         bool derive_more = Cfg::KEQV;   // K=V: tiles still to derive
         if constexpr (Cfg::KEQV) {
-            // rotation tables: f_i, the weights of the rotated dims, cos and sin of b f_i
+            // f_i and the weights of the rotated dims; cos and sin of j f_i for this
+            // thread's row j and pairs [32 h, 32 h + 32) into TMEM (|j f_i| < 128)
             for (int e = sid; e < 64; e += kMqSoftmaxThreads) sm.rope.freq[e] = p.rope_freq[e];
             for (int e = sid; e < 128; e += kMqSoftmaxThreads)
                 sm.rope.w[e] = __bfloat162float(p.w_k[(e >> 6) * (D / 2) + (e & 63)]);
-            for (int e = sid; e < 64 * 16; e += kMqSoftmaxThreads) {
-                const int ii = e >> 4, b = e & 15;
-                float sn, cs;
-                sincosf(static_cast<float>(static_cast<double>(b) * p.rope_freq[ii]), &sn, &cs);
-                sm.rope.fine[ii][b] = make_float2(cs, sn);
-            }
-            for (int e = sid; e < 64 * 8; e += kMqSoftmaxThreads) {
-                const int ii = e >> 3, a = e & 7;
-                float sn, cs;   // |16 a f_i| < 128
-                sincosf(static_cast<float>(static_cast<double>(16 * a) * p.rope_freq[ii]), &sn, &cs);
-                sm.rope.coarse[ii][a] = make_float2(cs, sn);
+            {
+                const int h = (warp - 2) >> 2;
+#pragma unroll 1
+                for (int u = 0; u < 4; ++u) {
+                    uint32_t cj[16];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        float sn, cs;
+                        sincosf(static_cast<float>(static_cast<double>(j) * p.rope_freq[32 * h + 8 * u + k]),
+                                &sn, &cs);
+                        cj[2 * k] = __float_as_uint(cs);
+                        cj[2 * k + 1] = __float_as_uint(sn);
+                    }
+                    ptx::tmem_st16(lane_addr + Cfg::TMEM_TRIG + 64 * h + 16 * u, cj);
+                }
+                ptx::tmem_wait_st();
             }
             ptx::named_barrier_sync(3, kMqSoftmaxThreads);
             const int dr = derive(0u);

@@ -125,7 +125,7 @@ cudaError_t launch_mq_impl(const LaunchArgs& a) {
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.grid));
-    cfg.blockDim = dim3(kMqThreads);
+    cfg.blockDim = dim3(Cfg::THREADS);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = a.stream;
     cfg.attrs = pdl;
