@@ -184,7 +184,7 @@ WORKLOADS = {
                  "new token through the multi-query kernel", B=8, S=8192, seed=1,
                  lengths=lengths_uniform(1, 8192, 8), layers=("global",), queries=1),
         Workload("global_mq1_b16_s131072", "decodeGQA long context, B=16, seq_lens uniform on "
-                 "[65536, 131072], one new token through the multi-query kernel", B=16,
+                 "[65536, 131072], one new token through the multi-query entry point", B=16,
                  S=131072, seed=3, lengths=lengths_uniform(65536, 131072, 16),
                  layers=("global",), queries=1),
         # Smaller instance of the batched sliding shape for profiler captures: the same
