@@ -178,10 +178,10 @@ WORKLOADS = {
         Workload("global_mq4_b8_s8192", "decodeGQA, 4 new tokens per sequence (multi-query), B=8, "
                  "seq_lens uniform on [1, 8192]", B=8, S=8192, seed=12,
                  lengths=lengths_uniform(1, 8192, 8), layers=("global",), queries=4),
-        # One new token through the multi-query (tensor-core) kernel, at the single-query
-        # shapes' seeds and lengths: the two kernels side by side on the same input.
+        # One new token through the multi-query entry point, at the single-query shapes'
+        # seeds and lengths (a one-token call runs the single-query kernel).
         Workload("global_mq1_b8_s8192", "decodeGQA, B=8, seq_lens uniform on [1, 8192], one "
-                 "new token through the multi-query kernel", B=8, S=8192, seed=1,
+                 "new token through the multi-query entry point", B=8, S=8192, seed=1,
                  lengths=lengths_uniform(1, 8192, 8), layers=("global",), queries=1),
         Workload("global_mq1_b16_s131072", "decodeGQA long context, B=16, seq_lens uniform on "
                  "[65536, 131072], one new token through the multi-query entry point", B=16,
