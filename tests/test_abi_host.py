@@ -46,6 +46,18 @@ def test_binding_constants_match_the_header():
         assert int(defines[name]) == value, name
 
 
+def test_keqv_kernel_threshold_agrees_everywhere():
+    """The capacity (128-position tiles per CTA) from which a K=V call runs the tcgen05
+    kernel: the library's rule, the bench's kernel naming and the K=V tests' roomy
+    caches must use the same number."""
+    import bench
+    src = open(os.path.join(ROOT, "decode_attention_gb300", "csrc", "gqa_decode.cu")).read()
+    lib_value = int(re.search(r"kKeqvTcTilesPerCta = (\d+);", src).group(1))
+    test_src = open(os.path.join(ROOT, "tests", "test_gpu_keqv.py")).read()
+    test_value = int(re.search(r"_TC_TILES_PER_CTA = (\d+)", test_src).group(1))
+    assert lib_value == bench.KEQV_TC_TILES_PER_CTA == test_value
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
