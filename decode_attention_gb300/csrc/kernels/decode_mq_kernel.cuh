@@ -19,15 +19,16 @@
 // elements (16 KB, 128-byte swizzled, exactly what TMA writes); the P.V mma of a
 // 128-wide head-dim block reads two adjacent stages.
 //
-// Warp roles (352 threads; 384 over a K=V cache).  Warp 0, lane 0: the producer.  It walks the same
-// schedule as the single-query kernel (static units, then claimed dynamic chunks)
+// Warp roles (352 threads; 384 over a K=V cache).  Warp 0, lane 0: the producer.  It
+// walks the same schedule as the single-query kernel (static units, then claimed dynamic
+// chunks)
 // and streams the tiles in the order K(0), K(1), V(0), K(2), V(1), ...: the scores
 // of tile i+1 are computed while the softmax of tile i runs.  K blocks go to one
 // stage ring and V blocks to another, each consumed in order by one warp (with two
 // consumers on one ring, a one-bit phase wait could see the other consumer's
-// earlier fill of the same stage).  It also loads each
-// piece's Q with TMA (box: 64 elements x g heads x T tokens) into one of two
-// buffers.  Warp 1: owns the TMEM allocation; lane 0 issues the scores' mma.
+// earlier fill of the same stage).  It also loads each piece's Q with TMA (box: 64
+// elements x g heads x T tokens) into the Q buffer, once the previous piece's last
+// scores are done.  Warp 1: owns the TMEM allocation; lane 0 issues the scores' mma.
 // Warp 10: lane 0 issues the P.V mma, and the whole warp zeroes the V rows of a tile
 // that lie outside its sequence's attended range before they are read (0 * NaN
 // would poison the sum).  A tcgen05.mma costs its issuing thread about 75 cycles
@@ -39,9 +40,10 @@
 // (lane 0) streams the V blocks from tile descriptors the producer hands it, and the
 // softmax warps also derive the next tile's rotated keys into TMEM.
 //
-// Pieces alternate between two O^T buffers in TMEM: a piece's output is written
-// after the next tile's P has been published, so the softmax warps never wait
-// for the last P.V of a piece before starting the next one.
+// Where the configuration has two O^T buffers in TMEM, pieces alternate between them: a
+// piece's output is written after the next tile's P has been published, so the softmax
+// warps never wait for the last P.V of a piece before starting the next one.  With one
+// buffer, a piece's output is written before the next piece's first P.V.
 //
 // Softmax.  Each query row keeps a reference max m (log2 units) that all threads
 // share; P = exp2(s - m), and m moves only when a score of the tile exceeds it by
