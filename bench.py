@@ -40,7 +40,7 @@ if ROOT not in sys.path:
 
 from decode_attention_gb300 import inputs  # noqa: E402
 
-DEFAULT_WORKLOAD = "global_b8_s8192"
+DEFAULT_WORKLOAD = "paged_mixed_b256"
 HBM_FALLBACK_GBS = 6800.0
 PROFILES = os.path.join(ROOT, "profiles")
 # the sources each main kernel is compiled from: a recorded DRAM traffic figure holds
@@ -59,9 +59,6 @@ KERNEL_SOURCES = {
         "decode_attention_gb300/csrc/kernels/ptx.cuh",
     ],
 }
-# K=V calls whose cache holds at least this many 128-position tiles per CTA (one CTA
-# per SM) run on the tcgen05 kernel (gqa_mq_kernel), smaller ones on gqa_decode_kernel
-KEQV_TC_TILES_PER_CTA = 64
 
 
 # ---------------------------------------------------------------------------
@@ -304,15 +301,16 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def main_kernel(call) -> str:
-    """The kernel a call's positions stream through."""
+def main_kernel(gqa, call) -> str:
+    """The kernel a call's positions stream through: multi-query calls with T >= 2 run
+    on the tcgen05 kernel; a K=V call runs where the library says it does."""
     if call.queries > 1:
         return "gqa_mq_kernel"
     if call.keqv:
         cap = call.case["v"].shape[1]   # K=V calls here are contiguous
-        B = len(call.seq_lens)
-        sms = torch.cuda.get_device_properties(0).multi_processor_count
-        if B * cap * call.geo["KVH"] // 128 >= KEQV_TC_TILES_PER_CTA * sms:
+        choice = gqa.gqa_decode_keqv_kernel(len(call.seq_lens), cap, call.geo["H"],
+                                            call.geo["KVH"], call.geo["D"])
+        if choice == gqa.GQA_KERNEL_TCGEN05:
             return "gqa_mq_kernel"
     return "gqa_decode_kernel"
 
@@ -459,7 +457,11 @@ def run_reference(args, wl):
     return 0
 
 
-def workload_config(wl, l2_note=None):
+# How the timed GPU steps treat L2 (both arms print the same config)
+L2_POLICY = "GPU steps: L2 flushed between timed steps by a write larger than L2"
+
+
+def workload_config(wl):
     if wl.rings:
         geo = [dict(layer=wl.layers[0], **dict(inputs.geometry(wl.layers[0]), window=w), ring=w)
                for w in wl.rings]
@@ -470,8 +472,7 @@ def workload_config(wl, l2_note=None):
            "geometry": geo}
     if wl.step:
         cfg["producer"] = "q/k/v norms, rope and the ring append run ahead of each attention call"
-    if l2_note:
-        cfg["l2"] = l2_note
+    cfg["l2"] = L2_POLICY
     return cfg
 
 
@@ -539,6 +540,19 @@ def run_ours(args, wl):
     bytes_all = sum_over_ranks(bytes_rank, world, dev)
     value = bytes_all / (t_max_ms * 1e-3) / 1e9
 
+    # ---- the launch floor: an empty kernel timed the same way (after the same L2
+    # flush, CUDA events on the same stream); no call can measure below it ----
+    floor_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.warmup + args.steps)]
+    torch.cuda._sleep(2_000_000)
+    for i, (a, b) in enumerate(floor_ev):
+        flush.fill_(i & 0xFF)
+        a.record(stream)
+        torch.cuda._sleep(0)
+        b.record(stream)
+    torch.cuda.synchronize()
+    launch_floor_us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in floor_ev[args.warmup:])
+
     # ---- end to end through the public API: pinned host inputs in, o out ----
     # A decode call takes q and seq_lens from the host and returns o.  In a step
     # workload the producer takes the raw projections and seq_lens from the host
@@ -596,7 +610,7 @@ def run_ours(args, wl):
     dom_ms = statistics.mean(dom.times_ms)
     achieved = dom.bytes / (dom_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
-    kernel = main_kernel(dom)
+    kernel = main_kernel(gqa, dom)
     roofline = {"bound": "hbm", "kernel": f"{kernel}<{dom.name}>",
                 "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -620,9 +634,10 @@ def run_ours(args, wl):
         "warmup": args.warmup, "ms_per_step": round(t_max_ms / args.steps, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "storage_dtype": "bf16", "data": "synthetic",
-        "config": workload_config(wl, f"flushed between timed steps (write of "
-                                      f"{flush.numel() >> 20} MiB > L2 {l2 >> 20} MiB)"),
+        "config": workload_config(wl),
+        "l2_flush": {"bytes": flush.numel(), "l2_bytes": l2},
         "us_per_layer": us_per_layer, "us_p10_p50_p90": pct,
+        "launch_floor_us": round(launch_floor_us, 2),
         "kv_bytes_per_step": sum(c.bytes for c in calls),
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,

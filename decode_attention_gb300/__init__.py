@@ -13,6 +13,11 @@ from ._native import (  # noqa: F401
     GQA_DEVICE_BAD_LENGTH,
     GQA_DEVICE_BAD_PAGE,
     GQA_DEVICE_WAIT_TIMEOUT,
+    GQA_KERNEL_NONE,
+    GQA_KERNEL_SPLIT_DECODE,
+    GQA_KERNEL_TCGEN05,
+    GQA_TEST_SINGLE_PIECE,
+    GQA_TEST_STALL,
     GQA_MAX_QUERIES_GLOBAL,
     GQA_MAX_QUERIES_SLIDING,
     GQA_MAX_SEQ,
@@ -27,6 +32,7 @@ from ._native import (  # noqa: F401
     GQAError,
     gqa_decode,
     gqa_decode_keqv,
+    gqa_decode_keqv_kernel,
     gqa_decode_keqv_paged,
     gqa_decode_mq,
     gqa_decode_mq_paged,
@@ -37,6 +43,9 @@ from ._native import (  # noqa: F401
     gqa_decode_paged,
     gqa_check_inputs_host,
     gqa_device_status,
+    gqa_get_test_mode,
+    gqa_noalloc_status,
+    gqa_set_test_mode,
     gqa_status_string,
     gqa_workspace_init,
     gqa_workspace_size,

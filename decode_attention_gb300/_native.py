@@ -29,6 +29,13 @@ GQA_DEVICE_WAIT_TIMEOUT = 1
 GQA_DEVICE_BAD_PAGE = 2
 GQA_DEVICE_BAD_LENGTH = 4
 
+GQA_KERNEL_NONE = 0
+GQA_KERNEL_SPLIT_DECODE = 1
+GQA_KERNEL_TCGEN05 = 2
+
+GQA_TEST_SINGLE_PIECE = 1
+GQA_TEST_STALL = 2
+
 PAGE_SIZE = 16
 GQA_MAX_SEQ = 262144   # longest cache (positions) a call accepts
 
@@ -37,7 +44,8 @@ EXPORTED_SYMBOLS = ("gqa_workspace_size", "gqa_workspace_init", "gqa_decode", "g
                     "gqa_decode_keqv", "gqa_decode_keqv_paged", "gqa_prepare_decode",
                     "gqa_prepare_decode_paged", "gqa_workspace_size_mq", "gqa_decode_mq",
                     "gqa_decode_mq_paged",
-                    "gqa_check_inputs_host",
+                    "gqa_check_inputs_host", "gqa_noalloc_status", "gqa_decode_keqv_kernel",
+                    "gqa_set_test_mode", "gqa_get_test_mode",
                     "gqa_status_string")
 
 _lock = threading.Lock()
@@ -103,6 +111,14 @@ def load_library(build_if_needed: bool = True) -> ctypes.CDLL:
         lib.gqa_device_status.restype = ci
         lib.gqa_check_inputs_host.argtypes = [vp, ci, ci, ci, vp, ci, ci, ctypes.POINTER(ci)]
         lib.gqa_check_inputs_host.restype = ci
+        lib.gqa_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+        lib.gqa_noalloc_status.restype = ci
+        lib.gqa_decode_keqv_kernel.argtypes = [ci, ci, ci, ci, ci]
+        lib.gqa_decode_keqv_kernel.restype = ci
+        lib.gqa_set_test_mode.argtypes = [ctypes.c_uint32]
+        lib.gqa_set_test_mode.restype = ctypes.c_uint32
+        lib.gqa_get_test_mode.argtypes = []
+        lib.gqa_get_test_mode.restype = ctypes.c_uint32
         lib.gqa_status_string.argtypes = [ci]
         lib.gqa_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -130,6 +146,34 @@ def _ptr(t):
 def _check(fn: str, status: int):
     if status != GQA_OK:
         raise GQAError(fn, status)
+
+
+class _OnDevice:
+    """The library's entry points, each called with ``device`` current: the library
+    takes its SM count, scratch and launch device from the current device."""
+
+    def __init__(self, device):
+        self._lib = load_library()
+        self._device = device
+
+    def __getattr__(self, name):
+        fn = getattr(self._lib, name)
+
+        def call(*args):
+            with torch.cuda.device(self._device):
+                return fn(*args)
+        return call
+
+
+def _lib_on(device) -> _OnDevice:
+    return _OnDevice(device)
+
+
+def _same_device(ref: torch.Tensor, **tensors):
+    """Every tensor argument must sit on the device of ``ref`` (q)."""
+    for name, t in tensors.items():
+        if t is not None:
+            _require(t.device == ref.device, f"{name} must be on {ref.device} (q's device)")
 
 
 def gqa_workspace_init(workspace: torch.Tensor, stream=None) -> None:
@@ -188,7 +232,8 @@ def gqa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens: torc
     _check_tensor("out", out, out.dtype, 3)
     _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = load_library().gqa_decode(
+    _same_device(q, k=k, v=v, seq_lens=seq_lens, out=out, workspace=workspace)
+    st = _lib_on(q.device).gqa_decode(
         _ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, S, H, KVH, D, int(window), _ptr(out),
         _out_code(out), _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
     _check("gqa_decode", st)
@@ -214,7 +259,9 @@ def gqa_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tens
     _check_tensor("out", out, out.dtype, 3)
     _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = load_library().gqa_decode_paged(
+    _same_device(q, k_pages=k_pages, v_pages=v_pages, block_table=block_table,
+                 seq_lens=seq_lens, out=out, workspace=workspace)
+    st = _lib_on(q.device).gqa_decode_paged(
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), B, P,
         block_table.shape[1], page_size, H, KVH, D, int(window), _ptr(out), _out_code(out),
         _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
@@ -240,7 +287,8 @@ def gqa_decode_ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens:
     _check_tensor("out", out, out.dtype, 3)
     _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = load_library().gqa_decode_ring(
+    _same_device(q, k=k, v=v, seq_lens=seq_lens, out=out, workspace=workspace)
+    st = _lib_on(q.device).gqa_decode_ring(
         _ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, C, H, KVH, D, int(window), _ptr(out),
         _out_code(out), _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
     _check("gqa_decode_ring", st)
@@ -265,7 +313,8 @@ def gqa_decode_keqv(q: torch.Tensor, v: torch.Tensor, w_k: torch.Tensor, seq_len
     _check_tensor("out", out, out.dtype, 3)
     _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = load_library().gqa_decode_keqv(
+    _same_device(q, v=v, w_k=w_k, seq_lens=seq_lens, out=out, workspace=workspace)
+    st = _lib_on(q.device).gqa_decode_keqv(
         _ptr(q), _ptr(v), _ptr(w_k), _ptr(seq_lens), B, S, H, KVH, D, _ptr(out), _out_code(out),
         _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
     _check("gqa_decode_keqv", st)
@@ -291,7 +340,9 @@ def gqa_decode_keqv_paged(q: torch.Tensor, v_pages: torch.Tensor, w_k: torch.Ten
     _check_tensor("out", out, out.dtype, 3)
     _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = load_library().gqa_decode_keqv_paged(
+    _same_device(q, v_pages=v_pages, w_k=w_k, block_table=block_table, seq_lens=seq_lens,
+                 out=out, workspace=workspace)
+    st = _lib_on(q.device).gqa_decode_keqv_paged(
         _ptr(q), _ptr(v_pages), _ptr(w_k), _ptr(block_table), _ptr(seq_lens), B, P,
         block_table.shape[1], page_size, H, KVH, D, _ptr(out), _out_code(out), _ptr(workspace),
         ws_bytes, _stream_handle(stream, q.device))
@@ -331,7 +382,8 @@ def gqa_decode_mq(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens: t
     _require(seq_lens.shape[0] == B, "seq_lens must have B entries")
     out = _mq_out(q, out, out_dtype)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = load_library().gqa_decode_mq(
+    _same_device(q, k=k, v=v, seq_lens=seq_lens, out=out, workspace=workspace)
+    st = _lib_on(q.device).gqa_decode_mq(
         _ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, T, S, H, KVH, D, int(window), _ptr(out),
         _out_code(out), _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
     _check("gqa_decode_mq", st)
@@ -354,7 +406,9 @@ def gqa_decode_mq_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.T
     _require(block_table.shape[0] == B and seq_lens.shape[0] == B, "batch size mismatch")
     out = _mq_out(q, out, out_dtype)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = load_library().gqa_decode_mq_paged(
+    _same_device(q, k_pages=k_pages, v_pages=v_pages, block_table=block_table,
+                 seq_lens=seq_lens, out=out, workspace=workspace)
+    st = _lib_on(q.device).gqa_decode_mq_paged(
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), B, T, P,
         block_table.shape[1], page_size, H, KVH, D, int(window), _ptr(out), _out_code(out),
         _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
@@ -384,7 +438,9 @@ def gqa_prepare_decode(q_raw: torch.Tensor, k_raw: torch.Tensor, v_raw, w_q: tor
     KVH = k_raw.shape[1]
     _require(tuple(v_cache.shape[2:]) == (KVH, D) and v_cache.shape[0] == B, "cache shape mismatch")
     _require(q_out.shape == q_raw.shape, "q_out must match q_raw")
-    st = load_library().gqa_prepare_decode(
+    _same_device(q_raw, k_raw=k_raw, v_raw=v_raw, w_q=w_q, w_k=w_k, seq_lens=seq_lens,
+                 q_out=q_out, k_cache=k_cache, v_cache=v_cache)
+    st = _lib_on(q_raw.device).gqa_prepare_decode(
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(w_q), _ptr(w_k), _ptr(seq_lens), B, H, KVH, D,
         _ptr(q_out), _ptr(k_cache), _ptr(v_cache), v_cache.shape[1], 1 if ring else 0,
         _stream_handle(stream, q_raw.device))
@@ -410,7 +466,9 @@ def gqa_prepare_decode_paged(q_raw: torch.Tensor, k_raw: torch.Tensor, v_raw, w_
     B, H, D = q_raw.shape
     KVH = k_raw.shape[1]
     P, page_size = v_pages.shape[0], v_pages.shape[1]
-    st = load_library().gqa_prepare_decode_paged(
+    _same_device(q_raw, k_raw=k_raw, v_raw=v_raw, w_q=w_q, w_k=w_k, block_table=block_table,
+                 seq_lens=seq_lens, q_out=q_out, k_pages=k_pages, v_pages=v_pages)
+    st = _lib_on(q_raw.device).gqa_prepare_decode_paged(
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(w_q), _ptr(w_k), _ptr(block_table),
         _ptr(seq_lens), B, P, block_table.shape[1], page_size, H, KVH, D, _ptr(q_out),
         _ptr(k_pages), _ptr(v_pages), _stream_handle(stream, q_raw.device))
@@ -432,7 +490,8 @@ def gqa_decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_le
     _require(seq_lens.shape[0] == B, "seq_lens must have B entries")
     _check_tensor("out", out, out.dtype, 3)
     _require(tuple(out.shape) == (B, H, D), "out must be [B, H, D]")
-    st = load_library().gqa_decode_noalloc(
+    _same_device(q, k=k, v=v, seq_lens=seq_lens, out=out)
+    st = _lib_on(q.device).gqa_decode_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, S, H, KVH, D, int(window), _ptr(out),
         _out_code(out), _stream_handle(stream, q.device))
     _check("gqa_decode_noalloc", st)
@@ -465,3 +524,30 @@ def gqa_device_status(workspace: torch.Tensor | None = None, stream=None) -> int
                                           _stream_handle(stream, dev))
     _check("gqa_device_status", st)
     return int(flags.value)
+
+
+def gqa_noalloc_status(stream=None, device=None) -> int:
+    """Read and clear the status word of gqa_decode_noalloc's fixed array on ``device``
+    (default: the current device); synchronises the stream.  Allocates nothing."""
+    flags = ctypes.c_uint32(0)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    st = _lib_on(dev).gqa_noalloc_status(ctypes.byref(flags), _stream_handle(stream, dev))
+    _check("gqa_noalloc_status", st)
+    return int(flags.value)
+
+
+def gqa_decode_keqv_kernel(B: int, capacity: int, H: int = 32, KVH: int = 4, D: int = 512,
+                           device=None) -> int:
+    """GQA_KERNEL_* code of the kernel a K=V call with these sizes runs on ``device``
+    (capacity: S, or 16 * max_pages for a paged cache)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    return int(_lib_on(dev).gqa_decode_keqv_kernel(B, capacity, H, KVH, D))
+
+
+def gqa_set_test_mode(flags: int) -> int:
+    """Set the process-wide test mode (GQA_TEST_* bits, 0 = normal); returns the previous one."""
+    return int(load_library().gqa_set_test_mode(int(flags)))
+
+
+def gqa_get_test_mode() -> int:
+    return int(load_library().gqa_get_test_mode())

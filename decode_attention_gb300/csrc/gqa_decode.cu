@@ -5,6 +5,7 @@
 // Spec, "Compute-graph nodes", the slidingDecodeGQA and decodeGQA rows; tensor
 // shapes from "Tensors of the main nodes"; 16-position pages from "At a glance",
 // Shape domain row).
+#include <atomic>
 #include <cstdint>
 #include <cmath>
 #include <cstring>
@@ -41,19 +42,24 @@ constexpr int kKeqvTcTilesPerCta = 64;
 // ---- workspace layout --------------------------------------------------------
 // [0, 4)              status word (uint32)
 // [64, 68)            dynamic-chunk claim counter (zero between calls)
+// [128, 132)          producers finished (zero between calls)
 // [256, 65792)        per-(b, kvh) partial lists, 4096 x int4
+// [65792, 82176)      per-(b, kvh) partials stored, 4096 x uint32 (zero between calls)
 // [ml_off, ...)       softmax partial (m, l): slots x G x 2 floats
 // [acc_off, ...)      softmax partial acc:    slots x G x D floats
 // slots = kMaxCtas + B * KVH + kMaxDynUnits bounds the partials one call can
 // store: static unit j keeps its piece of segment u at slot j + u, dynamic
 // chunk k at slot kMaxCtas + B * KVH + k.
-// The status word and the claim counter must be zero before a call; every
-// completed call leaves them so.
+// The status word and the counters must be zero before a call; every completed
+// call leaves them so (gqa_device_status zeroes the whole header after a call
+// that raised a status bit, e.g. one that timed out half-way).
 constexpr size_t kFlagsOff = 0;
 constexpr size_t kClaimOff = 64;
+constexpr size_t kDoneOff = 128;
 constexpr size_t kSegsOff = 256;
 constexpr size_t kMaxSegments = static_cast<size_t>(GQA_MAX_BATCH) * 16;
-constexpr size_t kHeaderBytes = kSegsOff + kMaxSegments * 16;
+constexpr size_t kSegCountOff = kSegsOff + kMaxSegments * 16;
+constexpr size_t kHeaderBytes = kSegCountOff + kMaxSegments * 4;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -88,6 +94,34 @@ struct DeviceState {
 };
 
 DeviceState g_dev[kMaxDevices];
+
+// Test modes of the calls that follow (GQA_TEST_* bits; 0 in normal use).
+std::atomic<uint32_t> g_test_mode{0};
+
+// Whether a K=V call runs on the tcgen05 kernel.  Long histories do (derived keys in
+// TMEM); short ones are latency-bound: the tcgen05 kernel's pipeline fill and per-piece
+// steps cost more than they save there, and the mma.sync streaming kernel finishes
+// first.  The host knows only the cache capacity, so the split is on capacity tiles
+// (128 positions) per CTA.
+bool keqv_long_history(int B, int capacity, int KVH, int grid) {
+    const long long cap_tiles = static_cast<long long>(B) * capacity * KVH / 128;
+    return cap_tiles >= static_cast<long long>(kKeqvTcTilesPerCta) * grid;
+}
+
+// CTAs of one persistent launch on the current device (its SM count), or 0.
+int device_grid() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    DeviceState& ds = g_dev[dev];
+    std::lock_guard<std::mutex> lock(ds.mu);
+    if (ds.sm_count == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return 0;
+        ds.sm_count = n;
+    }
+    return ds.sm_count < kMaxCtas ? ds.sm_count : kMaxCtas;
+}
 
 }  // namespace
 
@@ -202,6 +236,8 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
     a.p.ws_segs = reinterpret_cast<int4*>(w + kSegsOff);
     a.p.ws_flags = reinterpret_cast<uint32_t*>(w + kFlagsOff);
     a.p.ws_claim = reinterpret_cast<uint32_t*>(w + kClaimOff);
+    a.p.ws_seg_count = reinterpret_cast<uint32_t*>(w + kSegCountOff);
+    a.p.ws_done = reinterpret_cast<uint32_t*>(w + kDoneOff);
     a.p.dyn_slot_base = kMaxCtas + c.B * c.KVH;
     a.p.max_dyn = gqa::kMaxDynUnits;
     a.p.B = c.B;
@@ -214,6 +250,7 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
     a.p.max_pages = max_pages;
     a.p.out_f32 = out_dtype == GQA_OUT_F32 ? 1 : 0;
     a.p.T = c.T;
+    a.p.test_flags = g_test_mode.load(std::memory_order_relaxed);
     a.grid = grid;
     a.stream = stream;
     if (w_k) {
@@ -223,13 +260,9 @@ gqa_status_t run(const CallShape& c, bool paged, const void* q, const void* k, c
         for (int i = 0; i < 64; ++i)
             a.p.rope_freq[i] = std::pow(kGlobalRopeTheta, -2.0 * i / static_cast<double>(c.D));
         a.p.keqv_operand = reinterpret_cast<__nv_bfloat16*>(w + lay.operand_off);
-        // Long histories run on the tcgen05 kernel (derived keys in TMEM).  Short ones
-        // are latency-bound: its pipeline fill and per-piece steps cost more than they
-        // save there, and the mma.sync streaming kernel finishes first.  The host knows
-        // only the cache capacity, so the split is on capacity tiles per CTA.
-        const long long cap_tiles = static_cast<long long>(c.B) * capacity * c.KVH / 128;
-        const bool long_history = cap_tiles >= static_cast<long long>(kKeqvTcTilesPerCta) * grid;
-        const cudaError_t e = long_history ? gqa::launch_keqv_tc(a, paged) : gqa::launch_global_keqv(a, paged);
+        const cudaError_t e = keqv_long_history(c.B, capacity, c.KVH, grid)
+                                  ? gqa::launch_keqv_tc(a, paged)
+                                  : gqa::launch_global_keqv(a, paged);
         return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
     }
     // One new token per sequence is a single-token decode: the mma.sync kernel streams
@@ -438,6 +471,21 @@ gqa_status_t gqa_check_inputs_host(const int32_t* seq_lens, int B, int capacity,
     }
     return GQA_OK;
 }
+
+gqa_kernel_t gqa_decode_keqv_kernel(int B, int capacity, int H, int KVH, int D) {
+    if (geometry_of(H, KVH, D) != Geometry::kGlobal || B < 1 || B > GQA_MAX_BATCH ||
+        capacity < 1 || capacity > GQA_MAX_SEQ)
+        return GQA_KERNEL_NONE;
+    const int grid = device_grid();
+    if (grid == 0) return GQA_KERNEL_NONE;
+    return keqv_long_history(B, capacity, KVH, grid) ? GQA_KERNEL_TCGEN05 : GQA_KERNEL_SPLIT_DECODE;
+}
+
+uint32_t gqa_set_test_mode(uint32_t flags) {
+    return g_test_mode.exchange(flags & (GQA_TEST_SINGLE_PIECE | GQA_TEST_STALL));
+}
+
+uint32_t gqa_get_test_mode(void) { return g_test_mode.load(); }
 
 const char* gqa_status_string(gqa_status_t status) {
     switch (status) {

@@ -23,17 +23,26 @@ namespace {
 __device__ __align__(256) uint8_t g_noalloc_scratch[GQA_NOALLOC_SCRATCH_BYTES];
 
 // Layout of the fixed scratch for one call (offsets in bytes):
-//   [0, 4)         status word        } cleared before every call
-//   [64, 68)       claim counter      }
-//   [256, ...)     B*KVH partial lists (int4)
+//   [0, 4)         status word        (kept across calls; gqa_noalloc_status reads
+//                                      and clears it)
+//   [64, 68)       claim counter      } cleared before every call
+//   [128, 132)     producers finished }
+//   [256, 16640)   partials stored per segment, 4096 x uint32: at a fixed place, so
+//                  that calls of any shape find them zero (every completed call
+//                  leaves them so; gqa_noalloc_status zeroes them after a call that
+//                  raised a status bit)
+//   [16640, ...)   B*KVH partial lists (int4)
 //   [ml, ...)      slots x G x 2 floats;  [acc, ...) slots x G x D floats
 // with slots = grid + B*KVH + dyn: static unit j of the kernel keeps its piece
 // of segment u at slot j + u (j < grid), dynamic chunk k at slot grid + B*KVH + k
 // (k < dyn).  dyn is min(kDynChunksPerCta grid, kMaxDynUnits) when that fits the
 // array, else what does fit (down to 0: the kernel then splits the work into
 // static units only); the kernel is told the bound and never exceeds it.
-constexpr size_t kClearBytes = 128;
-constexpr size_t kSegsOff = 256;
+constexpr size_t kClaimOff = 64;
+constexpr size_t kDoneOff = 128;
+constexpr size_t kCountersBytes = 128;   // the claim and producer counters' lines
+constexpr size_t kSegCountOff = 256;
+constexpr size_t kSegsOff = kSegCountOff + static_cast<size_t>(GQA_MAX_BATCH) * 16 * 4;
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -134,8 +143,9 @@ extern "C" gqa_status_t gqa_decode_noalloc(const void* q, const void* k, const v
     if (lay.total > GQA_NOALLOC_SCRATCH_BYTES) return GQA_ERR_WORKSPACE;   // call too large
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // the status word and the claim counter must start at zero
-    if (cudaMemsetAsync(ws, 0, kClearBytes, s) != cudaSuccess) return GQA_ERR_CUDA;
+    // the claim and producer counters must start at zero (the status word keeps earlier
+    // calls' bits)
+    if (cudaMemsetAsync(ws + kClaimOff, 0, kCountersBytes, s) != cudaSuccess) return GQA_ERR_CUDA;
 
     gqa::LaunchArgs a;
     std::memset(&a, 0, sizeof a);
@@ -151,7 +161,9 @@ extern "C" gqa_status_t gqa_decode_noalloc(const void* q, const void* k, const v
     a.p.ws_ml = reinterpret_cast<float*>(ws + lay.ml_off);
     a.p.ws_segs = reinterpret_cast<int4*>(ws + kSegsOff);
     a.p.ws_flags = reinterpret_cast<uint32_t*>(ws);
-    a.p.ws_claim = reinterpret_cast<uint32_t*>(ws + 64);
+    a.p.ws_claim = reinterpret_cast<uint32_t*>(ws + kClaimOff);
+    a.p.ws_seg_count = reinterpret_cast<uint32_t*>(ws + kSegCountOff);
+    a.p.ws_done = reinterpret_cast<uint32_t*>(ws + kDoneOff);
     a.p.dyn_slot_base = lay.dyn_slot_base;
     a.p.max_dyn = lay.max_dyn;
     a.p.B = B;
@@ -163,8 +175,30 @@ extern "C" gqa_status_t gqa_decode_noalloc(const void* q, const void* k, const v
     a.p.num_pages = 0;
     a.p.max_pages = 0;
     a.p.out_f32 = out_dtype == GQA_OUT_F32 ? 1 : 0;
+    a.p.T = 1;
+    a.p.test_flags = gqa_get_test_mode();
     a.grid = grid;
     a.stream = s;
     const cudaError_t e = sliding ? gqa::launch_sliding(a, false) : gqa::launch_global(a, false);
     return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+extern "C" gqa_status_t gqa_noalloc_status(uint32_t* flags, gqa_stream_t stream) {
+    if (!flags) return GQA_ERR_INVALID_ARGUMENT;
+    *flags = 0;
+    uint8_t* ws = nullptr;
+    int grid = 0;
+    gqa_status_t st = device_scratch(&ws, &grid);
+    if (st != GQA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GQA_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return GQA_ERR_CUDA;
+    // after a raised bit (perhaps a call that timed out half-way) the word and every
+    // counter start again from zero
+    if (word != 0 &&
+        (cudaMemsetAsync(ws, 0, kSegsOff, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess))
+        return GQA_ERR_CUDA;
+    *flags = word;
+    return GQA_OK;
 }

@@ -24,11 +24,16 @@
 // "partial".  A segment with a single partial is written straight to the
 // output; otherwise each partial stores its (m, l, acc) softmax state in the
 // workspace (static unit j at slot j + u, dynamic chunk k at slot
-// dyn_slot_base + k) and the combine kernel (combine_kernel.cuh), launched
-// right behind this one, merges them -- static units in order, then the
-// segment's dynamic chunks in order -- with the log-sum-exp rule.  Which CTA
-// processes a unit does not change its arithmetic, so results are
-// bit-reproducible.
+// dyn_slot_base + k), and the partials are merged -- static units in order, then
+// the segment's dynamic chunks in order -- with the log-sum-exp rule:
+//   * policies with small partials (kMergeInKernel: slidingDecodeGQA, 2 KB) merge
+//     in this kernel: each partial counts itself on the segment's arrival counter,
+//     and the CTA whose partial completes the count merges them all, writes the
+//     output and zeroes the counter for the next call;
+//   * the others leave it to the combine kernel (combine_kernel.cuh), launched
+//     right behind this one, whose many blocks share the larger merges.
+// Which CTA processes a unit, or merges a segment, does not change the
+// arithmetic, so results are bit-reproducible.
 //
 // Data movement.  One producer thread walks the schedule and streams K and V
 // tiles of TP positions through a ring of shared-memory stages with TMA (4-D
@@ -73,6 +78,16 @@ constexpr uint32_t kFlagWaitTimeout = 1u;
 constexpr uint32_t kFlagBadPage = 2u;
 constexpr uint32_t kFlagBadLength = 4u;
 
+// Test modes (same values as the public header's GQA_TEST_* macros).
+//   kTestSinglePiece: one CTA streams every segment, so each segment is one piece
+//     written straight to the output (no split, no combine).
+//   kTestStall: each producer, after issuing its first tile, waits on a barrier
+//     that nothing completes; the wait gives up after kTestStallNs, which takes the
+//     timeout exit of every role.
+constexpr uint32_t kTestSinglePiece = 1u;
+constexpr uint32_t kTestStall = 2u;
+constexpr uint64_t kTestStallNs = 1000000ull;   // 1 ms
+
 struct DecodeParams {
     const __nv_bfloat16* q;       // [B, H, D]
     const int32_t* seq_lens;      // [B]
@@ -82,7 +97,10 @@ struct DecodeParams {
     float* ws_ml;                 // [slots, G, 2]
     int4* ws_segs;                // [B * KVH] partial list per segment (SegmentParts)
     uint32_t* ws_flags;           // device status word
-    uint32_t* ws_claim;           // dynamic-chunk claim counter (reset by the combine kernel)
+    uint32_t* ws_claim;           // dynamic-chunk claim counter (zero between calls)
+    uint32_t* ws_seg_count;       // [B * KVH] partials stored per segment (in-kernel merge;
+                                  // zero between calls)
+    uint32_t* ws_done;            // producers finished (in-kernel merge; zero between calls)
     int dyn_slot_base;            // first workspace slot of the dynamic chunks (> grid + B*KVH - 2)
     int max_dyn;                  // dynamic-chunk slots the workspace holds (<= kMaxDynUnits)
     int B, H, KVH;
@@ -94,6 +112,7 @@ struct DecodeParams {
     int out_f32;                  // 1: fp32 output, 0: bf16
     int T;                        // query tokens per sequence, at positions L - T .. L - 1
                                   // (0 or 1: the single decode token at L - 1)
+    uint32_t test_flags;          // kTestSinglePiece / kTestStall (0 in normal use)
     // single K=V cache (policies with kKeqV): the k_norm weight [D] and the rotary
     // frequencies theta^(-2i/D) of the rotated pairs, in fp64
     const __nv_bfloat16* w_k;
@@ -153,6 +172,15 @@ __device__ __forceinline__ int upper_seq(const T* pref, int B, long long x) {
     return lo;
 }
 
+// floor(a / b) for a >= 0, b > 0: one 32-bit division when a fits 32 bits (always,
+// for the sizes of this kernel's plan; the 64-bit division is a long software
+// routine on the critical path of every CTA's start).
+__device__ __forceinline__ long long div_floor(long long a, long long b) {
+    if ((static_cast<unsigned long long>(a) >> 32) == 0 && (static_cast<unsigned long long>(b) >> 32) == 0)
+        return static_cast<long long>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+    return a / b;
+}
+
 // Static tiles of each segment of sequence b.
 __device__ __forceinline__ int static_tiles(const PlanSmem& pl, int b) {
     return (pl.sn[b] + pl.unit - 1) / pl.unit;
@@ -161,11 +189,11 @@ __device__ __forceinline__ int static_tiles(const PlanSmem& pl, int b) {
 // (b, kvh) order and counted in tiles, are split evenly over the units: a unit
 // boundary never falls inside a tile, so no tile is read by two CTAs.
 __device__ __forceinline__ long long static_unit_begin(const PlanSmem& pl, int j) {
-    return static_cast<long long>(j) * pl.n_static / pl.g_eff;
+    return div_floor(static_cast<long long>(j) * pl.n_static, pl.g_eff);
 }
 // static unit containing static tile x (units are floor(j Ns / Ge))
 __device__ __forceinline__ int static_unit_of(const PlanSmem& pl, long long x) {
-    return static_cast<int>(((x + 1) * pl.g_eff - 1) / pl.n_static);
+    return static_cast<int>(div_floor((x + 1) * pl.g_eff - 1, pl.n_static));
 }
 
 // The partials of segment (b, kvh): static units first_s..first_s+ns_parts-1,
@@ -217,6 +245,7 @@ struct alignas(1024) KernelSmem {
     TileDesc desc[Pol::STAGES];
     alignas(8) uint64_t q_empty[2];           // q buffer free (consumer warps arrive)
     alignas(8) uint64_t ready[Pol::STAGES];   // K=V: the stage's rotation angles are ready
+    alignas(8) uint64_t stall_bar;            // kTestStall: a barrier nothing completes
     PlanSmem plan;
     // q of the next pieces (bf16, [G][D]), copied in by the producer with the
     // first tile of each piece; double-buffered over pieces
@@ -228,12 +257,14 @@ struct alignas(1024) KernelSmem {
     float l[Pol::G];
     typename Pol::Scratch scratch;   // each policy aligns its own members (16 B or more)
     int abort_flag;
+    int merge_last;                  // this CTA stored the last partial of the segment
 };
 
 // Bounded mbarrier wait.  Returns false when the CTA is aborting or the wait
-// timed out (which starts the abort).
+// timed out after limit_ns (which starts the abort).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
-                                             volatile int* abort_flag, uint32_t* flags) {
+                                             volatile int* abort_flag, uint32_t* flags,
+                                             uint64_t limit_ns = kWaitLimitNs) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t round = 0;; ++round) {
@@ -241,7 +272,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
             if (ptx::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         // time limit, with an iteration cap in case the timer does not advance
-        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs || round > kWaitMaxRounds) {
+        if (ptx::globaltimer_ns() - t0 > limit_ns || round > kWaitMaxRounds) {
             *abort_flag = 1;
             atomicOr(flags, kFlagWaitTimeout);
             return false;
@@ -365,8 +396,10 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
     const uint32_t tail_want = static_cast<uint32_t>(kDynTailPerCta) * ugrid;
     const uint32_t tail_cap = tail_want < cap / 2 ? tail_want : cap / 2;
     const uint32_t long_cap = cap - tail_cap;
-    // floor(N / g) >= kDynMinShare
-    const bool use_dyn = g > 0 && N >= static_cast<uint32_t>(kDynMinShare) * g && long_cap > 0;
+    // floor(N / g) >= kDynMinShare; none in the single-piece test mode
+    const bool single = (p.test_flags & kTestSinglePiece) != 0;
+    const bool use_dyn = !single && g > 0 && N >= static_cast<uint32_t>(kDynMinShare) * g &&
+                         long_cap > 0;
     int c = kDynMinChunk, T = 0;
     if (use_dyn) {
         const float Nf = static_cast<float>(N);
@@ -476,8 +509,80 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
         pl.n_dyn = dincl + d1incl;
         pl.c_dyn = c;
         pl.c_dyn1 = c1;
-        pl.g_eff = static_cast<int>(sincl < ugrid ? sincl : ugrid);
+        const uint32_t units = single ? 1u : ugrid;   // single piece: CTA 0 takes all
+        pl.g_eff = static_cast<int>(sincl < units ? sincl : units);
     }
+}
+
+// ---------------------------------------------------------------------------
+// In-kernel merge of a segment's partials
+// ---------------------------------------------------------------------------
+
+constexpr int kMergeBatch = 16;   // partials whose loads are in flight together
+
+// Output = the log-sum-exp merge of the segment's partials, in the fixed order of
+// SegmentParts: with M = max_j m_j, o = sum_j 2^(m_j - M) acc_j / sum_j 2^(m_j - M) l_j
+// (m in log2 units), evaluated as a running merge over batches of partials.  A
+// partial that saw no key (m = -inf) weighs 0; no key at all gives the empty sum, 0;
+// a NaN normaliser (bad page) stays NaN.  Thread t owns the outputs [2t, 2t + 2) of
+// the segment's G x D (kThreads = G D / 2).  The partials were stored by other SMs:
+// loads bypass L1.
+template <int G, int D, int kThreads>
+__device__ __forceinline__ void merge_segment(const DecodeParams& p, const SegmentParts& sp, int u,
+                                              size_t out_base, int tid) {
+    static_assert(G * D == 2 * kThreads, "two outputs per thread");
+    const int nparts = sp.count();
+    const int h = (2 * tid) / D;
+    const float2* acc2 = reinterpret_cast<const float2*>(p.ws_acc);
+    const float2* ml2 = reinterpret_cast<const float2*>(p.ws_ml);
+    float M = -INFINITY, den = 0.0f, nx = 0.0f, ny = 0.0f;
+    for (int j0 = 0; j0 < nparts; j0 += kMergeBatch) {
+        float2 mlj[kMergeBatch], aj[kMergeBatch];
+#pragma unroll
+        for (int q = 0; q < kMergeBatch; ++q) {
+            mlj[q] = make_float2(-INFINITY, 0.0f);
+            aj[q] = make_float2(0.0f, 0.0f);
+            if (j0 + q < nparts) {
+                const size_t sl = sp.slot(j0 + q, u);
+                mlj[q] = __ldcg(ml2 + sl * G + h);
+                aj[q] = __ldcg(acc2 + sl * (G * D / 2) + tid);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kMergeBatch; ++q) {
+            if (j0 + q >= nparts) break;
+            const float Mn = fmaxf(M, mlj[q].x);
+            const float sc = M == -INFINITY ? 0.0f : exp2f(M - Mn);
+            const float w = mlj[q].x == -INFINITY ? 0.0f : exp2f(mlj[q].x - Mn);
+            den = den * sc + w * mlj[q].y;
+            nx = nx * sc + w * aj[q].x;
+            ny = ny * sc + w * aj[q].y;
+            M = Mn;
+        }
+    }
+    const float inv = den == 0.0f ? 0.0f : 1.0f / den;
+    store_out2(p, out_base + 2 * static_cast<size_t>(tid), nx * inv, ny * inv);
+}
+
+// After this CTA's consumers stored a partial of segment u: count it, and if it was
+// the segment's last, merge all of them into the output.  Every consumer thread
+// calls this; `last` is a shared-memory flag.  One thread counts, with release
+// semantics (the CTA's partial stores, ordered before it by the barrier, are
+// visible to the merging CTA) and acquire semantics (if it completes the count, the
+// other CTAs' partials are visible here; the barrier after it passes that on).
+template <int G, int D, int kThreads>
+__device__ __forceinline__ void count_and_merge(const DecodeParams& p, const SegmentParts& sp,
+                                                int u, size_t out_base, int tid, volatile int* last) {
+    ptx::named_barrier_sync(1, kThreads);
+    if (tid == 0)
+        *last = ptx::atom_add_acq_rel_gpu(p.ws_seg_count + u, 1u) ==
+                        static_cast<uint32_t>(sp.count() - 1)
+                    ? 1
+                    : 0;
+    ptx::named_barrier_sync(1, kThreads);
+    if (!*last) return;
+    merge_segment<G, D, kThreads>(p, sp, u, out_base, tid);
+    if (tid == 0) p.ws_seg_count[u] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -517,6 +622,7 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
         ptx::mbar_init(ptx::smem_addr(&sm.q_empty[1]), NC);
         if (Pol::kKeqV)
             for (int s = 0; s < STAGES; ++s) ptx::mbar_init(ptx::smem_addr(&sm.ready[s]), 1);
+        ptx::mbar_init(ptx::smem_addr(&sm.stall_bar), 1);
         ptx::fence_mbar_init();
         sm.abort_flag = 0;
     }
@@ -542,8 +648,8 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
     // the partial list of every segment, for the combine kernel (each CTA a slice)
     {
         const int U = B * KVH;
-        const int u_end = static_cast<int>(static_cast<long long>(cta + 1) * U / gridDim.x);
-        for (int u = static_cast<int>(static_cast<long long>(cta) * U / gridDim.x) + tid; u < u_end;
+        const int u_end = (cta + 1) * U / static_cast<int>(gridDim.x);   // < 2^31: U <= 4096
+        for (int u = cta * U / static_cast<int>(gridDim.x) + tid; u < u_end;
              u += blockDim.x) {
             const int b = u / KVH, kvh = u - (u / KVH) * KVH;
             int4 e = make_int4(0, 0, 0, 0);
@@ -650,6 +756,11 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
                     }
                     first = false;
                     ++t_idx;
+                    // test mode: wait for a barrier that nothing completes (times out)
+                    if ((p.test_flags & kTestStall) && t_idx == 1 &&
+                        !wait_bounded(ptx::smem_addr(&sm.stall_bar), 0u, &sm.abort_flag, p.ws_flags,
+                                      kTestStallNs))
+                        return false;
                 }
                 a = e;
             }
@@ -663,7 +774,7 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
             const int b = upper_seq(pl.spref, B, x);
             const int st = static_tiles(pl, b);
             const long long rel = x - pl.spref[b];
-            const int kvh = static_cast<int>(rel / st);
+            const int kvh = static_cast<int>(div_floor(rel, st));
             const int k0 = static_cast<int>(rel - static_cast<long long>(kvh) * st);
             const int take = static_cast<int>(stop - x < st - k0 ? stop - x : st - k0);
             x += take;
@@ -706,6 +817,14 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
             const uint32_t first = t_idx > static_cast<uint32_t>(STAGES) ? t_idx - STAGES : 0u;
             for (uint32_t tt = first; tt < t_idx; ++tt)
                 wait_drain(ptx::smem_addr(&sm.full[tt % STAGES]), (tt / STAGES) & 1u);
+        }
+        if (Pol::kMergeInKernel && dynamic) {
+            // no combine kernel follows: the last producer to finish claiming zeroes
+            // the claim counter for the next call
+            if (ptx::atom_add_acq_rel_gpu(p.ws_done, 1u) == static_cast<uint32_t>(pl.g_eff - 1)) {
+                atomicExch(p.ws_claim, 0u);
+                atomicExch(p.ws_done, 0u);
+            }
         }
         return;
     }
@@ -780,11 +899,14 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
         const SegmentParts sp(pl, d.b, d.kvh, p.dyn_slot_base);
         const int nparts = sp.count();
         const size_t out_base = (static_cast<size_t>(d.b) * H + d.kvh * G) * D;
+        const int seg_u = d.b * p.KVH + d.kvh;
         if constexpr (Pol::kDirectEpilogue) {
             // each warp stores its own share of the result from registers: the
-            // output when the piece is the whole segment, else the partial (the
-            // combine kernel merges the partials after this grid completes)
+            // output when the piece is the whole segment, else the partial
             Pol::store(st, p, out_base, nparts == 1 ? -1 : d.slot, bad, warp, lane);
+            if constexpr (Pol::kMergeInKernel)
+                if (nparts > 1)
+                    count_and_merge<G, D, kConsumerThreads>(p, sp, seg_u, out_base, tid, &sm.merge_last);
         } else {
             // merged (m, l, acc) of this piece -> sm.m, sm.l, sm.acc (ends with a
             // consumer barrier)
@@ -799,7 +921,6 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
                                bad ? nan4 : make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
                 }
             } else {
-                // the combine kernel merges the partials after this grid completes
                 const size_t slot = static_cast<size_t>(d.slot);
                 float4* wacc4 = reinterpret_cast<float4*>(p.ws_acc + slot * G * D);
                 for (int i4 = tid; i4 < G * D / 4; i4 += kConsumerThreads)
@@ -808,6 +929,8 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
                     p.ws_ml[(slot * G + tid) * 2 + 0] = bad ? 0.0f : sm.m[tid];
                     p.ws_ml[(slot * G + tid) * 2 + 1] = bad ? nan : sm.l[tid];
                 }
+                if constexpr (Pol::kMergeInKernel)
+                    count_and_merge<G, D, kConsumerThreads>(p, sp, seg_u, out_base, tid, &sm.merge_last);
             }
             // sm.acc is reused by the next piece
             ptx::named_barrier_sync(1, kConsumerThreads);

@@ -168,6 +168,7 @@ struct alignas(1024) MqSmem {
     alignas(8) uint64_t o_ready[2];   // P.V of tile i complete
     alignas(8) uint64_t s_empty[2];   // the softmax warps have read S buffer i % 2
     alignas(8) uint64_t drain[2];     // the two mma warps' final commits
+    alignas(8) uint64_t stall_bar;    // test mode kTestStall: a barrier nothing completes
     int kind[Cfg::KST];               // K ring: a K block or the end-of-work marker
     MqTile desc[Cfg::KST];            // tile of a K block (its first stage)
     int rkind[Cfg::KEQV ? Cfg::RST : 1];       // R ring: an R block or the end-of-work marker
@@ -238,6 +239,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             ptx::mbar_init(ptx::smem_addr(&sm.vq_full[k]), 1);
             ptx::mbar_init(ptx::smem_addr(&sm.vq_empty[k]), 1);
         }
+        ptx::mbar_init(ptx::smem_addr(&sm.stall_bar), 1);
         sm.pv_stop = 0x7fffffff;
         ptx::fence_mbar_init();
         sm.abort_flag = 0;
@@ -262,8 +264,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // partial list of every segment, for the combine kernel
     {
         const int U = B * KVH;
-        const int u_end = static_cast<int>(static_cast<long long>(cta + 1) * U / gridDim.x);
-        for (int u = static_cast<int>(static_cast<long long>(cta) * U / gridDim.x) + tid; u < u_end;
+        const int u_end = (cta + 1) * U / static_cast<int>(gridDim.x);   // < 2^31: U <= 4096
+        for (int u = cta * U / static_cast<int>(gridDim.x) + tid; u < u_end;
              u += blockDim.x) {
             const int b = u / KVH, kvh = u - (u / KVH) * KVH;
             int4 e = make_int4(0, 0, 0, 0);
@@ -451,6 +453,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
                 return true;
             };
+            uint32_t tiles_emitted = 0;
             // The tiles of positions [p0, p1) of segment (b, kvh).
             auto emit_piece = [&](int b, int kvh, int p0, int p1, int slot, bool unit_end) -> bool {
                 const uint32_t ob = n_piece & 1u;
@@ -473,6 +476,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     d.flags = (t == t_first ? kDescFirst : 0) | (last ? kDescLast : 0);
                     d.ob = Cfg::OBUFS == 2 ? static_cast<int>(ob) : 0;
                     if (!emit_tile(d)) return false;
+                    // test mode: wait for a barrier that nothing completes (times out)
+                    // (after the piece's Q load has gone out, so that every copy the
+                    // producer drains on the way out completes)
+                    if ((p.test_flags & kTestStall) && ++tiles_emitted == 1) {
+                        if (!wait_servicing(0u, 0u)) return false;
+                        if (!wait_bounded(ptx::smem_addr(&sm.stall_bar), 0u, &sm.abort_flag, p.ws_flags,
+                                          kTestStallNs))
+                            return false;
+                    }
                 }
                 return true;
             };
@@ -484,7 +496,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const int b = upper_seq(pl.spref, B, x);
                 const int st = static_tiles(pl, b);
                 const long long rel = x - pl.spref[b];
-                const int kvh = static_cast<int>(rel / st);
+                const int kvh = static_cast<int>(div_floor(rel, st));
                 const int k0 = static_cast<int>(rel - static_cast<long long>(kvh) * st);
                 const int take = static_cast<int>(stop - x < st - k0 ? stop - x : st - k0);
                 x += take;

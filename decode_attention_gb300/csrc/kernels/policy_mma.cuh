@@ -43,6 +43,9 @@ struct MmaPolicy {
     // every warp holds the full running max/normaliser and its own slice of the
     // output, so results are stored straight from registers
     static constexpr bool kDirectEpilogue = true;
+    // split segments are merged by the combine kernel (16 KB partials: its many blocks
+    // share the merges better than one CTA per segment)
+    static constexpr bool kMergeInKernel = false;
     static constexpr bool kKeqV = false;   // separate K and V tiles
 
     struct Scratch {

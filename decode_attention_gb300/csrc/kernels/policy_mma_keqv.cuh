@@ -40,6 +40,9 @@ struct MmaKeqV {
     static constexpr bool kSwizzle128 = true;
     static constexpr int kBoxRows = 16;
     static constexpr bool kDirectEpilogue = true;
+    // split segments are merged by the combine kernel (16 KB partials: its many blocks
+    // share the merges better than one CTA per segment)
+    static constexpr bool kMergeInKernel = false;
     static constexpr bool kKeqV = true;              // only the value tile is loaded
     static constexpr int kRot = 64;                  // rotated pairs (i, i + D/2), i < kRot
     static constexpr int kHalf = D / 2;

@@ -32,6 +32,9 @@ struct SlidingCore {
     static constexpr bool kSwizzle128 = false;    // plain [position][D] tiles
     static constexpr int kBoxRows = 64;           // TMA box height on a contiguous cache
     static constexpr bool kDirectEpilogue = false;   // warps merge through shared memory
+    // split segments are merged in the main kernel (small partials), not by the
+    // combine kernel
+    static constexpr bool kMergeInKernel = true;
     static constexpr bool kKeqV = false;   // separate K and V tiles
     static_assert(kPosPerWarp == 8, "reduce-scatter below assumes 8 positions x 2 heads");
 

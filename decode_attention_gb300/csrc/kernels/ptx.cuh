@@ -52,6 +52,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// atom.add at GPU scope with acquire-release semantics.  Release: the writes that
+// happen before it (this thread's, and through a preceding CTA barrier its CTA's)
+// are visible to a thread that acquires the value it wrote.  Acquire: the writes
+// released before the values it read are visible after it.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

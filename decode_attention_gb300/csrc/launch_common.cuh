@@ -43,10 +43,11 @@ bool encode_kv_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t o
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Launches the main kernel and, right behind it, the combine kernel.  Both opt
-// in to programmatic dependent launch: each may start while the kernel before it
-// in the stream drains, and waits (griddepcontrol.wait) before touching global
-// memory that kernel writes.
+// Launches the main kernel and, unless the policy merges split segments in the
+// main kernel, the combine kernel right behind it.  Both opt in to programmatic
+// dependent launch: each may start while the kernel before it in the stream
+// drains, and waits (griddepcontrol.wait) before touching global memory that
+// kernel writes.
 template <class Pol, bool kPaged>
 cudaError_t launch_decode(const LaunchArgs& a) {
     constexpr size_t kSmem = sizeof(KernelSmem<Pol>) + 1024;   // + alignment slack
@@ -81,7 +82,7 @@ cudaError_t launch_decode(const LaunchArgs& a) {
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gqa_decode_kernel<Pol, kPaged>, tm_k, tm_v, a.p);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || Pol::kMergeInKernel) return e;
 
     const int segments = a.p.B * a.p.KVH;
     constexpr int kChunksPerSeg = (Pol::G * Pol::D / 4 + kCombineThreads - 1) / kCombineThreads;

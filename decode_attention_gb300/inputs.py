@@ -187,6 +187,13 @@ WORKLOADS = {
                  "[65536, 131072], one new token through the multi-query entry point", B=16,
                  S=131072, seed=3, lengths=lengths_uniform(65536, 131072, 16),
                  layers=("global",), queries=1),
+        # Smaller instance of the paged mixed batch for profiler captures: the first 16
+        # lengths of the B=256 draw (same seed), 16-position pages in a random order,
+        # 3.2 GB of pools.
+        Workload("paged_mixed_b16", "paged mixed batch, B=16, lognormal seq_lens (median 4096, "
+                 "sigma 1) clipped to [1, 65536]; one sliding and one global call (profiling size)",
+                 B=16, S=65536, seed=4, lengths=lengths_lognormal(4096, 1.0, 1, 65536, 16),
+                 layers=("sliding", "global"), paged=True),
         # Smaller instance of the batched sliding shape for profiler captures: the same
         # bytes per call as sliding_b64_s32768 (every sequence reads its full 1024-position
         # window) with a 2 GB cache instead of 34 GB.

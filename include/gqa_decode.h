@@ -181,12 +181,13 @@ gqa_status_t gqa_device_status(void *workspace, uint32_t *flags, gqa_stream_t st
  *   - Its first call on a device, with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress) and the SM count.  Make
  *     that first call before any stream capture.
- *   - Every call clears the array's status word and claim counter with a
- *     128-byte cudaMemsetAsync on `stream`.
+ *   - Every call clears the array's claim counter with a 64-byte
+ *     cudaMemsetAsync on `stream`.
  * All calls on a device share the one array, and it keeps the last call's
  * contents.  Calls whose kernels overlap on the GPU (different streams) race on
- * it; serialise them.  The device status bits of this call are not reported
- * (gqa_device_status reads workspaces only).
+ * it; serialise them.  The array has its own device status word, which
+ * collects the GQA_DEVICE_* bits of every call until gqa_noalloc_status reads
+ * and clears it (gqa_device_status reads workspaces only).
  */
 #define GQA_NOALLOC_SCRATCH_BYTES (16u << 20)
 
@@ -194,6 +195,15 @@ gqa_status_t gqa_decode_noalloc(const void *q, const void *k, const void *v,
                                 const int32_t *seq_lens, int B, int S, int H, int KVH, int D,
                                 int window, void *out, gqa_out_dtype_t out_dtype,
                                 gqa_stream_t stream);
+
+/*
+ * Read and clear the device status word of gqa_decode_noalloc's fixed array on the
+ * current device: synchronises `stream`, stores the OR of the GQA_DEVICE_* bits
+ * raised by gqa_decode_noalloc calls since the last read into *flags, and zeroes
+ * the word when it was nonzero.  Allocates nothing.  Errors: GQA_ERR_INVALID_ARGUMENT
+ * for a NULL flags pointer, GQA_ERR_CUDA for a failed CUDA call.
+ */
+gqa_status_t gqa_noalloc_status(uint32_t *flags, gqa_stream_t stream);
 
 /*
  * Decode over a window-capped ring-buffer cache.  Each sliding layer of the
@@ -371,6 +381,49 @@ gqa_status_t gqa_decode_mq_paged(const void *q, const void *k_pages, const void 
 gqa_status_t gqa_check_inputs_host(const int32_t *seq_lens, int B, int capacity, int window,
                                    const int32_t *block_table, int max_pages, int P,
                                    int *first_bad);
+
+/*
+ * Which kernel a gqa_decode_keqv / gqa_decode_keqv_paged call with these sizes
+ * runs on the current device.  `capacity` is the cache capacity in positions: S
+ * for a contiguous cache, 16 * max_pages for a paged one.  The choice depends on
+ * the capacity and the device's SM count only (never on the lengths, which stay
+ * on the device): a cache of at least 64 tiles of 128 positions per SM takes the
+ * tcgen05 kernel (GQA_KERNEL_TCGEN05), a smaller one the split-KV mma.sync kernel
+ * (GQA_KERNEL_SPLIT_DECODE).  Returns GQA_KERNEL_NONE for arguments the call would
+ * refuse (other geometries, B outside [1, 256], capacity outside [1, 262144]) or
+ * when the device cannot be queried.  One CUDA attribute query on first use per
+ * device; nothing is enqueued.
+ */
+typedef enum {
+    GQA_KERNEL_NONE = 0,
+    GQA_KERNEL_SPLIT_DECODE = 1, /* gqa_decode_kernel: persistent split-KV, warp-level mma */
+    GQA_KERNEL_TCGEN05 = 2       /* gqa_mq_kernel: tcgen05 mma with TMEM accumulators */
+} gqa_kernel_t;
+
+gqa_kernel_t gqa_decode_keqv_kernel(int B, int capacity, int H, int KVH, int D);
+
+/*
+ * Test modes, for the library's own tests (0 in normal use).  The mode is
+ * process-wide; every gqa_decode* call reads it once when it is made, so a change
+ * affects the calls made after it returns.  gqa_set_test_mode returns the previous
+ * mode; bits other than these are ignored.
+ *
+ *   GQA_TEST_SINGLE_PIECE  every (sequence, KV head) segment is computed in one
+ *       piece by one CTA and written straight to the output: no split-KV partials
+ *       and no combine.  The result differs from a normal call by rounding only;
+ *       the tests check that it agrees within 1e-5.  Slow (one SM does all work).
+ *   GQA_TEST_STALL  each CTA's producer, after issuing its first tile, waits on a
+ *       barrier that nothing completes.  That wait gives up after 1 ms: the call
+ *       takes its timeout exit (every role leaves, copies and tensor-core work in
+ *       flight are drained, TMEM is released), raises GQA_DEVICE_WAIT_TIMEOUT and
+ *       leaves its outputs invalid.  The workspace is fit for the next call once
+ *       gqa_device_status (or gqa_noalloc_status) has read and cleared the word.
+ */
+#define GQA_TEST_SINGLE_PIECE 1u
+#define GQA_TEST_STALL 2u
+
+uint32_t gqa_set_test_mode(uint32_t flags);
+uint32_t gqa_get_test_mode(void);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *gqa_status_string(gqa_status_t status);

@@ -93,3 +93,18 @@ def poison_outside_window(k: torch.Tensor, v: torch.Tensor, lens, window: int):
 
 def cuda_case(B, S, geo, lens, seed):
     return inputs.contiguous_case(B, S, geo["H"], geo["KVH"], geo["D"], lens, seed, device="cuda")
+
+
+def keqv_tcgen05_capacity(B: int, S: int) -> int:
+    """The smallest cache capacity >= S (at most GQA_MAX_SEQ) for which the library
+    runs a K=V call of B sequences on the tcgen05 kernel (gqa_decode_keqv_kernel)."""
+    import decode_attention_gb300 as gqa
+    lo, hi = S, gqa.GQA_MAX_SEQ
+    assert gqa.gqa_decode_keqv_kernel(B, hi) == gqa.GQA_KERNEL_TCGEN05, "no capacity takes tcgen05"
+    while lo < hi:
+        mid = (lo + hi) // 2
+        if gqa.gqa_decode_keqv_kernel(B, mid) == gqa.GQA_KERNEL_TCGEN05:
+            hi = mid
+        else:
+            lo = mid + 1
+    return lo

@@ -46,16 +46,31 @@ def test_binding_constants_match_the_header():
         assert int(defines[name]) == value, name
 
 
-def test_keqv_kernel_threshold_agrees_everywhere():
-    """The capacity (128-position tiles per CTA) from which a K=V call runs the tcgen05
-    kernel: the library's rule, the bench's kernel naming and the K=V tests' roomy
-    caches must use the same number."""
-    import bench
-    src = open(os.path.join(ROOT, "decode_attention_gb300", "csrc", "gqa_decode.cu")).read()
-    lib_value = int(re.search(r"kKeqvTcTilesPerCta = (\d+);", src).group(1))
-    test_src = open(os.path.join(ROOT, "tests", "test_gpu_keqv.py")).read()
-    test_value = int(re.search(r"_TC_TILES_PER_CTA = (\d+)", test_src).group(1))
-    assert lib_value == bench.KEQV_TC_TILES_PER_CTA == test_value
+def test_binding_kernel_and_test_mode_codes_match_the_header():
+    text = open(HEADER).read()
+    kernels = dict(re.findall(r"(GQA_KERNEL_[A-Z_0-9]+) = (\d+)", text))
+    assert {k: int(v) for k, v in kernels.items()} == {
+        "GQA_KERNEL_NONE": gqa.GQA_KERNEL_NONE, "GQA_KERNEL_SPLIT_DECODE": gqa.GQA_KERNEL_SPLIT_DECODE,
+        "GQA_KERNEL_TCGEN05": gqa.GQA_KERNEL_TCGEN05}
+    defines = dict(re.findall(r"#define (GQA_TEST_[A-Z_]+) (\d+)u?\b", text))
+    assert int(defines["GQA_TEST_SINGLE_PIECE"]) == gqa.GQA_TEST_SINGLE_PIECE
+    assert int(defines["GQA_TEST_STALL"]) == gqa.GQA_TEST_STALL
+
+
+def test_test_mode_round_trip(lib):
+    assert gqa.gqa_get_test_mode() == 0
+    assert gqa.gqa_set_test_mode(gqa.GQA_TEST_SINGLE_PIECE | 0x80) == 0
+    assert gqa.gqa_get_test_mode() == gqa.GQA_TEST_SINGLE_PIECE   # unknown bits dropped
+    assert gqa.gqa_set_test_mode(0) == gqa.GQA_TEST_SINGLE_PIECE
+    assert gqa.gqa_get_test_mode() == 0
+
+
+def test_keqv_kernel_query_refuses_bad_sizes(lib):
+    # refused before the device is queried
+    assert lib.gqa_decode_keqv_kernel(4, 1024, *SLIDING) == gqa.GQA_KERNEL_NONE
+    assert lib.gqa_decode_keqv_kernel(0, 1024, *GLOBAL) == gqa.GQA_KERNEL_NONE
+    assert lib.gqa_decode_keqv_kernel(4, 0, *GLOBAL) == gqa.GQA_KERNEL_NONE
+    assert lib.gqa_decode_keqv_kernel(4, 262145, *GLOBAL) == gqa.GQA_KERNEL_NONE
 
 
 def test_library_exports_every_declared_symbol(lib):

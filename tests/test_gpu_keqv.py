@@ -19,7 +19,7 @@ import torch
 import decode_attention_gb300 as gqa
 import oracle
 from decode_attention_gb300 import inputs
-from tests.helpers import BF16_NAN, GLOBAL, assert_parity
+from tests.helpers import BF16_NAN, GLOBAL, assert_parity, keqv_tcgen05_capacity
 
 pytestmark = pytest.mark.gpu
 
@@ -28,21 +28,14 @@ if not torch.cuda.is_available():
 
 H, KVH, D = GLOBAL["H"], GLOBAL["KVH"], GLOBAL["D"]
 
-# the capacity (in 128-position tiles per CTA, one CTA per SM) from which the
-# library takes the tcgen05 kernel
-_TC_TILES_PER_CTA = 64
-
 
 def capacity(B, S, roomy):
-    """S, or a roomy capacity: 1.5x the tcgen05 threshold, within the longest cache
-    the library accepts."""
+    """S (the library runs the split-KV kernel there), or a roomy capacity: the
+    smallest one at or above S that the library routes to the tcgen05 kernel."""
     if not roomy:
+        assert gqa.gqa_decode_keqv_kernel(B, S) == gqa.GQA_KERNEL_SPLIT_DECODE
         return S
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    need = -(-_TC_TILES_PER_CTA * sms * 128 // (B * KVH))
-    cap = min(max(S, need * 3 // 2), gqa.GQA_MAX_SEQ)
-    assert cap >= need, "the roomy cache must take the tcgen05 kernel"
-    return cap
+    return keqv_tcgen05_capacity(B, S)
 
 
 def case(lens, S, seed):

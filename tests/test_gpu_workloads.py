@@ -32,6 +32,26 @@ def sampled(lens, k=3, seed=0):
     return sorted(pick)
 
 
+def sampled_paged(lens, seed=0, at_least=16):
+    """At least 16 sequences of a paged batch: the four longest (the global call gives
+    them dynamic chunks), four whose sliding window starts inside a page (L > 1024,
+    L % 16 != 0), the two shortest, two more with L % 16 != 0 below the window, the
+    first and last, and random ones up to the count."""
+    lens = np.asarray(lens)
+    idx = np.arange(len(lens))
+    order = np.argsort(-lens, kind="stable")
+    pick = set(order[:4].tolist()) | set(order[-2:].tolist()) | {0, len(lens) - 1}
+    mid_page = idx[(lens > 1024) & (lens % 16 != 0)]
+    short_ragged = idx[(lens <= 1024) & (lens % 16 != 0)]
+    rng = np.random.default_rng(seed)
+    for group, n in ((mid_page, 4), (short_ragged, 2)):
+        pick |= set(rng.choice(group, size=min(n, len(group)), replace=False).tolist())
+    rest = [i for i in idx.tolist() if i not in pick]
+    need = max(0, at_least - len(pick))
+    pick |= set(rng.choice(rest, size=min(need, len(rest)), replace=False).tolist())
+    return sorted(int(i) for i in pick if lens[i] > 0)
+
+
 @pytest.mark.parametrize("name", WORKLOADS)
 def test_workload_sampled_parity(name):
     wl = inputs.WORKLOADS[name]
@@ -46,7 +66,10 @@ def test_workload_sampled_parity(name):
         torch.cuda.synchronize()
         assert gqa.gqa_device_status() == 0
         assert torch.equal(out16, out32.to(torch.bfloat16))
-        for b in sampled(lens, seed=wl.seed):
+        picks = sampled_paged(lens, seed=wl.seed) if wl.paged else sampled(lens, seed=wl.seed)
+        if wl.paged:
+            assert len(picks) >= 16
+        for b in picks:
             slices = bench.host_slices(c, b)
             ref = bench.oracle_for(c, slices)
             assert_parity(out32[b], ref, f"{name}/{c.name} b={b} L={slices[3]}")

@@ -5,8 +5,10 @@ library's fixed device scratch array instead of a workspace.
 
 The GPU tests call it through the C ABI (ctypes binding) twice in a row and
 compare each result with gqa_decode's on the same inputs, within the parity
-tolerance the other tests use.  This file is collected last, and it needs no
-state from the other tests (it passes alone in a fresh process too).
+tolerance the other tests use, and once with the fp64 oracle.  They also check that
+a call changes neither the device's free memory nor torch's allocator, and that the
+fixed scratch's status word reports a clamped length.  This file is collected last,
+and it needs no state from the other tests (it passes alone in a fresh process too).
 """
 import numpy as np
 import pytest
@@ -14,7 +16,7 @@ import torch
 
 import decode_attention_gb300 as gqa
 from decode_attention_gb300 import inputs
-from tests.helpers import TOL_MAX_ABS, TOL_REL_L2
+from tests.helpers import TOL_MAX_ABS, TOL_REL_L2, assert_parity, oracle_contiguous
 
 needs_gpu = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
 
@@ -60,6 +62,9 @@ def test_matches_gqa_decode_on_two_calls(layer, lens):
         close(out, ref)
         outs.append(out)
     close(outs[1], outs[0])
+    # the fp64 oracle, independently of gqa_decode (the two share their kernels)
+    for b, r in oracle_contiguous(case, geo["window"]).items():
+        assert_parity(outs[1][b], r, f"{layer} b={b} L={lens[b]}")
     # bf16 output through the same scratch: the round-to-nearest-even of the fp32
     # result (bf16 cannot meet the fp32 max-abs gate at |o| ~ 4)
     out16 = torch.empty(ref.shape, dtype=torch.bfloat16, device="cuda")
@@ -104,9 +109,10 @@ def test_decode_global_with_fewer_dynamic_slots():
 @pytest.mark.gpu
 @needs_gpu
 def test_larger_call_after_a_smaller_one():
-    # The scratch layout depends on the call's shape.  A small call leaves split-softmax
-    # partials in the scratch; a larger call after it must still start from clean
-    # per-segment arrival counters (they sit where no call's partials ever go).
+    # The scratch layout depends on the call's shape.  A small call leaves its
+    # split-softmax partials and partial lists in the scratch where a larger call
+    # puts other things; the larger call rewrites every partial list and slot it
+    # reads, so the leftovers must not change its result.
     geo = inputs.geometry("global")
     small = [3000, 4097, 5000]
     c1 = inputs.contiguous_case(len(small), max(small), geo["H"], geo["KVH"], geo["D"], small,
@@ -121,3 +127,46 @@ def test_larger_call_after_a_smaller_one():
     gqa.gqa_decode_noalloc(c2["q"], c2["k"], c2["v"], c2["seq_lens"], 0, out)
     torch.cuda.synchronize()
     close(out, ref)
+
+
+@pytest.mark.gpu
+@needs_gpu
+def test_a_call_allocates_no_device_memory():
+    geo = inputs.geometry("global")
+    lens = [3000, 8192, 17]
+    case = inputs.contiguous_case(len(lens), 8192, geo["H"], geo["KVH"], geo["D"], lens, seed=81,
+                                  device="cuda")
+    out = torch.empty(len(lens), geo["H"], geo["D"], dtype=torch.float32, device="cuda")
+    # the first call loads the kernels (module loading may take device memory)
+    gqa.gqa_decode_noalloc(case["q"], case["k"], case["v"], case["seq_lens"], 0, out)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    stats0 = torch.cuda.memory_stats()
+    for _ in range(3):
+        gqa.gqa_decode_noalloc(case["q"], case["k"], case["v"], case["seq_lens"], 0, out)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    stats1 = torch.cuda.memory_stats()
+    assert free1 == free0, f"device free memory moved by {free0 - free1} bytes"
+    for key in ("allocation.all.allocated", "segment.all.allocated"):
+        assert stats1.get(key, 0) == stats0.get(key, 0), key
+
+
+@pytest.mark.gpu
+@needs_gpu
+def test_status_word_reports_a_clamped_length():
+    geo = inputs.geometry("sliding")
+    B, S = 2, 1024
+    case = inputs.contiguous_case(B, S, geo["H"], geo["KVH"], geo["D"], [S, S], seed=82, device="cuda")
+    out = torch.empty(B, geo["H"], geo["D"], dtype=torch.float32, device="cuda")
+    gqa.gqa_noalloc_status()   # start from a clear word
+    gqa.gqa_decode_noalloc(case["q"], case["k"], case["v"], case["seq_lens"], geo["window"], out)
+    assert gqa.gqa_noalloc_status() == 0
+    bad = torch.tensor([S + 5, S], dtype=torch.int32, device="cuda")   # above the capacity
+    gqa.gqa_decode_noalloc(case["q"], case["k"], case["v"], bad, geo["window"], out)
+    assert gqa.gqa_noalloc_status() == gqa.GQA_DEVICE_BAD_LENGTH
+    # the read cleared the word; the clamped call equals the call at the capacity
+    ref = out.clone()
+    gqa.gqa_decode_noalloc(case["q"], case["k"], case["v"], case["seq_lens"], geo["window"], out)
+    assert gqa.gqa_noalloc_status() == 0
+    assert torch.equal(out, ref)
