@@ -143,11 +143,14 @@ struct PlanSmem {
     int lo[kMaxBatch];               // first attended position
     int n[kMaxBatch];                // attended positions
     int sn[kMaxBatch];               // static head length of each segment of sequence b
-    int dn[kMaxBatch];               // long dynamic chunks of each segment of sequence b
-    int dn1[kMaxBatch];              // short dynamic chunks of each segment of sequence b
-    long long spref[kMaxBatch + 1];  // KVH * sum_{b' < b} st_b' (static tiles, below)
-    int dpref[kMaxBatch + 1];        // KVH * sum_{b' < b} dn_b'
-    int dpref1[kMaxBatch + 1];       // KVH * sum_{b' < b} dn1_b'
+    // (chunk counts and their prefixes are at most kMaxDynUnits; static tiles at most
+    // B KVH 2^18 / 16 < 2^32: narrow types keep the plan within the multi-query kernel's
+    // shared-memory budget)
+    uint16_t dn[kMaxBatch];          // long dynamic chunks of each segment of sequence b
+    uint16_t dn1[kMaxBatch];         // short dynamic chunks of each segment of sequence b
+    uint32_t spref[kMaxBatch + 1];   // KVH * sum_{b' < b} st_b' (static tiles, below)
+    uint16_t dpref[kMaxBatch + 1];   // KVH * sum_{b' < b} dn_b'
+    uint16_t dpref1[kMaxBatch + 1];  // KVH * sum_{b' < b} dn1_b'
     long long n_static;              // Ns: static tiles in total
     int unit;                        // positions per tile: the static head of a segment is
                                      // st_b = ceil(sn_b / unit) tiles, all whole but the last
@@ -463,8 +466,8 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
         const int sn = n[j] - d * c - d1 * c1;
         if (b < B) {
             pl.sn[b] = sn;
-            pl.dn[b] = d;
-            pl.dn1[b] = d1;
+            pl.dn[b] = static_cast<uint16_t>(d);
+            pl.dn1[b] = static_cast<uint16_t>(d1);
         }
         sloc[j] = srun;
         dloc[j] = drun;
@@ -492,16 +495,16 @@ __device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, 
     for (int j = 0; j < kPer; ++j) {
         const int b = lane * kPer + j;
         if (b <= B) {
-            pl.spref[b] = static_cast<long long>(sexcl + sloc[j]);
-            pl.dpref[b] = dexcl + dloc[j];
-            pl.dpref1[b] = d1excl + d1loc[j];
+            pl.spref[b] = sexcl + sloc[j];
+            pl.dpref[b] = static_cast<uint16_t>(dexcl + dloc[j]);
+            pl.dpref1[b] = static_cast<uint16_t>(d1excl + d1loc[j]);
         }
     }
     if (lane == 31) {
         if (B == kMaxBatch) {
             pl.spref[kMaxBatch] = sincl;
-            pl.dpref[kMaxBatch] = dincl;
-            pl.dpref1[kMaxBatch] = d1incl;
+            pl.dpref[kMaxBatch] = static_cast<uint16_t>(dincl);
+            pl.dpref1[kMaxBatch] = static_cast<uint16_t>(d1incl);
         }
         pl.n_static = static_cast<long long>(sincl);
         pl.unit = unit;
@@ -791,7 +794,7 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
             // long chunks followed by its short ones
             const bool is_long = k < pl.n_dyn0;
             const int kk = is_long ? k : k - pl.n_dyn0;
-            const int* pref = is_long ? pl.dpref : pl.dpref1;
+            const uint16_t* pref = is_long ? pl.dpref : pl.dpref1;
             const int b = upper_seq(pref, B, kk);
             const int per = is_long ? pl.dn[b] : pl.dn1[b];
             const int rel = kk - pref[b];

@@ -37,8 +37,9 @@
 // of the tile's scores and head-dim element j of each O^T block; they run the
 // softmax and the epilogue, the two warps of a quarter splitting the query rows
 // (two warps per scheduler hide each other's latencies).  Over a K=V cache, warp 11
-// (lane 0) streams the V blocks from tile descriptors the producer hands it, and the
-// softmax warps also derive the next tile's rotated keys into TMEM.
+// (lane 0) streams the V blocks from tile descriptors the producer hands it, warps
+// 2..5 run the softmax (one per quarter, all query rows) and warps 6..9 derive each
+// tile's rotated keys into TMEM while the softmax of the tile before runs.
 //
 // Where the configuration has two O^T buffers in TMEM, pieces alternate between them: a
 // piece's output is written after the next tile's P has been published, so the softmax
@@ -61,6 +62,8 @@
 
 #include <type_traits>
 
+#include <cuda_fp16.h>
+
 #include "decode_kernel.cuh"
 
 namespace gqa {
@@ -71,10 +74,6 @@ constexpr float kMqTau = 24.0f;                    // rescale threshold, log2 un
 constexpr int kMqPLbo = 144;                       // P core matrices along positions (padded
                                                    // from 128 B so stores hit distinct banks)
 constexpr int kMqPSbo = (kMqTile / 8) * kMqPLbo;   // P 8-row groups: 2304 B
-constexpr int kMqThreads = 352;         // producer, scores, 8 softmax warps, P.V
-constexpr int kMqSoftmaxThreads = 256;
-constexpr int kMqPvWarp = 10;
-constexpr int kMqVWarp = 11;            // K=V: the V producer (a 12th warp)
 constexpr int kMqVq = 8;                // tile descriptors in flight to the V producer
 
 constexpr int tmem_cols_for(int cols) {
@@ -99,48 +98,66 @@ struct MqCfg {
     static constexpr int NMAX = RMAX <= 16 ? 16 : 32;   // mma N bound
     static constexpr int QATOM = NMAX * 128;            // Q rows of one 64-element column block
     static constexpr int QBYTES = NSUB * QATOM;
-    static constexpr int PBYTES = (2 * NMAX / 8) * kMqPSbo;   // P^T: hi rows, then lo rows
+    // P^T rows: the bf16 hi parts in [0, PLO), the lo parts in [PLO, 2 PLO); this is the
+    // P.V mma's N.  Over a K=V cache only the RMAX query rows (and their lo parts) exist.
+    static constexpr int PLO = KEQV ? RMAX : NMAX;
+    static constexpr int PROWS = 2 * PLO;
+    static constexpr int PBYTES = (PROWS / 8) * kMqPSbo;
     static constexpr int TMEM_S = 0;                    // S^T buffers: columns [0, 2 NMAX)
     static constexpr int TMEM_O = 2 * NMAX;             // O^T: OBUFS piece buffers of NB blocks
-    static constexpr int OBUF = NB * 2 * NMAX;          // of 2 NMAX columns (hi part, lo part)
+    static constexpr int OBUF = NB * PROWS;             // of PROWS columns (hi part, lo part)
     // K=V: the derived rotated keys of a tile, the A operand of the rotated k-steps:
     // 128 rows x 128 bf16 (rotated dims i and D/2 + i, i < 64), hi then lo
     static constexpr int TMEM_KROT = TMEM_O + OBUFS * OBUF;
     static constexpr int KROT_COLS = KEQV ? 128 : 0;
-    // K=V: cos and sin of j f_i for tile row j (the TMEM lane) and rotated pair i, fp32:
-    // pair 32 h + k of the thread half h at columns 64 h + 2 k (cos) and 64 h + 2 k + 1
+    // K=V: the key of tile row j (the TMEM lane) on rotated pair i is R(j f_i) (w * v):
+    // per pair group m (pairs i = 2m, 2m + 1), fp32 at columns 8m + t (t = i - 2m):
+    // cos(j f_i) w_i, then at + 2: -sin(j f_i) w_{D/2+i}, + 4: cos(j f_i) w_{D/2+i},
+    // + 6: sin(j f_i) w_i
     static constexpr int TMEM_TRIG = TMEM_KROT + KROT_COLS;
-    static constexpr int TRIG_COLS = KEQV ? 128 : 0;
+    static constexpr int TRIG_COLS = KEQV ? 256 : 0;
+    // Warp roles: 0 producer, 1 scores mma (and TMEM owner), then the softmax warps (8,
+    // two per TMEM lane quarter; over a K=V cache 4, one per quarter), then over a K=V
+    // cache 8 key-deriving warps (two per quarter), then the P.V warp and, over a K=V
+    // cache, the V producer.
+    static constexpr int SMX_WARPS = KEQV ? 4 : 8;
+    static constexpr int SMX_THREADS = 32 * SMX_WARPS;
+    static constexpr int DRV_WARPS = KEQV ? 8 : 0;
+    static constexpr int DRV_THREADS = 32 * DRV_WARPS;
+    static constexpr int PV_WARP = 2 + SMX_WARPS + DRV_WARPS;
     static constexpr int NK = KEQV ? NSUB - 2 : NSUB;   // stages of a K block
     // Over a K=V cache a second producer warp streams the V blocks, so that waits on the
     // V ring (paced by the P.V warp) never hold up the K and R rings.
     static constexpr bool SPLIT_V = KEQV;
-    static constexpr int THREADS = SPLIT_V ? kMqThreads + 32 : kMqThreads;
+    static constexpr int V_WARP = PV_WARP + 1;          // the V producer (SPLIT_V)
+    static constexpr int THREADS = 32 * (PV_WARP + 1 + (SPLIT_V ? 1 : 0));
     static constexpr int TMEM_COLS = tmem_cols_for(TMEM_TRIG + TRIG_COLS);
     static_assert(TMEM_TRIG + TRIG_COLS <= 512, "TMEM holds 512 columns");
     static_assert(OBUFS == 1 || OBUFS == 2, "one or two O^T buffers");
-    static_assert(!KEQV || (D == 512 && G == 8 && MAXT == 1 && RST == 2), "K=V: decodeGQA, one query");
+    static_assert(!KEQV || (D == 512 && G == 8 && MAXT == 1 && RST >= 2 && RST % 2 == 0),
+                  "K=V: decodeGQA, one query, whole tiles of R blocks");
     static_assert(VST % 2 == 0, "a P.V block reads two adjacent stages");
     static_assert(NSUB % 2 == 0 && RMAX <= 32, "geometry");
     // query rows fill the mma N bound; over a K=V cache the scores' B operand holds
     // the hi and the lo parts of q * w as 2 RMAX rows
     static_assert(RMAX == NMAX || (KEQV && 2 * RMAX == NMAX), "query rows fill the mma N bound");
+    static_assert(PROWS % 16 == 0, "the P.V mma's N is a multiple of 16");
 };
 
 using MqGlobal = MqCfg<512, 8, 4, 4, 4, 1>;     // decodeGQA, T <= 4
 using MqGlobal2 = MqCfg<512, 8, 2, 4, 6, 2>;   // decodeGQA, T <= 2: smaller Q and P, more stages
 using MqSliding = MqCfg<256, 2, 8, 4, 6, 2>;   // slidingDecodeGQA, T <= 8
-using MqKeqV = MqCfg<512, 8, 1, 4, 4, 1, true, 2>;   // decodeGQA over a single K=V cache (one
-                                                     // O^T buffer: TMEM holds the rotation factors)
+using MqKeqV = MqCfg<512, 8, 1, 6, 4, 1, true, 2>;   // decodeGQA over a single K=V cache (one
+                                                     // O^T buffer: TMEM holds the rotation factors;
+                                                     // the R ring holds two tiles)
 
-// Rotation data of the K=V key derivation in shared memory (the per-row factors cos and
-// sin of j f_i live in TMEM): per tile, cos and sin of t f_i for the tile's first position t.
+// Rotation data of the K=V key derivation in shared memory (the per-row factors of
+// R(j f_i) live in TMEM): per tile, cos and sin of t f_i for the tile's first position t.
 struct MqRopeTables {
     float2 base[64];
-    float w[128];        // k_norm weight of the rotated dims: w[i], then w[D/2 + i]
-    double freq[64];     // f_i = theta^(-2i/D)
 };
 struct MqNoTables {};
+
 
 struct MqTile {
     int b, kvh;
@@ -157,7 +174,10 @@ constexpr int kMqKindK = 0, kMqKindV = 1, kMqKindDone = 2, kMqKindR = 3, kMqKind
 template <class Cfg>
 struct alignas(1024) MqSmem {
     uint8_t stage[Cfg::STAGES][kMqStageBytes];   // K ring, then V ring: [128 rows][128 B], swizzled
-    uint8_t q[Cfg::QBYTES];                       // [column block][NMAX rows][128 B], swizzled
+    // [column block][NMAX rows][128 B], swizzled.  Over a K=V cache the column blocks of
+    // the rotated dims (0 and NSUB/2) hold R(-t f) q of the current tile instead (f16 hi
+    // rows [0, G), lo rows [G, 2 G)), written per tile by the key-deriving warps
+    uint8_t q[Cfg::QBYTES];
     uint8_t pm[2][Cfg::PBYTES];                   // P^T [buffer], core-matrix layout
     alignas(8) uint64_t full[Cfg::STAGES];
     alignas(8) uint64_t empty[Cfg::STAGES];
@@ -174,6 +194,8 @@ struct alignas(1024) MqSmem {
     int rkind[Cfg::KEQV ? Cfg::RST : 1];       // R ring: an R block or the end-of-work marker
     MqTile rdesc[Cfg::KEQV ? Cfg::RST : 1];    // tile of an R block (its first stage)
     alignas(8) uint64_t krot_full;             // K=V: the derived keys of the next tile are in TMEM
+    alignas(8) uint64_t krot_empty;            // K=V: the rotated mma of the last tile completed
+    alignas(8) uint64_t r_full[2];             // K=V: the rotated mma of tile i (S buffer i % 2) completed
     // K=V: tiles whose V blocks the V producer issues, in order (FIFO from the producer)
     MqTile vq[Cfg::SPLIT_V ? kMqVq : 1];
     alignas(8) uint64_t vq_full[Cfg::SPLIT_V ? kMqVq : 1];
@@ -185,7 +207,7 @@ struct alignas(1024) MqSmem {
                                       // with the last p_full; larger until then)
     PlanSmem plan;
     float red[4][Cfg::NMAX];
-    uint32_t red_bad[8];
+    uint32_t red_bad[Cfg::SMX_WARPS];
     float epi_m[Cfg::NMAX];   // the finished piece whose epilogue is pending: reference max,
     float epi_l[Cfg::NMAX];   // normaliser and bad-page bits per query row
     uint32_t epi_bad;
@@ -228,13 +250,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         ptx::mbar_init(ptx::smem_addr(&sm.q_empty), 1);
         for (int j = 0; j < 2; ++j) {
             ptx::mbar_init(ptx::smem_addr(&sm.s_full[j]), 2);   // mma commit + the tile's descriptor
-            ptx::mbar_init(ptx::smem_addr(&sm.p_full[j]), 8);   // one arrival per softmax warp
+            ptx::mbar_init(ptx::smem_addr(&sm.p_full[j]), Cfg::SMX_WARPS);   // one arrival per softmax warp
             ptx::mbar_init(ptx::smem_addr(&sm.p_empty[j]), 1);
             ptx::mbar_init(ptx::smem_addr(&sm.o_ready[j]), 1);
-            ptx::mbar_init(ptx::smem_addr(&sm.s_empty[j]), 8);   // one arrival per softmax warp
+            ptx::mbar_init(ptx::smem_addr(&sm.s_empty[j]), Cfg::SMX_WARPS);   // one per softmax warp
             ptx::mbar_init(ptx::smem_addr(&sm.drain[j]), 1);
         }
-        ptx::mbar_init(ptx::smem_addr(&sm.krot_full), 8);   // one arrival per softmax warp
+        ptx::mbar_init(ptx::smem_addr(&sm.krot_full), Cfg::KEQV ? Cfg::DRV_WARPS : 1);   // one per key-deriving warp
+        ptx::mbar_init(ptx::smem_addr(&sm.krot_empty), 1);   // the rotated mma's commit
+        ptx::mbar_init(ptx::smem_addr(&sm.r_full[0]), 1);
+        ptx::mbar_init(ptx::smem_addr(&sm.r_full[1]), 1);
         for (int k = 0; k < (Cfg::SPLIT_V ? kMqVq : 0); ++k) {
             ptx::mbar_init(ptx::smem_addr(&sm.vq_full[k]), 1);
             ptx::mbar_init(ptx::smem_addr(&sm.vq_empty[k]), 1);
@@ -301,8 +326,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ============================ producer ============================
         if (lane == 0) {
             const uint64_t policy = ptx::policy_evict_first();
-            // Q rows: the query rows, or over a K=V cache the hi and lo rows of q * w
-            const uint32_t q_bytes = static_cast<uint32_t>(NSUB * (Cfg::KEQV ? 2 * R : R) * 128);
+            // Q rows: the query rows, or over a K=V cache the hi and lo rows of q * w on the
+            // unrotated dims (the rotated dims' blocks hold R(-t f) q, written per tile)
+            const uint32_t q_bytes = static_cast<uint32_t>((Cfg::KEQV ? (NSUB - 2) * 2 * R : NSUB * R) * 128);
             constexpr uint32_t kPageBytes = kPageRows * 128;
             uint32_t kseq = 0, vseq = 0, rseq = 0;   // stages issued on the K, V and R rings
             uint32_t vpush = 0;                      // K=V: tiles handed to the V producer
@@ -325,6 +351,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     for (int c = 0; c < NSUB; ++c) {
                         // (elements, rows, ...): the q rows of the KV head's group, or the
                         // K=V scores operand [B, KVH, 2 G, D] of the segment
+                        if (Cfg::KEQV && (c == 0 || c == NSUB / 2)) continue;
                         if (Cfg::KEQV)
                             ptx::tma_load_4d(qdst + c * Cfg::QATOM, &tm_q, q_bar, 64 * c, 0, q_kvh, q_b, policy);
                         else
@@ -511,7 +538,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (k >= pl.n_dyn) break;
                 const bool is_long = k < pl.n_dyn0;
                 const int kk = is_long ? k : k - pl.n_dyn0;
-                const int* pref = is_long ? pl.dpref : pl.dpref1;
+                const uint16_t* pref = is_long ? pl.dpref : pl.dpref1;
                 const int b = upper_seq(pref, B, kk);
                 const int per = is_long ? pl.dn[b] : pl.dn1[b];
                 const int rel = kk - pref[b];
@@ -608,27 +635,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 ++seq;
             }
             if (!ok) break;
-            if constexpr (Cfg::KEQV) {
-                // rotated dims: A = the keys derived into TMEM (hi, then lo), B = the raw q in
-                // rows [0, G) of column blocks 0 and NSUB/2 (rows [G, 2 G) are zero there)
-                if (!__all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&sm.krot_full), i & 1u,
-                                                          &sm.abort_flag, p.ws_flags)))
-                    break;
-                ptx::tc_fence_after();
-                if (lane == 0) {
-#pragma unroll
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t a_t = tmem + Cfg::TMEM_KROT + part * 64 + kk * 8;
-                            const uint64_t bq = ptx::smem_desc(
-                                qbase + (kk < 4 ? 0 : NSUB / 2) * Cfg::QATOM + (kk & 3) * 32, 16, 1024,
-                                ptx::kSwizzle128B);
-                            ptx::umma_ts(s_col, a_t, bq, idesc_s, 1u);
-                        }
-                }
-                __syncwarp();
-            }
+            // (over a K=V cache the rotated dims are added by a softmax thread once the
+            // keys are derived, so this warp moves on to the next tile's K block)
             if (lane == 0) {
                 if (d.flags & kDescLast) ptx::umma_commit(ptx::smem_addr(&sm.q_empty));
                 ptx::umma_commit(ptx::smem_addr(&sm.s_full[i & 1u]));
@@ -643,11 +651,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             wait_drain(ptx::smem_addr(&sm.drain[0]), 0u);
         }
         __syncwarp();
-    } else if (warp == kMqPvWarp) {
+    } else if (warp == Cfg::PV_WARP) {
         // ========= P.V: O^T[d, r] += V^T[d, pos] P^T[pos, r] (lane 0 issues) + V fix-up =========
-        // P^T holds the bf16 hi parts in rows [0, NMAX) and the lo parts in rows
-        // [NMAX, 2 NMAX): one mma applies P to ~16 significant bits.
-        const uint32_t idesc_o = ptx::idesc_bf16_f32(kMqTile, 2 * NMAX, 1, 0);
+        // P^T holds the bf16 hi parts in rows [0, PLO) and the lo parts in rows
+        // [PLO, 2 PLO): one mma applies P to ~16 significant bits.
+        const uint32_t idesc_o = ptx::idesc_bf16_f32(kMqTile, Cfg::PROWS, 1, 0);
         for (uint32_t i = 0;; ++i) {
             if (!__all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&sm.p_full[i & 1u]), (i >> 1) & 1u,
                                                       &sm.abort_flag, p.ws_flags)))
@@ -683,7 +691,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 ptx::tc_fence_after();
                 if (lane == 0) {
                     const uint32_t a0 = stage0 + s * kMqStageBytes;
-                    const uint32_t o_col = tmem + Cfg::TMEM_O + d.ob * Cfg::OBUF + mb * 2 * NMAX;
+                    const uint32_t o_col = tmem + Cfg::TMEM_O + d.ob * Cfg::OBUF + mb * Cfg::PROWS;
 #pragma unroll
                     for (int kk = 0; kk < kMqTile / 16; ++kk) {
                         const uint64_t a = ptx::smem_desc(a0 + kk * 2048, kMqStageBytes, 1024,
@@ -710,7 +718,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             wait_drain(ptx::smem_addr(&sm.drain[1]), 0u);
         }
         __syncwarp();
-    } else if (Cfg::SPLIT_V && warp == kMqVWarp) {
+    } else if (Cfg::SPLIT_V && warp == Cfg::V_WARP) {
         // ========== K=V: V producer, tile i's V blocks in tile order (lane 0) ==========
         // The tiles come from the producer through the descriptor FIFO.
         if (lane == 0) {
@@ -759,18 +767,200 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
         }
         __syncwarp();
+    } else if (Cfg::KEQV && warp >= 2 + Cfg::SMX_WARPS) {
+        // ======= K=V: key derivation (warps 6..13, two per TMEM lane quarter) =======
+        // Thread j of lane quarter q owns TMEM lane j = tile row j, the two warps of a
+        // quarter halves h of its 64 rotated pairs.  For tile i (first
+        // position t) the keys on the rotated dims are rope(w * v, t + j): pair i of the
+        // row rotated by (t + j) f_i.  R((t + j) f) = R(t f) R(j f), and
+        // <q, R(t f) y> = <R(-t f) q, y>, so the keys here are R(j f) (w * v), with factors
+        // that do not depend on the tile (TRIG columns, set once per CTA), and the scores'
+        // B operand on those dims is R(-t f) q, rotated once per tile (8 heads x 64 pairs).
+        // Both are written as f16 hi + lo parts (~22 significant bits each; |values| stay
+        // far below the f16 range), so the rotated dims lose nothing to the split.
+        if constexpr (Cfg::KEQV) {
+            constexpr int kDThreads = Cfg::DRV_THREADS;
+            const int q4 = warp & 3;
+            const int h = (warp - 2 - Cfg::SMX_WARPS) >> 2;   // half of the pairs
+            const int j = 32 * q4 + lane;
+            const int did = tid - 64 - Cfg::SMX_THREADS;   // 0 .. kDThreads - 1
+            const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+            // the factors of row j: cos and sin of j f_i (|j f_i| < 128) times the k_norm
+            // weights of the pair's two dims
+            {
+#pragma unroll 1
+                for (int c16 = 8 * h; c16 < 8 * h + 8; ++c16) {   // 16 columns = 2 pair groups
+                    uint32_t cols[16];
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            const int i = 4 * c16 + 2 * g + t;
+                            float sn, cs;
+                            sincosf(static_cast<float>(static_cast<double>(j) * p.rope_freq[i]), &sn, &cs);
+                            const float wa = __bfloat162float(p.w_k[i]);
+                            const float wb = __bfloat162float(p.w_k[D / 2 + i]);
+                            cols[8 * g + t] = __float_as_uint(cs * wa);
+                            cols[8 * g + 2 + t] = __float_as_uint(-sn * wb);
+                            cols[8 * g + 4 + t] = __float_as_uint(cs * wb);
+                            cols[8 * g + 6 + t] = __float_as_uint(sn * wa);
+                        }
+                    }
+                    ptx::tmem_st16(lane_addr + Cfg::TMEM_TRIG + 16 * c16, cols);
+                }
+                ptx::tmem_wait_st();
+            }
+            // R(-t f) q: thread did takes head r = did / 32 and pairs [2 (did % 32), + 2)
+            const int qr = did >> 5;
+            const int qp = (did & 31) * 2;
+            float qa[2] = {0.f, 0.f}, qb[2] = {0.f, 0.f};
+            int seg_b = -1, seg_kvh = -1;
+            const uint32_t qrot = ptx::smem_addr(&sm.q[0]);   // column blocks 0 and NSUB/2
+            // byte offset of elements [qp, qp + 2) of row rr in a swizzled column block
+            auto qrot_off = [&](int rr) -> uint32_t {
+                return static_cast<uint32_t>((rr >> 3) * 1024 + (rr & 7) * 128 +
+                                             ((((qp >> 3) ^ (rr & 7)) << 4) | ((qp & 7) * 2)));
+            };
+            ptx::named_barrier_sync(4, kDThreads);
+            for (uint32_t ti = 0;; ++ti) {
+                const uint32_t q0 = 2u * ti;
+                // the tile's two R stages, and the keys' TMEM and the q buffer free (the
+                // rotated mma of the previous tile completed)
+                const bool okd =
+                    wait_bounded(ptx::smem_addr(&sm.full[rstg(q0)]), (q0 / RST1) & 1u, &sm.abort_flag,
+                                 p.ws_flags) &&
+                    wait_bounded(ptx::smem_addr(&sm.full[rstg(q0 + 1)]), ((q0 + 1) / RST1) & 1u,
+                                 &sm.abort_flag, p.ws_flags) &&
+                    wait_bounded(ptx::smem_addr(&sm.krot_empty), (ti & 1u) ^ 1u, &sm.abort_flag,
+                                 p.ws_flags);
+                if (ptx::named_barrier_or(4, kDThreads, !okd)) break;
+                ptx::tc_fence_after();
+                const int rs = rstg(q0) - KST - VST;
+                if (sm.rkind[rs] == kMqKindDoneR) break;
+                const MqTile d = sm.rdesc[rs];
+                if (d.b != seg_b || d.kvh != seg_kvh) {
+                    // a new segment: this thread's q values of the rotated dims
+                    seg_b = d.b;
+                    seg_kvh = d.kvh;
+                    const __nv_bfloat16* qrow =
+                        p.q + (static_cast<size_t>(d.b) * H + d.kvh * G + qr) * D + qp;
+                    const uint32_t xa = *reinterpret_cast<const uint32_t*>(qrow);
+                    const uint32_t xb = *reinterpret_cast<const uint32_t*>(qrow + D / 2);
+                    qa[0] = bf16lo(xa);
+                    qa[1] = bf16hi(xa);
+                    qb[0] = bf16lo(xb);
+                    qb[1] = bf16hi(xb);
+                }
+                // cos, sin of t f_i: the angle reaches 2.6e5 rad, so it is reduced mod 2 pi
+                // in fp64 before sincosf
+                if (did < 64) {
+                    const double ang = static_cast<double>(d.t) * p.rope_freq[did];
+                    const double turns = rint(ang * 0.15915494309189535);   // 1 / (2 pi)
+                    const double rr = fma(-turns, 6.283185307179586, ang);
+                    float sn, cs;
+                    sincosf(static_cast<float>(rr), &sn, &cs);
+                    sm.rope.base[did] = make_float2(cs, sn);
+                }
+                ptx::named_barrier_sync(5, kDThreads);
+                // R(-t f) q: (a, b) -> (a cos + b sin, b cos - a sin); f16 hi rows [0, G),
+                // lo rows [G, 2 G); block 0 holds dims i, block 1 dims D/2 + i
+                {
+                    float ra[2], rb[2];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const float2 cs = sm.rope.base[qp + t];
+                        ra[t] = qa[t] * cs.x + qb[t] * cs.y;
+                        rb[t] = qb[t] * cs.x - qa[t] * cs.y;
+                    }
+                    const __half2 h0 = __floats2half2_rn(ra[0], ra[1]);
+                    const __half2 h1 = __floats2half2_rn(rb[0], rb[1]);
+                    const __half2 l0 = __floats2half2_rn(ra[0] - __low2float(h0), ra[1] - __high2float(h0));
+                    const __half2 l1 = __floats2half2_rn(rb[0] - __low2float(h1), rb[1] - __high2float(h1));
+                    constexpr uint32_t kYBlock = (NSUB / 2) * Cfg::QATOM;
+                    ptx::sts32(qrot + qrot_off(qr), *reinterpret_cast<const uint32_t*>(&h0));
+                    ptx::sts32(qrot + kYBlock + qrot_off(qr), *reinterpret_cast<const uint32_t*>(&h1));
+                    ptx::sts32(qrot + qrot_off(G + qr), *reinterpret_cast<const uint32_t*>(&l0));
+                    ptx::sts32(qrot + kYBlock + qrot_off(G + qr), *reinterpret_cast<const uint32_t*>(&l1));
+                }
+                // the keys of row j: y = R(j f) (w * v) per pair, as packed fp32 pairs of
+                // adjacent pairs (2m, 2m + 1):
+                //   y_a = (cos w_a) v_a + (-sin w_b) v_b,  y_b = (cos w_b) v_b + (sin w_a) v_a
+                const uint32_t sx = stage0 + rstg(q0) * kMqStageBytes;       // dims [0, 64)
+                const uint32_t sy = stage0 + rstg(q0 + 1) * kMqStageBytes;   // dims [D/2, D/2 + 64)
+                const uint32_t rowoff = (j >> 3) * 1024 + (j & 7) * 128;
+                {   // this warp's half of the pairs: [32 h, 32 h + 32)
+                    uint32_t hx[16], hy[16], lx[16], ly[16];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {   // pairs 32 h + 8 u .. + 8
+                        uint32_t f[32];
+                        const uint32_t tcol = lane_addr + Cfg::TMEM_TRIG + 4 * (32 * h + 8 * u);
+                        ptx::tmem_ld16(tcol, *reinterpret_cast<uint32_t(*)[16]>(&f[0]));
+                        ptx::tmem_ld16(tcol + 16, *reinterpret_cast<uint32_t(*)[16]>(&f[16]));
+                        const uint32_t unit = static_cast<uint32_t>(((4 * h + u) ^ (j & 7)) << 4);
+                        const uint4 vx4 = ptx::lds128(sx + rowoff + unit);
+                        const uint4 vy4 = ptx::lds128(sy + rowoff + unit);
+                        ptx::tmem_wait_ld();
+                        const uint32_t vx[4] = {vx4.x, vx4.y, vx4.z, vx4.w};
+                        const uint32_t vy[4] = {vy4.x, vy4.y, vy4.z, vy4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {   // pair group 16 h + 4 u + e
+                            const uint32_t* c = &f[8 * e];
+                            const uint64_t va = ptx::f2_from_bf16x2(vx[e]);
+                            const uint64_t vb = ptx::f2_from_bf16x2(vy[e]);
+                            const uint64_t ya = ptx::f2_fma(ptx::f2_pack(__uint_as_float(c[0]), __uint_as_float(c[1])), va,
+                                                            ptx::f2_mul(ptx::f2_pack(__uint_as_float(c[2]), __uint_as_float(c[3])), vb));
+                            const uint64_t yb = ptx::f2_fma(ptx::f2_pack(__uint_as_float(c[4]), __uint_as_float(c[5])), vb,
+                                                            ptx::f2_mul(ptx::f2_pack(__uint_as_float(c[6]), __uint_as_float(c[7])), va));
+                            // f16 hi + lo parts
+                            const float2 fa = ptx::f2_unpack(ya), fb = ptx::f2_unpack(yb);
+                            const __half2 h0 = __floats2half2_rn(fa.x, fa.y);
+                            const __half2 h1 = __floats2half2_rn(fb.x, fb.y);
+                            const float2 g0 = __half22float2(h0), g1 = __half22float2(h1);
+                            const float2 ra = ptx::f2_unpack(ptx::f2_sub(ya, ptx::f2_pack(g0.x, g0.y)));
+                            const float2 rb = ptx::f2_unpack(ptx::f2_sub(yb, ptx::f2_pack(g1.x, g1.y)));
+                            const __half2 l0 = __floats2half2_rn(ra.x, ra.y);
+                            const __half2 l1 = __floats2half2_rn(rb.x, rb.y);
+                            hx[4 * u + e] = *reinterpret_cast<const uint32_t*>(&h0);
+                            hy[4 * u + e] = *reinterpret_cast<const uint32_t*>(&h1);
+                            lx[4 * u + e] = *reinterpret_cast<const uint32_t*>(&l0);
+                            ly[4 * u + e] = *reinterpret_cast<const uint32_t*>(&l1);
+                        }
+                    }
+                    // columns: dims i (x) at i / 2, dims D/2 + i (y) at 32 + i / 2; lo parts 64 later
+                    const uint32_t kb = lane_addr + Cfg::TMEM_KROT + 16 * h;
+                    ptx::tmem_st16(kb, hx);
+                    ptx::tmem_st16(kb + 32, hy);
+                    ptx::tmem_st16(kb + 64, lx);
+                    ptx::tmem_st16(kb + 96, ly);
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::fence_proxy_async_smem();   // R(-t f) q is read by the tensor core
+                // every thread is done with the R stages and the angle table, and has
+                // stored its keys and its part of R(-t f) q
+                ptx::named_barrier_sync(5, kDThreads);
+                if (did == 0) {
+                    ptx::mbar_arrive(ptx::smem_addr(&sm.empty[rstg(q0)]));
+                    ptx::mbar_arrive(ptx::smem_addr(&sm.empty[rstg(q0 + 1)]));
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.krot_full));
+            }
+        }
     } else {
-        // ================ softmax and epilogue (warps 2..9, two per TMEM lane quarter) ================
+        // ================ softmax and epilogue (warps 2..9, two per TMEM lane quarter;
+        // over a K=V cache warps 2..5, one per quarter) ================
         // Thread j of lane quarter q (warp % 4) owns TMEM lane j: position j of the
-        // tile's scores and head-dim element j of each O^T block.  The two warps of a
-        // quarter split the query rows: warps 2..5 rows [0, RH), warps 6..9 [RH, 2 RH).
-        // rows per warp; over a K=V cache the G query rows' scores are the sum of a hi
-        // column r and a lo column G + r
-        constexpr int RH = Cfg::KEQV ? Cfg::RMAX / 2 : NMAX / 2;
+        // tile's scores and head-dim element j of each O^T block.  Where two warps share
+        // a quarter they split the query rows: warps 2..5 rows [0, RH), warps 6..9
+        // [RH, 2 RH).  Over a K=V cache the G query rows' scores are the sum of a hi
+        // column r and a lo column G + r.
+        constexpr int RH = Cfg::KEQV ? Cfg::RMAX : NMAX / 2;   // rows per warp
+        constexpr int kSmx = Cfg::SMX_THREADS;
         const int q4 = warp & 3;
-        const int r0 = ((warp - 2) >> 2) * RH;      // first row of this warp
+        const int r0 = Cfg::KEQV ? 0 : ((warp - 2) >> 2) * RH;   // first row of this warp
         const int j = 32 * q4 + lane;
-        const int sid = tid - 64;                    // 0 .. 255 over the softmax warps
+        const int sid = tid - 64;                    // 0 .. kSmx - 1 over the softmax warps
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         const float nan = __uint_as_float(0x7fc00000u);
         float m_ref[RH], l_part[RH];
@@ -780,132 +970,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             l_part[k] = 0.0f;
         }
         uint32_t bad_q = 0;   // bit t: query t attended a bad page in this piece
-        // P rows past the query rows in use stay zero (the P.V mma reads 2 NMAX rows)
-        for (int i = sid; i < 2 * Cfg::PBYTES / 16; i += kMqSoftmaxThreads)
+        // P rows past the query rows in use stay zero (the P.V mma reads PROWS rows)
+        for (int i = sid; i < 2 * Cfg::PBYTES / 16; i += kSmx)
             ptx::sts128(ptx::smem_addr(&sm.pm[0][0]) + i * 16, 0u, 0u, 0u, 0u);
-        ptx::named_barrier_sync(3, kMqSoftmaxThreads);
-        // K=V: derives tile ti's rotated keys rope(w * v, t + j) into TMEM (the A operand of
-        // the scores' rotated k-steps) from the R ring; 1 when done, 0 when there is no
-        // tile ti, -1 when the CTA is aborting.  Thread j (two per row, halves h of the
-        // 64 rotated pairs) takes the pairs [32 h, 32 h + 32) of row j.
-        auto derive = [&](uint32_t ti) -> int {
-            if constexpr (Cfg::KEQV) {
-                const uint32_t q0 = 2u * ti;
-                const bool okd =
-                    wait_bounded(ptx::smem_addr(&sm.full[rstg(q0)]), (q0 / RST1) & 1u, &sm.abort_flag,
-                                 p.ws_flags) &&
-                    wait_bounded(ptx::smem_addr(&sm.full[rstg(q0 + 1)]), ((q0 + 1) / RST1) & 1u,
-                                 &sm.abort_flag, p.ws_flags);
-                if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !okd)) return -1;
-                const int rs = rstg(q0) - KST - VST;
-                if (sm.rkind[rs] == kMqKindDoneR) return 0;
-                const int t0 = sm.rdesc[rs].t;
-                // cos, sin of t0 f_i: the angle reaches 2.6e5 rad, so it is reduced mod
-                // 2 pi in fp64 before sincosf; (t0 + j) f_i by the angle sum below
-                if (sid < 64) {
-                    const double ang = static_cast<double>(t0) * sm.rope.freq[sid];
-                    const double turns = rint(ang * 0.15915494309189535);   // 1 / (2 pi)
-                    const double rr = fma(-turns, 6.283185307179586, ang);
-                    float sn, cs;
-                    sincosf(static_cast<float>(rr), &sn, &cs);
-                    sm.rope.base[sid] = make_float2(cs, sn);
-                }
-                ptx::named_barrier_sync(3, kMqSoftmaxThreads);
-                const int h = (warp - 2) >> 2;
-                const uint32_t sx = stage0 + rstg(q0) * kMqStageBytes;       // dims [0, 64)
-                const uint32_t sy = stage0 + rstg(q0 + 1) * kMqStageBytes;   // dims [D/2, D/2 + 64)
-                const uint32_t rowoff = (j >> 3) * 1024 + (j & 7) * 128;
-                uint32_t hx[16], hy[16], lx[16], ly[16];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    // cos, sin of j f_i for this row's pairs 32 h + 8 u .. + 8
-                    uint32_t cj[16];
-                    ptx::tmem_ld16(lane_addr + Cfg::TMEM_TRIG + 64 * h + 16 * u, cj);
-                    ptx::tmem_wait_ld();
-                    const uint32_t unit = static_cast<uint32_t>(((4 * h + u) ^ (j & 7)) << 4);
-                    const uint4 vx4 = ptx::lds128(sx + rowoff + unit);
-                    const uint4 vy4 = ptx::lds128(sy + rowoff + unit);
-                    const uint32_t vx[4] = {vx4.x, vx4.y, vx4.z, vx4.w};
-                    const uint32_t vy[4] = {vy4.x, vy4.y, vy4.z, vy4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float k0[2], k1[2];
-#pragma unroll
-                        for (int tt = 0; tt < 2; ++tt) {
-                            const int ii = 32 * h + 8 * u + 2 * e + tt;
-                            const float2 tb = sm.rope.base[ii];
-                            const float fc = __uint_as_float(cj[2 * (2 * e + tt)]);
-                            const float fs = __uint_as_float(cj[2 * (2 * e + tt) + 1]);
-                            const float c = tb.x * fc - tb.y * fs;    // cos((t0 + j) f_i)
-                            const float sn = tb.y * fc + tb.x * fs;   // sin((t0 + j) f_i)
-                            const float x = sm.rope.w[ii] * (tt ? bf16hi(vx[e]) : bf16lo(vx[e]));
-                            const float y = sm.rope.w[64 + ii] * (tt ? bf16hi(vy[e]) : bf16lo(vy[e]));
-                            k0[tt] = x * c - y * sn;
-                            k1[tt] = y * c + x * sn;
-                        }
-                        const __nv_bfloat162 h0 = __floats2bfloat162_rn(k0[0], k0[1]);
-                        const __nv_bfloat162 h1 = __floats2bfloat162_rn(k1[0], k1[1]);
-                        const __nv_bfloat162 l0 =
-                            __floats2bfloat162_rn(k0[0] - __low2float(h0), k0[1] - __high2float(h0));
-                        const __nv_bfloat162 l1 =
-                            __floats2bfloat162_rn(k1[0] - __low2float(h1), k1[1] - __high2float(h1));
-                        hx[4 * u + e] = *reinterpret_cast<const uint32_t*>(&h0);
-                        hy[4 * u + e] = *reinterpret_cast<const uint32_t*>(&h1);
-                        lx[4 * u + e] = *reinterpret_cast<const uint32_t*>(&l0);
-                        ly[4 * u + e] = *reinterpret_cast<const uint32_t*>(&l1);
-                    }
-                }
-                // columns: dims i (x) at i / 2, dims D/2 + i (y) at 32 + i / 2; lo parts 64 later
-                const uint32_t kb = lane_addr + Cfg::TMEM_KROT + 16 * h;
-                ptx::tmem_st16(kb, hx);
-                ptx::tmem_st16(kb + 32, hy);
-                ptx::tmem_st16(kb + 64, lx);
-                ptx::tmem_st16(kb + 96, ly);
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                // every thread is done with the R stages and has stored its keys
-                ptx::named_barrier_sync(3, kMqSoftmaxThreads);
-                if (sid == 0) {
-                    ptx::mbar_arrive(ptx::smem_addr(&sm.empty[rstg(q0)]));
-                    ptx::mbar_arrive(ptx::smem_addr(&sm.empty[rstg(q0 + 1)]));
-                }
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.krot_full));
-                return 1;
-            } else {
-                (void)ti;
-                return 0;
-            }
-        };
-        bool derive_more = Cfg::KEQV;   // K=V: tiles still to derive
-        if constexpr (Cfg::KEQV) {
-            // f_i and the weights of the rotated dims; cos and sin of j f_i for this
-            // thread's row j and pairs [32 h, 32 h + 32) into TMEM (|j f_i| < 128)
-            for (int e = sid; e < 64; e += kMqSoftmaxThreads) sm.rope.freq[e] = p.rope_freq[e];
-            for (int e = sid; e < 128; e += kMqSoftmaxThreads)
-                sm.rope.w[e] = __bfloat162float(p.w_k[(e >> 6) * (D / 2) + (e & 63)]);
-            {
-                const int h = (warp - 2) >> 2;
-#pragma unroll 1
-                for (int u = 0; u < 4; ++u) {
-                    uint32_t cj[16];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float sn, cs;
-                        sincosf(static_cast<float>(static_cast<double>(j) * p.rope_freq[32 * h + 8 * u + k]),
-                                &sn, &cs);
-                        cj[2 * k] = __float_as_uint(cs);
-                        cj[2 * k + 1] = __float_as_uint(sn);
-                    }
-                    ptx::tmem_st16(lane_addr + Cfg::TMEM_TRIG + 64 * h + 16 * u, cj);
-                }
-                ptx::tmem_wait_st();
-            }
-            ptx::named_barrier_sync(3, kMqSoftmaxThreads);
-            const int dr = derive(0u);
-            derive_more = dr == 1;
-            if (dr < 0) derive_more = false;
-        }
+        ptx::named_barrier_sync(3, kSmx);
         // A finished piece whose output is still to be written: its last tile and
         // that tile's index; its reference max, normaliser and bad bits are in smem.
         bool epi_pending = false;
@@ -918,7 +986,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         auto finish_piece = [&]() -> bool {
             const bool okw = wait_bounded(ptx::smem_addr(&sm.o_ready[epi_i & 1u]), (epi_i >> 1) & 1u,
                                           &sm.abort_flag, p.ws_flags);
-            if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !okw)) return false;
+            if (ptx::named_barrier_or(1, kSmx, !okw)) return false;
             ptx::tc_fence_after();
             const uint32_t bad_all = sm.epi_bad;
             const SegmentParts sp(pl, epi.b, epi.kvh, p.dyn_slot_base);
@@ -926,11 +994,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (r0 < R) {
 #pragma unroll
                 for (int mb = 0; mb < NB; ++mb) {
-                    // row r's sum is its hi column r plus its lo column NMAX + r
+                    // row r's sum is its hi column r plus its lo column PLO + r
                     uint32_t oh[RH], ol[RH];
-                    const uint32_t ob = lane_addr + Cfg::TMEM_O + epi.ob * Cfg::OBUF + mb * 2 * NMAX + r0;
+                    const uint32_t ob = lane_addr + Cfg::TMEM_O + epi.ob * Cfg::OBUF + mb * Cfg::PROWS + r0;
                     ptx::tmem_ld<RH>(ob, oh);
-                    ptx::tmem_ld<RH>(ob + NMAX, ol);
+                    ptx::tmem_ld<RH>(ob + Cfg::PLO, ol);
                     ptx::tmem_wait_ld();
 #pragma unroll
                     for (int k = 0; k < RH; ++k) {
@@ -963,7 +1031,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (uint32_t i = 0;; ++i) {
             bool ok = wait_bounded(ptx::smem_addr(&sm.s_full[i & 1u]), (i >> 1) & 1u, &sm.abort_flag,
                                    p.ws_flags);
-            if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
+            if (ptx::named_barrier_or(1, kSmx, !ok)) break;
             ptx::tc_fence_after();
             const MqTile d = sm.s_desc[i & 1u];
             if (d.flags & kDescDone) {
@@ -972,11 +1040,45 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // i - 2, so p_full[i % 2] never runs two phases ahead of it.
                 ok = wait_bounded(ptx::smem_addr(&sm.p_empty[i & 1u]), ((i >> 1) & 1u) ^ 1u,
                                   &sm.abort_flag, p.ws_flags);
-                if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
+                if (ptx::named_barrier_or(1, kSmx, !ok)) break;
                 if (sid == 0) sm.pv_stop = static_cast<int>(i);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.p_full[i & 1u]));
                 break;
+            }
+            if constexpr (Cfg::KEQV) {
+                // The rotated dims of tile i: A = the keys R(j f) (w * v) derived into TMEM
+                // (hi, then lo), B = R(-t f) q of the tile in the Q buffer's column blocks 0
+                // and NSUB/2 (hi rows [0, G), lo rows [G, 2 G)), all f16.  One thread adds
+                // them to S once the keys are derived; the unrotated part is complete.
+                ok = wait_bounded(ptx::smem_addr(&sm.krot_full), i & 1u, &sm.abort_flag, p.ws_flags);
+                if (ptx::named_barrier_or(1, kSmx, !ok)) break;
+                ptx::tc_fence_after();
+                if (sid == 0) {
+                    const uint32_t idesc_r = ptx::idesc_f16_f32(kMqTile, N, 0, 0);
+                    const uint32_t s_col = tmem + Cfg::TMEM_S + (i & 1u) * NMAX;
+                    const uint32_t qbase = ptx::smem_addr(&sm.q[0]);
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t a_t = tmem + Cfg::TMEM_KROT + part * 64 + kk * 8;
+                            const uint64_t bq = ptx::smem_desc(
+                                qbase + (kk < 4 ? 0 : NSUB / 2) * Cfg::QATOM + (kk & 3) * 32, 16, 1024,
+                                ptx::kSwizzle128B);
+                            ptx::umma_ts(s_col, a_t, bq, idesc_r, 1u);
+                        }
+                    // the keys and R(-t f) q may be overwritten with the next tile's
+                    ptx::umma_commit(ptx::smem_addr(&sm.krot_empty));
+                    ptx::umma_commit(ptx::smem_addr(&sm.r_full[i & 1u]));
+                    // the issuer sees its mma complete even when the CTA is aborting (TMEM
+                    // is released only after every mma has completed)
+                    wait_drain(ptx::smem_addr(&sm.r_full[i & 1u]), (i >> 1) & 1u);
+                }
+                ok = wait_bounded(ptx::smem_addr(&sm.r_full[i & 1u]), (i >> 1) & 1u, &sm.abort_flag,
+                                  p.ws_flags);
+                if (ptx::named_barrier_or(1, kSmx, !ok)) break;
+                ptx::tc_fence_after();
             }
             if (d.flags & kDescFirst) {
 #pragma unroll
@@ -1011,12 +1113,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.s_empty[i & 1u]));
-            // K=V: the next tile's rotated keys (its scores can run during this softmax)
-            if (derive_more) {
-                const int dr = derive(i + 1);
-                if (dr < 0) break;
-                derive_more = dr == 1;
-            }
             float s[RH];
             bool need = false;
 #pragma unroll
@@ -1030,7 +1126,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 s[k] = valid ? __uint_as_float(sr[k]) * kLog2e : -INFINITY;
                 need |= s[k] > m_ref[k] + kMqTau;
             }
-            if (ptx::named_barrier_or(2, kMqSoftmaxThreads, need)) {
+            if (ptx::named_barrier_or(2, kSmx, need)) {
                 // new reference max of every row: the tile's max where it is larger
 #pragma unroll
                 for (int k = 0; k < RH; ++k) {
@@ -1039,7 +1135,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
                     if (lane == 0) sm.red[q4][r0 + k] = mx;
                 }
-                ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+                ptx::named_barrier_sync(3, kSmx);
                 float alpha[RH];
 #pragma unroll
                 for (int k = 0; k < RH; ++k) {
@@ -1049,14 +1145,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     alpha[k] = (m_ref[k] == -INFINITY || mn == -INFINITY) ? 0.0f : exp2f(m_ref[k] - mn);
                     m_ref[k] = mn;
                 }
-                ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+                ptx::named_barrier_sync(3, kSmx);
                 if (!(d.flags & kDescFirst)) {
                     // O^T holds the earlier tiles of this piece: rescale it once their
                     // P.V is complete (the P.V of this tile waits for p_full)
                     const uint32_t ip = i - 1;
                     ok = wait_bounded(ptx::smem_addr(&sm.o_ready[ip & 1u]), (ip >> 1) & 1u,
                                       &sm.abort_flag, p.ws_flags);
-                    if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
+                    if (ptx::named_barrier_or(1, kSmx, !ok)) break;
                     ptx::tc_fence_after();
 #pragma unroll
                     for (int mb = 0; mb < NB; ++mb) {
@@ -1065,7 +1161,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         for (int part = 0; part < 2; ++part) {
                             uint32_t o[RH];
                             const uint32_t ta = lane_addr + Cfg::TMEM_O + d.ob * Cfg::OBUF +
-                                                mb * 2 * NMAX + part * NMAX + r0;
+                                                mb * Cfg::PROWS + part * Cfg::PLO + r0;
                             ptx::tmem_ld<RH>(ta, o);
                             ptx::tmem_wait_ld();
 #pragma unroll
@@ -1082,9 +1178,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // P buffer i % 2 is free once the P.V of tile i - 2 is done
             ok = wait_bounded(ptx::smem_addr(&sm.p_empty[i & 1u]), ((i >> 1) & 1u) ^ 1u, &sm.abort_flag,
                               p.ws_flags);
-            if (ptx::named_barrier_or(1, kMqSoftmaxThreads, !ok)) break;
+            if (ptx::named_barrier_or(1, kSmx, !ok)) break;
             if (r0 < N) {
-                // hi part in row r, lo part in row NMAX + r; rows past R stay zero
+                // hi part in row r, lo part in row PLO + r; rows past R stay zero
                 const uint32_t pb = ptx::smem_addr(&sm.pm[i & 1u][0]);
 #pragma unroll
                 for (int k = 0; k < RH; ++k) {
@@ -1093,7 +1189,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const __nv_bfloat16 hb = __float2bfloat16_rn(pv);
                     const __nv_bfloat16 lb = __float2bfloat16_rn(pv - __bfloat162float(hb));
                     ptx::sts16(pb + mq_p_off(r0 + k, j), *reinterpret_cast<const uint16_t*>(&hb));
-                    ptx::sts16(pb + mq_p_off(NMAX + r0 + k, j), *reinterpret_cast<const uint16_t*>(&lb));
+                    ptx::sts16(pb + mq_p_off(Cfg::PLO + r0 + k, j), *reinterpret_cast<const uint16_t*>(&lb));
                 }
             }
             // one O^T buffer: the pending piece's output is read before this new piece's
@@ -1124,7 +1220,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             const uint32_t bq = __reduce_or_sync(0xffffffffu, bad_q);
             if (lane == 0) sm.red_bad[warp - 2] = bq;
-            ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+            ptx::named_barrier_sync(3, kSmx);
             if (sid < NMAX)
                 sm.epi_l[sid] = (sm.red[0][sid] + sm.red[1][sid]) + (sm.red[2][sid] + sm.red[3][sid]);
             if (q4 == 0 && lane < RH) {
@@ -1136,11 +1232,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             if (sid == 0) {
                 uint32_t bad_all = 0;
-                for (int w = 0; w < 8; ++w) bad_all |= sm.red_bad[w];
+                for (int w = 0; w < Cfg::SMX_WARPS; ++w) bad_all |= sm.red_bad[w];
                 sm.epi_bad = bad_all;
                 if (bad_all) atomicOr(p.ws_flags, kFlagBadPage);
             }
-            ptx::named_barrier_sync(3, kMqSoftmaxThreads);
+            ptx::named_barrier_sync(3, kSmx);
             epi = d;
             epi_i = i;
             epi_pending = true;

@@ -62,6 +62,38 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* addr, uint32_
     return old;
 }
 
+// ---- packed fp32 pairs (a b64 register: .x in the low half, .y in the high half) ----
+
+__device__ __forceinline__ uint64_t f2_pack(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+// the two bf16 of a packed pair (low half first), widened to fp32 exactly
+__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t v) {
+    return f2_pack(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -225,6 +257,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same with f16 A and B (both operands of one mma have the same type).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Allocates `ncols` TMEM columns (a power of two >= 32) for this CTA; the whole warp
 // executes it and the base address lands in shared memory at `dst`.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
@@ -348,6 +386,10 @@ __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[n]) 
 
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
 __device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {

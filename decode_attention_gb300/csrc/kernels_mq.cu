@@ -85,6 +85,7 @@ bool encode_keqv_operand_map(CUtensorMap* map, const void* base, int B, int KVH)
 template <class Cfg, bool kPaged>
 cudaError_t launch_mq_impl(const LaunchArgs& a) {
     constexpr size_t kSmem = sizeof(MqSmem<Cfg>) + 1024;   // + alignment slack
+    static_assert(kSmem <= 232448, "227 KB of shared memory per CTA");
     constexpr int kMaxDevices = 64;
     static std::once_flag once[kMaxDevices];
     static cudaError_t attr_err[kMaxDevices];
