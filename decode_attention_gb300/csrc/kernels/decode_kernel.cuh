@@ -221,6 +221,66 @@ struct SegmentParts {
     }
 };
 
+// One piece of a CTA's work: positions [p0, p1) of segment (b, kvh), whose partial
+// goes to workspace slot `slot`; unit_end marks the last piece of the static unit and
+// every dynamic chunk (the producer claims the next chunk one tile before its end).
+struct Piece {
+    int b, kvh, p0, p1, slot;
+    bool unit_end;
+};
+
+// The CTA's pieces in order: the pieces of consecutive segments in its static unit
+// [x, stop) (static tiles of `tile` positions), then dynamic chunks claimed through the
+// counter (a claim may already be in flight in `claimed`, -1 when not).  Fills `pc` and
+// returns true, or returns false when no piece is left.  One call site per producer
+// keeps the producer's code (and its instruction-cache footprint) small.
+__device__ __forceinline__ bool next_piece(const PlanSmem& pl, const DecodeParams& p, int cta,
+                                           int tile, bool dynamic, long long& x, long long stop,
+                                           int& claimed, Piece& pc) {
+    const int B = p.B, KVH = p.KVH;
+    if (x < stop) {
+        const int b = upper_seq(pl.spref, B, x);
+        const int st = static_tiles(pl, b);
+        const long long rel = x - pl.spref[b];
+        const int kvh = static_cast<int>(div_floor(rel, st));
+        const int k0 = static_cast<int>(rel - static_cast<long long>(kvh) * st);
+        const int take = static_cast<int>(stop - x < st - k0 ? stop - x : st - k0);
+        x += take;
+        const int e = k0 + take == st ? pl.sn[b] : (k0 + take) * tile;
+        pc.b = b;
+        pc.kvh = kvh;
+        pc.p0 = pl.lo[b] + k0 * tile;
+        pc.p1 = pl.lo[b] + e;
+        pc.slot = cta + b * KVH + kvh;
+        pc.unit_end = x >= stop;
+        return true;
+    }
+    if (!dynamic) return false;
+    if (claimed < 0) claimed = static_cast<int>(atomicAdd(p.ws_claim, 1u));
+    const int k = claimed;
+    claimed = -1;
+    if (k >= pl.n_dyn) return false;
+    // chunk k: long chunks first, then the short ones; a segment's tail is its long
+    // chunks followed by its short ones
+    const bool is_long = k < pl.n_dyn0;
+    const int kk = is_long ? k : k - pl.n_dyn0;
+    const uint16_t* pref = is_long ? pl.dpref : pl.dpref1;
+    const int b = upper_seq(pref, B, kk);
+    const int per = is_long ? pl.dn[b] : pl.dn1[b];
+    const int rel = kk - pref[b];
+    const int kvh = rel / per;
+    const int idx = rel - kvh * per;
+    const int len = is_long ? pl.c_dyn : pl.c_dyn1;
+    const int local = is_long ? idx : pl.dn[b] + idx;
+    pc.b = b;
+    pc.kvh = kvh;
+    pc.p0 = pl.lo[b] + pl.sn[b] + (is_long ? 0 : pl.dn[b] * pl.c_dyn) + idx * len;
+    pc.p1 = pc.p0 + len;
+    pc.slot = p.dyn_slot_base + pl.dpref[b] + pl.dpref1[b] + kvh * (pl.dn[b] + pl.dn1[b]) + local;
+    pc.unit_end = true;
+    return true;
+}
+
 // What the producer publishes with every stage.
 struct TileDesc {
     int b, kvh;
@@ -770,43 +830,12 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
             return true;
         };
 
-        // ---- the static unit of this CTA: pieces of consecutive static heads ----
+        // ---- the static unit of this CTA, then dynamic chunks ----
         long long x = static_unit_begin(pl, cta);
         const long long stop = static_unit_begin(pl, cta + 1);
-        while (ok && x < stop) {
-            const int b = upper_seq(pl.spref, B, x);
-            const int st = static_tiles(pl, b);
-            const long long rel = x - pl.spref[b];
-            const int kvh = static_cast<int>(div_floor(rel, st));
-            const int k0 = static_cast<int>(rel - static_cast<long long>(kvh) * st);
-            const int take = static_cast<int>(stop - x < st - k0 ? stop - x : st - k0);
-            x += take;
-            const int e = k0 + take == st ? pl.sn[b] : (k0 + take) * TP;
-            ok = emit_piece(b, kvh, pl.lo[b] + k0 * TP, pl.lo[b] + e, cta + b * KVH + kvh, x >= stop);
-        }
-        // ---- dynamic chunks ----
-        while (ok && dynamic) {
-            if (claimed < 0) claimed = static_cast<int>(atomicAdd(p.ws_claim, 1u));
-            const int k = claimed;
-            claimed = -1;
-            if (k >= pl.n_dyn) break;
-            // chunk k: long chunks first, then the short ones; a segment's tail is its
-            // long chunks followed by its short ones
-            const bool is_long = k < pl.n_dyn0;
-            const int kk = is_long ? k : k - pl.n_dyn0;
-            const uint16_t* pref = is_long ? pl.dpref : pl.dpref1;
-            const int b = upper_seq(pref, B, kk);
-            const int per = is_long ? pl.dn[b] : pl.dn1[b];
-            const int rel = kk - pref[b];
-            const int kvh = rel / per;
-            const int idx = rel - kvh * per;
-            const int len = is_long ? pl.c_dyn : pl.c_dyn1;
-            const int local = is_long ? idx : pl.dn[b] + idx;
-            const int p0 = pl.lo[b] + pl.sn[b] + (is_long ? 0 : pl.dn[b] * pl.c_dyn) + idx * len;
-            const int slot = p.dyn_slot_base + pl.dpref[b] + pl.dpref1[b] +
-                             kvh * (pl.dn[b] + pl.dn1[b]) + local;
-            ok = emit_piece(b, kvh, p0, p0 + len, slot, true);
-        }
+        Piece pc;
+        while (ok && next_piece(pl, p, cta, TP, dynamic, x, stop, claimed, pc))
+            ok = emit_piece(pc.b, pc.kvh, pc.p0, pc.p1, pc.slot, pc.unit_end);
         if (ok) {
             // end-of-work descriptor (a plain arrival, no bytes)
             const int s = t_idx % STAGES;

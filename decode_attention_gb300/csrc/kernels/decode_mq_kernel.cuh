@@ -460,8 +460,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 return true;
             };
             // Tiles arrive in order.  Multi-query: K(i), then V(i - 1).  K=V: K(i - 1) and
-            // tile i - 1 to the V producer, then R(i) one tile ahead (the softmax warps
-            // derive tile i's rotated keys while tile i - 1's scores are read).  K goes
+            // tile i - 1 to the V producer, then R(i) one tile ahead (the key-deriving warps
+            // derive tile i's rotated keys while tile i - 1's scores are computed).  K goes
             // first: R(i) waits for the derivation of tile i - 1 to free the R ring, and
             // K(i - 1) must not.
             MqTile cur;
@@ -516,41 +516,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 return true;
             };
 
-            // the static unit of this CTA, then dynamic chunks (as in the single-query kernel)
+            // the static unit of this CTA, then dynamic chunks (as in the single-query kernel);
+            // one call site of emit_piece keeps the producer's code small
             long long x = static_unit_begin(pl, cta);
             const long long stop = static_unit_begin(pl, cta + 1);
-            while (ok && x < stop) {
-                const int b = upper_seq(pl.spref, B, x);
-                const int st = static_tiles(pl, b);
-                const long long rel = x - pl.spref[b];
-                const int kvh = static_cast<int>(div_floor(rel, st));
-                const int k0 = static_cast<int>(rel - static_cast<long long>(kvh) * st);
-                const int take = static_cast<int>(stop - x < st - k0 ? stop - x : st - k0);
-                x += take;
-                const int e = k0 + take == st ? pl.sn[b] : (k0 + take) * kMqTile;
-                ok = emit_piece(b, kvh, pl.lo[b] + k0 * kMqTile, pl.lo[b] + e, cta + b * KVH + kvh,
-                                x >= stop);
-            }
-            while (ok && dynamic) {
-                if (claimed < 0) claimed = static_cast<int>(atomicAdd(p.ws_claim, 1u));
-                const int k = claimed;
-                claimed = -1;
-                if (k >= pl.n_dyn) break;
-                const bool is_long = k < pl.n_dyn0;
-                const int kk = is_long ? k : k - pl.n_dyn0;
-                const uint16_t* pref = is_long ? pl.dpref : pl.dpref1;
-                const int b = upper_seq(pref, B, kk);
-                const int per = is_long ? pl.dn[b] : pl.dn1[b];
-                const int rel = kk - pref[b];
-                const int kvh = rel / per;
-                const int idx = rel - kvh * per;
-                const int len = is_long ? pl.c_dyn : pl.c_dyn1;
-                const int local = is_long ? idx : pl.dn[b] + idx;
-                const int p0 = pl.lo[b] + pl.sn[b] + (is_long ? 0 : pl.dn[b] * pl.c_dyn) + idx * len;
-                const int slot = p.dyn_slot_base + pl.dpref[b] + pl.dpref1[b] +
-                                 kvh * (pl.dn[b] + pl.dn1[b]) + local;
-                ok = emit_piece(b, kvh, p0, p0 + len, slot, true);
-            }
+            Piece pc;
+            while (ok && next_piece(pl, p, cta, kMqTile, dynamic, x, stop, claimed, pc))
+                ok = emit_piece(pc.b, pc.kvh, pc.p0, pc.p1, pc.slot, pc.unit_end);
             // end of work: end-of-work markers where the next K (and R) block would be,
             // then the blocks still owed
             if (ok) {
@@ -888,10 +860,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const uint32_t sx = stage0 + rstg(q0) * kMqStageBytes;       // dims [0, 64)
                 const uint32_t sy = stage0 + rstg(q0 + 1) * kMqStageBytes;   // dims [D/2, D/2 + 64)
                 const uint32_t rowoff = (j >> 3) * 1024 + (j & 7) * 128;
-                {   // this warp's half of the pairs: [32 h, 32 h + 32)
-                    uint32_t hx[16], hy[16], lx[16], ly[16];
-#pragma unroll
+                {   // this warp's half of the pairs: [32 h, 32 h + 32), 8 pairs per round
+                    // (a rolled loop: the kernel's roles share the SM's instruction caches)
+                    // keys columns: dims i (x) at i / 2, dims D/2 + i (y) at 32 + i / 2; lo parts
+                    // 64 later
+                    const uint32_t kb = lane_addr + Cfg::TMEM_KROT + 16 * h;
+#pragma unroll 1
                     for (int u = 0; u < 4; ++u) {   // pairs 32 h + 8 u .. + 8
+                        uint32_t hx[4], hy[4], lx[4], ly[4];
                         uint32_t f[32];
                         const uint32_t tcol = lane_addr + Cfg::TMEM_TRIG + 4 * (32 * h + 8 * u);
                         ptx::tmem_ld16(tcol, *reinterpret_cast<uint32_t(*)[16]>(&f[0]));
@@ -920,18 +896,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             const float2 rb = ptx::f2_unpack(ptx::f2_sub(yb, ptx::f2_pack(g1.x, g1.y)));
                             const __half2 l0 = __floats2half2_rn(ra.x, ra.y);
                             const __half2 l1 = __floats2half2_rn(rb.x, rb.y);
-                            hx[4 * u + e] = *reinterpret_cast<const uint32_t*>(&h0);
-                            hy[4 * u + e] = *reinterpret_cast<const uint32_t*>(&h1);
-                            lx[4 * u + e] = *reinterpret_cast<const uint32_t*>(&l0);
-                            ly[4 * u + e] = *reinterpret_cast<const uint32_t*>(&l1);
+                            hx[e] = *reinterpret_cast<const uint32_t*>(&h0);
+                            hy[e] = *reinterpret_cast<const uint32_t*>(&h1);
+                            lx[e] = *reinterpret_cast<const uint32_t*>(&l0);
+                            ly[e] = *reinterpret_cast<const uint32_t*>(&l1);
                         }
+                        ptx::tmem_st4(kb + 4 * u, hx);
+                        ptx::tmem_st4(kb + 32 + 4 * u, hy);
+                        ptx::tmem_st4(kb + 64 + 4 * u, lx);
+                        ptx::tmem_st4(kb + 96 + 4 * u, ly);
                     }
-                    // columns: dims i (x) at i / 2, dims D/2 + i (y) at 32 + i / 2; lo parts 64 later
-                    const uint32_t kb = lane_addr + Cfg::TMEM_KROT + 16 * h;
-                    ptx::tmem_st16(kb, hx);
-                    ptx::tmem_st16(kb + 32, hy);
-                    ptx::tmem_st16(kb + 64, lx);
-                    ptx::tmem_st16(kb + 96, ly);
                 }
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
@@ -956,6 +930,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // [RH, 2 RH).  Over a K=V cache the G query rows' scores are the sum of a hi
         // column r and a lo column G + r.
         constexpr int RH = Cfg::KEQV ? Cfg::RMAX : NMAX / 2;   // rows per warp
+        // the loops over head-dim blocks (rescale, epilogue) stay rolled where that costs no
+        // registers: the kernel's roles share the SM's instruction caches, and smaller code
+        // misses them less (with 32 query rows rolling them spills, so they are unrolled)
+        constexpr int kBlockUnroll = Cfg::RMAX > 16 ? NB : 1;
         constexpr int kSmx = Cfg::SMX_THREADS;
         const int q4 = warp & 3;
         const int r0 = Cfg::KEQV ? 0 : ((warp - 2) >> 2) * RH;   // first row of this warp
@@ -992,7 +970,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const SegmentParts sp(pl, epi.b, epi.kvh, p.dyn_slot_base);
             const bool direct = sp.count() == 1;
             if (r0 < R) {
-#pragma unroll
+#pragma unroll (kBlockUnroll)
                 for (int mb = 0; mb < NB; ++mb) {
                     // row r's sum is its hi column r plus its lo column PLO + r
                     uint32_t oh[RH], ol[RH];
@@ -1154,7 +1132,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                       &sm.abort_flag, p.ws_flags);
                     if (ptx::named_barrier_or(1, kSmx, !ok)) break;
                     ptx::tc_fence_after();
-#pragma unroll
+#pragma unroll (kBlockUnroll)
                     for (int mb = 0; mb < NB; ++mb) {
                         // the hi column and the lo column of each row
 #pragma unroll
