@@ -459,19 +459,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 ++vpush;
                 return true;
             };
-            // Tiles arrive in order.  Multi-query: K(i), then V(i - 1).  K=V: K(i - 1) and
-            // tile i - 1 to the V producer, then R(i) one tile ahead (the key-deriving warps
-            // derive tile i's rotated keys while tile i - 1's scores are computed).  K goes
-            // first: R(i) waits for the derivation of tile i - 1 to free the R ring, and
-            // K(i - 1) must not.
-            MqTile cur;
-            bool have_cur = false;
+            // Tiles arrive in order.  Multi-query: K(i), then V(i - 1).  K=V: K(i), tile i to
+            // the V producer, then R(i).  R(i) waits for the derivation of tile i - 1 to free
+            // the R ring; the scores warp does not wait for any derivation, so K(i) goes out
+            // first and the K stream runs ahead of the derivation.
             auto emit_tile = [&](MqTile nxt) -> bool {
                 if constexpr (Cfg::KEQV) {
-                    if (have_cur && !(emit_block(cur, kMqKindK) && push_v(cur))) return false;
-                    if (!emit_block(nxt, kMqKindR)) return false;
-                    cur = nxt;
-                    have_cur = true;
+                    if (!(emit_block(nxt, kMqKindK) && push_v(nxt) && emit_block(nxt, kMqKindR)))
+                        return false;
                 } else {
                     if (!emit_block(nxt, kMqKindK)) return false;
                     if (have_prev && !emit_block(prev, kMqKindV)) return false;
@@ -531,8 +526,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 none.slot = none.ob = 0;
                 none.flags = kDescDone;
                 if constexpr (Cfg::KEQV) {
-                    if (have_cur) ok = emit_block(cur, kMqKindK) && push_v(cur);
-                    if (ok) ok = emit_block(none, kMqKindDoneR);
+                    ok = emit_block(none, kMqKindDoneR);
                     if (ok) ok = emit_block(none, kMqKindDone);
                     if (ok) ok = push_v(none);
                 } else {
