@@ -380,7 +380,9 @@ __device__ __forceinline__ void store_out4(const DecodeParams& p, size_t idx, fl
 }
 
 // ---------------------------------------------------------------------------
-// Plan computation (warp 0; lane l owns sequences 8l .. 8l + 7).  Lengths are
+// Plan computation, by warps 0..7: lane l of warp w owns sequence b = 32 w + l.
+// Every thread of the CTA calls it (the other warps only take part in its CTA
+// barriers); it ends with a barrier after which the plan is complete.  Lengths are
 // clamped to [0, capacity].  The tail of each segment becomes dynamic chunks:
 // long ones of c_dyn positions, then short ones of c_dyn1 ~ c_dyn / 4, all whole
 // tiles of `unit` positions.  At most cap = min(kDynChunksPerCta * grid,
@@ -398,183 +400,204 @@ __device__ __forceinline__ void store_out4(const DecodeParams& p, size_t idx, fl
 // their lengths; together they never take more than half of a segment.
 //
 // Only the chunk counts are bounded, so c_dyn, F and T may be rounded freely:
-// they are taken in float (all CTAs compute the same values), which keeps this
-// warp's serial latency low.  The counts themselves are integers: n_b <= 2^18,
-// B <= 256, KVH <= 16, so every sum fits 32 bits.
+// they are taken in float (every thread of every CTA computes the same values).
+// The counts themselves are integers: n_b <= 2^18, B <= 256, KVH <= 16, so every
+// sum fits 32 bits.
+//
+// Three passes, one sequence per lane: (1) lengths, ranges and a warp scan of n;
+// (2) the chunk sizing from the total, each sequence's split and warp scans of
+// its tile and chunk counts; (3) the prefix arrays.  The warps' sums cross over
+// through `xsum` (32 words of shared memory that nothing else uses meanwhile; the
+// caller passes the first stage buffer, which no copy has been issued to yet).
+// One short pass per warp instead of one warp walking eight sequences per lane
+// keeps the plan's latency (and the code fetched cold on each SM) small.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, int grid,
-                                           int lane, int cta, int unit) {
-    constexpr int kPer = kMaxBatch / 32;
+constexpr int kPlanWarps = kMaxBatch / 32;   // 8
+
+__device__ __forceinline__ void build_plan(PlanSmem& pl, const DecodeParams& p, int grid, int warp,
+                                           int lane, int cta, int unit, uint32_t* xsum) {
     const int B = p.B, KVH = p.KVH;
-    int n[kPer];
-    {
-        int L[kPer];
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int b = lane * kPer + j;
-            L[j] = b < B ? __ldg(p.seq_lens + b) : 0;
+    const int b = warp * 32 + lane;
+    const bool plan_warp = warp < kPlanWarps;
+    const bool in_batch = plan_warp && b < B;
+    // ---- pass 1: clamped lengths, attended ranges, warp scan of n ----
+    int n = 0, nincl = 0;
+    if (plan_warp) {
+        int x = in_batch ? __ldg(p.seq_lens + b) : 0;
+        if (x < 0 || x > p.capacity) {
+            if (in_batch && cta == 0) atomicOr(p.ws_flags, kFlagBadLength);
+            x = x < 0 ? 0 : p.capacity;
         }
-        bool bad = false;
+        // union of the queries' ranges: query 0 (position x - T) starts the
+        // earliest window, the last query ends at x
+        const int span = p.window > 0 ? p.window + (p.T > 1 ? p.T - 1 : 0) : 0;
+        const int lo = (span > 0 && x > span) ? x - span : 0;
+        n = in_batch ? x - lo : 0;
+        if (in_batch) {
+            pl.lo[b] = lo;
+            pl.n[b] = n;
+        }
+        nincl = n;
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int b = lane * kPer + j;
-            int x = L[j];
-            if (x < 0 || x > p.capacity) {
-                bad = b < B;
-                x = x < 0 ? 0 : p.capacity;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, nincl, off);
+            if (lane >= off) nincl += t;
+        }
+        if (lane == 31) xsum[warp] = static_cast<uint32_t>(nincl);
+    }
+    __syncthreads();
+    // ---- pass 2: chunk sizing (every plan thread alike), this sequence's split ----
+    uint32_t st_incl = 0;
+    int d_incl = 0, d1_incl = 0, st_own = 0, d_own = 0, d1_own = 0;
+    bool single = false;
+    int c = kDynMinChunk, c1 = kDynMinChunk;
+    if (plan_warp) {
+        uint32_t tot = 0, nbase = 0;
+#pragma unroll
+        for (int w = 0; w < kPlanWarps; ++w) {
+            const uint32_t v = xsum[w];
+            tot += v;
+            nbase += w < warp ? v : 0u;
+        }
+        const uint32_t N = tot * static_cast<uint32_t>(KVH);
+        const uint32_t ugrid = static_cast<uint32_t>(grid);
+        const uint32_t g = N < ugrid ? N : ugrid;
+        const uint32_t cdyn = static_cast<uint32_t>(kDynChunksPerCta) * ugrid;
+        const uint32_t cap = cdyn < static_cast<uint32_t>(p.max_dyn) ? cdyn : static_cast<uint32_t>(p.max_dyn);
+        // the short chunks' slots are set aside first (at most half of them)
+        const uint32_t tail_want = static_cast<uint32_t>(kDynTailPerCta) * ugrid;
+        const uint32_t tail_cap = tail_want < cap / 2 ? tail_want : cap / 2;
+        const uint32_t long_cap = cap - tail_cap;
+        // floor(N / g) >= kDynMinShare; none in the single-piece test mode
+        single = (p.test_flags & kTestSinglePiece) != 0;
+        const bool use_dyn = !single && g > 0 && N >= static_cast<uint32_t>(kDynMinShare) * g &&
+                             long_cap > 0;
+        int T = 0;
+        if (use_dyn) {
+            const float Nf = static_cast<float>(N);
+            // chunk length: at least kDynMinChunk, about N / (kDynFraction cap), whole tiles
+            const int cf = static_cast<int>(ceilf(Nf / static_cast<float>(kDynFraction * long_cap)));
+            c = ((cf + unit - 1) / unit) * unit;
+            c = c < kDynMinChunk ? kDynMinChunk : c;
+            const uint32_t csmall = static_cast<uint32_t>(kDynSmallPerCta) * ugrid;
+            const float small = static_cast<float>(csmall < long_cap ? csmall : long_cap);
+            const float cff = static_cast<float>(c);
+            const float F = fmaxf(fminf(ceilf(Nf / small), kDynFraction * cff), kDynMinSpan * cff);
+            const int t = static_cast<int>(static_cast<float>(tot) / F + 0.5f);
+            const int tmax = static_cast<int>(long_cap) / KVH;
+            T = t < tmax ? t : tmax;
+        }
+        // short chunks of c1 ~ c / kDynTailRatio positions, about kDynTailPerCta per CTA,
+        // claimed after the long ones: when the long chunks run out, CTAs still differ
+        // by up to one long chunk of work, and the short ones even that out
+        c1 = c;
+        int T1 = 0;
+        if (T > 0) {
+            // (never below kDynMinChunk: shorter pieces cost more in their epilogue
+            // and claim than they gain in balance)
+            c1 = (c / kDynTailRatio) / unit * unit;
+            if (c1 >= kDynMinChunk) {
+                const int want = (static_cast<int>(tail_cap) + KVH / 2) / KVH;
+                const int room = static_cast<int>(cap) / KVH - T;
+                T1 = want < room ? want : room;
+            } else {
+                c1 = c;
             }
-            // union of the queries' ranges: query 0 (position x - T) starts the
-            // earliest window, the last query ends at x
-            const int span = p.window > 0 ? p.window + (p.T > 1 ? p.T - 1 : 0) : 0;
-            const int lo = (span > 0 && x > span) ? x - span : 0;
-            n[j] = b < B ? x - lo : 0;
-            if (b < B) {
-                pl.lo[b] = lo;
-                pl.n[b] = n[j];
-            }
         }
-        if (bad && cta == 0) atomicOr(p.ws_flags, kFlagBadLength);
-    }
-    // exclusive prefix of n over the sequences (lane-local run, then a warp scan)
-    int nloc[kPer], nrun = 0;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        nloc[j] = nrun;
-        nrun += n[j];
-    }
-    int nincl = nrun;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int tn = __shfl_up_sync(0xffffffffu, nincl, off);
-        if (lane >= off) nincl += tn;
-    }
-    const int nexcl = nincl - nrun;
-    const uint32_t tot = static_cast<uint32_t>(__shfl_sync(0xffffffffu, nincl, 31));
-    const uint32_t N = tot * static_cast<uint32_t>(KVH);
-    const uint32_t ugrid = static_cast<uint32_t>(grid);
-    const uint32_t g = N < ugrid ? N : ugrid;
-    const uint32_t cdyn = static_cast<uint32_t>(kDynChunksPerCta) * ugrid;
-    const uint32_t cap = cdyn < static_cast<uint32_t>(p.max_dyn) ? cdyn : static_cast<uint32_t>(p.max_dyn);
-    // the short chunks' slots are set aside first (at most half of them)
-    const uint32_t tail_want = static_cast<uint32_t>(kDynTailPerCta) * ugrid;
-    const uint32_t tail_cap = tail_want < cap / 2 ? tail_want : cap / 2;
-    const uint32_t long_cap = cap - tail_cap;
-    // floor(N / g) >= kDynMinShare; none in the single-piece test mode
-    const bool single = (p.test_flags & kTestSinglePiece) != 0;
-    const bool use_dyn = !single && g > 0 && N >= static_cast<uint32_t>(kDynMinShare) * g &&
-                         long_cap > 0;
-    int c = kDynMinChunk, T = 0;
-    if (use_dyn) {
-        const float Nf = static_cast<float>(N);
-        // chunk length: at least kDynMinChunk, about N / (kDynFraction cap), whole tiles
-        const int cf = static_cast<int>(ceilf(Nf / static_cast<float>(kDynFraction * long_cap)));
-        c = ((cf + unit - 1) / unit) * unit;
-        c = c < kDynMinChunk ? kDynMinChunk : c;
-        const uint32_t csmall = static_cast<uint32_t>(kDynSmallPerCta) * ugrid;
-        const float small = static_cast<float>(csmall < long_cap ? csmall : long_cap);
-        const float cff = static_cast<float>(c);
-        const float F = fmaxf(fminf(ceilf(Nf / small), kDynFraction * cff), kDynMinSpan * cff);
-        const int t = static_cast<int>(static_cast<float>(tot) / F + 0.5f);
-        const int tmax = static_cast<int>(long_cap) / KVH;
-        T = t < tmax ? t : tmax;
-    }
-    // short chunks of c1 ~ c / kDynTailRatio positions, about kDynTailPerCta per CTA,
-    // claimed after the long ones: when the long chunks run out, CTAs still differ
-    // by up to one long chunk of work, and the short ones even that out
-    int c1 = c, T1 = 0;
-    if (T > 0) {
-        // (never below kDynMinChunk: shorter pieces cost more in their epilogue
-        // and claim than they gain in balance)
-        c1 = (c / kDynTailRatio) / unit * unit;
-        if (c1 >= kDynMinChunk) {
-            const int want = (static_cast<int>(tail_cap) + KVH / 2) / KVH;
-            const int room = static_cast<int>(cap) / KVH - T;
-            T1 = want < room ? want : room;
-        } else {
-            c1 = c;
-        }
-    }
-    // sequence b gets d_b = f(P_b + n_b) - f(P_b) long chunks per kv head, P_b the sum
-    // of n over the sequences before b and f(x) = floor(x * (T / sum n)): f is
-    // monotone and f(sum n) <= T, so the d_b are >= 0 and add up to at most T; the
-    // same with T1 for the short ones.  Together they take at most half a segment.
-    const float r = T > 0 ? static_cast<float>(T) / static_cast<float>(tot) : 0.0f;
-    const float r1 = T1 > 0 ? static_cast<float>(T1) / static_cast<float>(tot) : 0.0f;
-    const float inv2c = 1.0f / static_cast<float>(2 * c);
-    const float inv2c1 = 1.0f / static_cast<float>(2 * c1);
-    uint32_t sloc[kPer], srun = 0;
-    int dloc[kPer], drun = 0, d1loc[kPer], d1run = 0;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int b = lane * kPer + j;
+        // sequence b gets d_b = f(P_b + n_b) - f(P_b) long chunks per kv head, P_b the sum
+        // of n over the sequences before b and f(x) = floor(x * (T / sum n)): f is
+        // monotone and f(sum n) <= T, so the d_b are >= 0 and add up to at most T; the
+        // same with T1 for the short ones.  Together they take at most half a segment.
         int d = 0, d1 = 0;
-        if (T > 0 && n[j] > 0) {
-            const float x0 = static_cast<float>(nexcl + nloc[j]);
-            const float x1 = static_cast<float>(nexcl + nloc[j] + n[j]);
+        if (T > 0 && n > 0) {
+            const float r = static_cast<float>(T) / static_cast<float>(tot);
+            const float x0 = static_cast<float>(nbase + static_cast<uint32_t>(nincl - n));
+            const float x1 = static_cast<float>(nbase + static_cast<uint32_t>(nincl));
             d = __float2int_rd(__fmul_rn(x1, r)) - __float2int_rd(__fmul_rn(x0, r));
-            int h = __float2int_rd(static_cast<float>(n[j]) * inv2c);   // floor(n / 2c)
-            h -= (h * 2 * c > n[j]) ? 1 : 0;
+            int h = __float2int_rd(static_cast<float>(n) * (1.0f / static_cast<float>(2 * c)));
+            h -= (h * 2 * c > n) ? 1 : 0;   // floor(n / 2c)
             d = d < h ? d : h;
             if (T1 > 0) {
+                const float r1 = static_cast<float>(T1) / static_cast<float>(tot);
                 d1 = __float2int_rd(__fmul_rn(x1, r1)) - __float2int_rd(__fmul_rn(x0, r1));
-                const int left = n[j] - 2 * d * c;                       // >= 0
-                int h1 = __float2int_rd(static_cast<float>(left) * inv2c1);
+                const int left = n - 2 * d * c;   // >= 0
+                int h1 = __float2int_rd(static_cast<float>(left) * (1.0f / static_cast<float>(2 * c1)));
                 h1 -= (h1 * 2 * c1 > left) ? 1 : 0;
                 d1 = d1 < h1 ? d1 : h1;
             }
         }
-        const int sn = n[j] - d * c - d1 * c1;
-        if (b < B) {
+        const int sn = n - d * c - d1 * c1;
+        if (in_batch) {
             pl.sn[b] = sn;
             pl.dn[b] = static_cast<uint16_t>(d);
             pl.dn1[b] = static_cast<uint16_t>(d1);
         }
-        sloc[j] = srun;
-        dloc[j] = drun;
-        d1loc[j] = d1run;
-        srun += static_cast<uint32_t>((sn + unit - 1) / unit) * static_cast<uint32_t>(KVH);
-        drun += d * KVH;
-        d1run += d1 * KVH;
-    }
-    uint32_t sincl = srun;
-    int dincl = drun, d1incl = d1run;
+        st_own = ((sn + unit - 1) / unit) * KVH;
+        d_own = d * KVH;
+        d1_own = d1 * KVH;
+        st_incl = static_cast<uint32_t>(st_own);
+        d_incl = d_own;
+        d1_incl = d1_own;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t ts = __shfl_up_sync(0xffffffffu, sincl, off);
-        const int td = __shfl_up_sync(0xffffffffu, dincl, off);
-        const int td1 = __shfl_up_sync(0xffffffffu, d1incl, off);
-        if (lane >= off) {
-            sincl += ts;
-            dincl += td;
-            d1incl += td1;
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t ts = __shfl_up_sync(0xffffffffu, st_incl, off);
+            const int td = __shfl_up_sync(0xffffffffu, d_incl, off);
+            const int td1 = __shfl_up_sync(0xffffffffu, d1_incl, off);
+            if (lane >= off) {
+                st_incl += ts;
+                d_incl += td;
+                d1_incl += td1;
+            }
+        }
+        if (lane == 31) {   // (words 0 .. 7 are still being read: these are 8 .. 31)
+            xsum[8 + warp] = st_incl;
+            xsum[16 + warp] = static_cast<uint32_t>(d_incl);
+            xsum[24 + warp] = static_cast<uint32_t>(d1_incl);
         }
     }
-    const uint32_t sexcl = sincl - srun;
-    const int dexcl = dincl - drun, d1excl = d1incl - d1run;
+    __syncthreads();
+    // ---- pass 3: exclusive prefixes over the sequences (entry B holds the totals) ----
+    if (plan_warp) {
+        uint32_t sb = 0, st_tot = 0;
+        int db = 0, d_tot = 0, d1b = 0, d1_tot = 0;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int b = lane * kPer + j;
+        for (int w = 0; w < kPlanWarps; ++w) {
+            const uint32_t vs = xsum[8 + w];
+            const int vd = static_cast<int>(xsum[16 + w]), vd1 = static_cast<int>(xsum[24 + w]);
+            st_tot += vs;
+            d_tot += vd;
+            d1_tot += vd1;
+            if (w < warp) {
+                sb += vs;
+                db += vd;
+                d1b += vd1;
+            }
+        }
         if (b <= B) {
-            pl.spref[b] = sexcl + sloc[j];
-            pl.dpref[b] = static_cast<uint16_t>(dexcl + dloc[j]);
-            pl.dpref1[b] = static_cast<uint16_t>(d1excl + d1loc[j]);
+            pl.spref[b] = sb + st_incl - static_cast<uint32_t>(st_own);
+            pl.dpref[b] = static_cast<uint16_t>(db + d_incl - d_own);
+            pl.dpref1[b] = static_cast<uint16_t>(d1b + d1_incl - d1_own);
         }
-    }
-    if (lane == 31) {
-        if (B == kMaxBatch) {
-            pl.spref[kMaxBatch] = sincl;
-            pl.dpref[kMaxBatch] = static_cast<uint16_t>(dincl);
-            pl.dpref1[kMaxBatch] = static_cast<uint16_t>(d1incl);
+        if (warp == 0 && lane == 0) {
+            if (B == kMaxBatch) {
+                pl.spref[kMaxBatch] = st_tot;
+                pl.dpref[kMaxBatch] = static_cast<uint16_t>(d_tot);
+                pl.dpref1[kMaxBatch] = static_cast<uint16_t>(d1_tot);
+            }
+            pl.n_static = static_cast<long long>(st_tot);
+            pl.unit = unit;
+            pl.n_dyn0 = d_tot;
+            pl.n_dyn = d_tot + d1_tot;
+            pl.c_dyn = c;
+            pl.c_dyn1 = c1;
+            const uint32_t units = single ? 1u : static_cast<uint32_t>(grid);   // single piece: CTA 0 takes all
+            pl.g_eff = static_cast<int>(st_tot < units ? st_tot : units);
         }
-        pl.n_static = static_cast<long long>(sincl);
-        pl.unit = unit;
-        pl.n_dyn0 = dincl;
-        pl.n_dyn = dincl + d1incl;
-        pl.c_dyn = c;
-        pl.c_dyn1 = c1;
-        const uint32_t units = single ? 1u : ugrid;   // single piece: CTA 0 takes all
-        pl.g_eff = static_cast<int>(sincl < units ? sincl : units);
+        // xsum lies in a stage buffer that TMA writes next: order these generic-proxy
+        // accesses before those async-proxy writes
+        ptx::fence_proxy_async_smem();
     }
+    __syncthreads();
 }
 
 // ---------------------------------------------------------------------------
@@ -664,6 +687,7 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
     constexpr int kBoxesPerTile = TP / kBoxRows;
     constexpr int kChunksPerRow = D / kChunkElems;
     static_assert(TP % kBoxRows == 0, "tile must be whole boxes");
+    static_assert(block_threads<Pol>() >= 32 * kPlanWarps, "the plan takes eight warps");
 
     extern __shared__ uint8_t smem_raw[];
     // aligned to 1024 B by pointer arithmetic on smem_raw, so that the compiler still
@@ -699,21 +723,25 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
     ptx::allow_dependent_launch();
 
     // ---- plan: clamped lengths, attended ranges, static/dynamic split ----
-    if (warp == 0) build_plan(pl, p, gridDim.x, lane, cta, TP);
-    __syncthreads();
+    build_plan(pl, p, gridDim.x, warp, lane, cta, TP, reinterpret_cast<uint32_t*>(&sm.kv[0][0][0]));
 
-    // sequences with nothing to attend produce zeros (the empty sum)
-    for (int b = cta; b < B; b += gridDim.x) {
-        if (pl.n[b] != 0) continue;
-        const size_t base = static_cast<size_t>(b) * H * D;
-        for (int i = tid; i < H * D; i += blockDim.x) store_out(p, base + i, 0.0f);
-    }
-    // the partial list of every segment, for the combine kernel (each CTA a slice)
-    {
+    // Work that no tile waits for: zeros for the sequences with nothing to attend (the
+    // empty sum) and the partial list of every segment, which the combine kernel reads
+    // (each CTA a slice).  The consumer warps do it while the first tiles load; a CTA without
+    // work does it with all of its threads and leaves.
+    const bool has_work = cta < pl.g_eff;   // (false also for an all-empty batch)
+    if (!has_work || warp < NC) {
+        const int nt = has_work ? kConsumerThreads : static_cast<int>(blockDim.x);
+        for (int b = cta; b < B; b += gridDim.x) {
+            if (pl.n[b] != 0) continue;
+            const size_t base = static_cast<size_t>(b) * H * D;
+            for (int i = tid; i < H * D; i += nt) store_out(p, base + i, 0.0f);
+        }
+        // (policies that merge in this kernel do not need the lists; they are written
+        // anyway, off the critical path, as a record of how each segment was split)
         const int U = B * KVH;
         const int u_end = (cta + 1) * U / static_cast<int>(gridDim.x);   // < 2^31: U <= 4096
-        for (int u = cta * U / static_cast<int>(gridDim.x) + tid; u < u_end;
-             u += blockDim.x) {
+        for (int u = cta * U / static_cast<int>(gridDim.x) + tid; u < u_end; u += nt) {
             const int b = u / KVH, kvh = u - (u / KVH) * KVH;
             int4 e = make_int4(0, 0, 0, 0);
             if (pl.n[b] != 0 && pl.g_eff > 0) {
@@ -723,7 +751,7 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
             p.ws_segs[u] = e;
         }
     }
-    if (cta >= pl.g_eff) return;   // also covers an all-empty batch
+    if (!has_work) return;
 
     const uint32_t kv_base = ptx::smem_addr(&sm.kv[0][0][0]);
     constexpr int kTensors = KernelSmem<Pol>::kTensors;

@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     constexpr int D = Cfg::D, G = Cfg::G, NSUB = Cfg::NSUB, NB = Cfg::NB, STAGES = Cfg::STAGES;
     constexpr int KST = Cfg::KST, VST = Cfg::VST;
     constexpr int NMAX = Cfg::NMAX;
+    static_assert(Cfg::THREADS >= 32 * kPlanWarps, "the plan takes eight warps");
 
     extern __shared__ uint8_t smem_raw[];
     // aligned to 1024 B by pointer arithmetic on smem_raw, so that the compiler still
@@ -277,21 +278,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     ptx::grid_dependency_wait();
     ptx::allow_dependent_launch();
 
-    if (warp == 0) build_plan(pl, p, gridDim.x, lane, cta, kMqTile);
-    __syncthreads();
+    build_plan(pl, p, gridDim.x, warp, lane, cta, kMqTile, reinterpret_cast<uint32_t*>(&sm.stage[0][0]));
 
-    // sequences with nothing to attend produce zeros for all T queries
-    for (int b = cta; b < B; b += gridDim.x) {
-        if (pl.n[b] != 0) continue;
-        const size_t base = static_cast<size_t>(b) * T * H * D;
-        for (int i = tid; i < T * H * D; i += blockDim.x) store_out(p, base + i, 0.0f);
-    }
-    // partial list of every segment, for the combine kernel
-    {
+    // Work that no tile waits for: zeros for the sequences with nothing to attend (all T
+    // queries) and the partial list of every segment for the combine kernel (each CTA a
+    // slice).  The softmax warps do it while the first tiles load (bookkeeping() below);
+    // a CTA without work does it with all of its threads and leaves.
+    auto bookkeeping = [&](int t0, int nt) {
+        for (int b = cta; b < B; b += gridDim.x) {
+            if (pl.n[b] != 0) continue;
+            const size_t base = static_cast<size_t>(b) * T * H * D;
+            for (int i = t0; i < T * H * D; i += nt) store_out(p, base + i, 0.0f);
+        }
         const int U = B * KVH;
         const int u_end = (cta + 1) * U / static_cast<int>(gridDim.x);   // < 2^31: U <= 4096
-        for (int u = cta * U / static_cast<int>(gridDim.x) + tid; u < u_end;
-             u += blockDim.x) {
+        for (int u = cta * U / static_cast<int>(gridDim.x) + t0; u < u_end; u += nt) {
             const int b = u / KVH, kvh = u - (u / KVH) * KVH;
             int4 e = make_int4(0, 0, 0, 0);
             if (pl.n[b] != 0 && pl.g_eff > 0) {
@@ -300,8 +301,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             p.ws_segs[u] = e;
         }
+    };
+    if (cta >= pl.g_eff) {   // (also for an all-empty batch)
+        bookkeeping(tid, static_cast<int>(blockDim.x));
+        return;
     }
-    if (cta >= pl.g_eff) return;   // also covers an all-empty batch
 
     if (warp == 1) ptx::tmem_alloc(ptx::smem_addr(&sm.tmem_base), Cfg::TMEM_COLS);
     ptx::tc_fence_before();
@@ -942,6 +946,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             l_part[k] = 0.0f;
         }
         uint32_t bad_q = 0;   // bit t: query t attended a bad page in this piece
+        bookkeeping(sid, kSmx);
         // P rows past the query rows in use stay zero (the P.V mma reads PROWS rows)
         for (int i = sid; i < 2 * Cfg::PBYTES / 16; i += kSmx)
             ptx::sts128(ptx::smem_addr(&sm.pm[0][0]) + i * 16, 0u, 0u, 0u, 0u);
