@@ -315,6 +315,18 @@ def main_kernel(gqa, call) -> str:
     return "gqa_decode_kernel"
 
 
+def launches_per_call(gqa, call) -> int:
+    """Kernels one call launches: the producer 1; a slidingDecodeGQA decode 1 (split
+    segments merge in the main kernel); a decodeGQA decode 2 (main and combine kernels);
+    a K=V call on the tcgen05 kernel 3 (the scores-operand kernel first)."""
+    if call.raw is not None:
+        return 1
+    kernel = main_kernel(gqa, call)
+    if kernel == "gqa_mq_kernel":
+        return 3 if call.keqv else 2
+    return 1 if call.layer == "sliding" else 2
+
+
 def recorded_traffic(workload: str, layer: str, kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
     path = os.path.join(PROFILES, "traffic.json")
@@ -642,8 +654,7 @@ def run_ours(args, wl):
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        # a decode call is two launches (decode and combine kernels), the producer one
-        "gpu_launches": args.steps * sum(1 if c.raw is not None else 2 for c in calls),
+        "gpu_launches": args.steps * sum(launches_per_call(gqa, c) for c in calls),
         "clocks": clock_summary(clock_rows, t_wall0, t_wall1),
         "device_status": status,
     }
