@@ -19,7 +19,9 @@
 // memory when a piece ends.  Two warps per scheduler, and 8 positions per warp
 // per tile, keep the shuffle and shared-memory latency chains overlapped.
 // Scores are kept in log2 units (q is pre-multiplied by log2(e)), so every
-// exponential is exp2.
+// exponential is exp2.  The products run on packed fp32 pairs (fma.rn.f32x2: the
+// two halves of a bf16x2 word, widened exactly), two fp32 FMAs per instruction;
+// each score sums its even and its odd products in two chains.
 #pragma once
 
 #include "decode_kernel.cuh"
@@ -45,10 +47,10 @@ struct SlidingCore {
     };
 
     struct State {
-        float q[G][8];     // q[h][8*lane + e] * log2(e)
-        float acc[G][8];   // unnormalised output, dims 8*lane + e
-        float m[G];        // running max (log2 units), same in every lane
-        float l[G];        // running normaliser, same in every lane
+        uint64_t q[G][4];     // q[h][8*lane + 2e, + 2e + 1] * log2(e), packed fp32 pairs
+        uint64_t acc[G][4];   // unnormalised output, dims 8*lane + 2e, + 2e + 1 (pairs)
+        float m[G];           // running max (log2 units), same in every lane
+        float l[G];           // running normaliser, same in every lane
     };
 
     __device__ static __forceinline__ void begin(State& st, const __nv_bfloat16* q_heads, int warp,
@@ -60,11 +62,9 @@ struct SlidingCore {
             const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                st.q[h][2 * e] = bf16lo(w[e]) * kLog2e;
-                st.q[h][2 * e + 1] = bf16hi(w[e]) * kLog2e;
+                st.q[h][e] = ptx::f2_pack(bf16lo(w[e]) * kLog2e, bf16hi(w[e]) * kLog2e);
+                st.acc[h][e] = ptx::f2_pack(0.0f, 0.0f);
             }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) st.acc[h][e] = 0.0f;
             st.m[h] = -INFINITY;
             st.l[h] = 0.0f;
         }
@@ -88,17 +88,18 @@ struct SlidingCore {
         for (int j = 0; j < kPosPerWarp; ++j) {
             const uint4 raw = ptx::lds128(row_addr(k_tile, row0 + j, lane));
             const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-            float s0 = 0.0f, s1 = 0.0f;
+            // even and odd products of each head in the two halves of a pair
+            uint64_t s0 = ptx::f2_mul(st.q[0][0], ptx::f2_from_bf16x2(w[0]));
+            uint64_t s1 = ptx::f2_mul(st.q[1][0], ptx::f2_from_bf16x2(w[0]));
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float k0 = bf16lo(w[e]), k1 = bf16hi(w[e]);
-                s0 = fmaf(st.q[0][2 * e], k0, s0);
-                s0 = fmaf(st.q[0][2 * e + 1], k1, s0);
-                s1 = fmaf(st.q[1][2 * e], k0, s1);
-                s1 = fmaf(st.q[1][2 * e + 1], k1, s1);
+            for (int e = 1; e < 4; ++e) {
+                const uint64_t kk = ptx::f2_from_bf16x2(w[e]);
+                s0 = ptx::f2_fma(st.q[0][e], kk, s0);
+                s1 = ptx::f2_fma(st.q[1][e], kk, s1);
             }
-            v[2 * j] = s0;
-            v[2 * j + 1] = s1;
+            const float2 a0 = ptx::f2_unpack(s0), a1 = ptx::f2_unpack(s1);
+            v[2 * j] = a0.x + a0.y;
+            v[2 * j + 1] = a1.x + a1.y;
         }
         // ---- reduce-scatter: lane l ends with the full score of index l >> 1 ----
 #pragma unroll
@@ -160,10 +161,13 @@ struct SlidingCore {
         st.m[1] = mn1;
 
         // ---- P.V ----
+        {
+            const uint64_t aa0 = ptx::f2_pack(a0, a0), aa1 = ptx::f2_pack(a1, a1);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            st.acc[0][e] *= a0;
-            st.acc[1][e] *= a1;
+            for (int e = 0; e < 4; ++e) {
+                st.acc[0][e] = ptx::f2_mul(st.acc[0][e], aa0);
+                st.acc[1][e] = ptx::f2_mul(st.acc[1][e], aa1);
+            }
         }
 #pragma unroll
         for (int j = 0; j < kPosPerWarp; ++j) {
@@ -173,13 +177,12 @@ struct SlidingCore {
             const bool valid = (row0 + j >= vlo) && (row0 + j < vhi);
             if (!valid) raw = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            const uint64_t pp0 = ptx::f2_pack(p0, p0), pp1 = ptx::f2_pack(p1, p1);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float x0 = bf16lo(w[e]), x1 = bf16hi(w[e]);
-                st.acc[0][2 * e] = fmaf(p0, x0, st.acc[0][2 * e]);
-                st.acc[0][2 * e + 1] = fmaf(p0, x1, st.acc[0][2 * e + 1]);
-                st.acc[1][2 * e] = fmaf(p1, x0, st.acc[1][2 * e]);
-                st.acc[1][2 * e + 1] = fmaf(p1, x1, st.acc[1][2 * e + 1]);
+                const uint64_t xx = ptx::f2_from_bf16x2(w[e]);
+                st.acc[0][e] = ptx::f2_fma(pp0, xx, st.acc[0][e]);
+                st.acc[1][e] = ptx::f2_fma(pp1, xx, st.acc[1][e]);
             }
         }
     }
@@ -197,8 +200,10 @@ struct SlidingCore {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             float4* dst = reinterpret_cast<float4*>(&sc.wacc[warp][h][lane * 8]);
-            dst[0] = make_float4(st.acc[h][0], st.acc[h][1], st.acc[h][2], st.acc[h][3]);
-            dst[1] = make_float4(st.acc[h][4], st.acc[h][5], st.acc[h][6], st.acc[h][7]);
+            const float2 x0 = ptx::f2_unpack(st.acc[h][0]), x1 = ptx::f2_unpack(st.acc[h][1]);
+            const float2 x2 = ptx::f2_unpack(st.acc[h][2]), x3 = ptx::f2_unpack(st.acc[h][3]);
+            dst[0] = make_float4(x0.x, x0.y, x1.x, x1.y);
+            dst[1] = make_float4(x2.x, x2.y, x3.x, x3.y);
         }
         ptx::named_barrier_sync(1, NC * 32);
         const int tid = warp * 32 + lane;
