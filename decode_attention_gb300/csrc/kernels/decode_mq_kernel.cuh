@@ -968,8 +968,27 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint32_t bad_all = sm.epi_bad;
             const SegmentParts sp(pl, epi.b, epi.kvh, p.dyn_slot_base);
             const bool direct = sp.count() == 1;
+            // This code runs once per piece, and mostly cold: its loop over head-dim blocks
+            // stays rolled, each row's scale is taken once, and each kind of piece stores
+            // through one short path, so that few instruction lines are fetched.  (Fully
+            // unrolled, with a division and both output types per element, the last
+            // epilogue of a CTA took ~15 us on decodeGQA B=8, T=4.)
             if (r0 < R) {
-#pragma unroll (kBlockUnroll)
+                // per row k of this warp: direct pieces 1 / l (0 for a row that saw no key,
+                // NaN for a bad page), partials 1 (NaN for a bad page)
+                float scale[RH];
+#pragma unroll
+                for (int k = 0; k < RH; ++k) {
+                    const int r = r0 + k;
+                    const bool bad = r < R && ((bad_all >> (r / G)) & 1u);
+                    const float lr = (direct && r < R) ? sm.epi_l[r] : 1.0f;
+                    scale[k] = bad ? nan : (lr == 0.0f ? 0.0f : 1.0f / lr);
+                }
+                // row r0 + k is query token r0 / G + k / G (r0 is a multiple of G), head
+                // k % G of the group: output row (b T + t) H + kvh G + g of [B, T, H, D]
+                const size_t out_row0 = (static_cast<size_t>(epi.b) * T + r0 / G) * H + epi.kvh * G;
+                float* const part0 = p.ws_acc + (static_cast<size_t>(epi.slot) * R + r0) * D;
+#pragma unroll 1
                 for (int mb = 0; mb < NB; ++mb) {
                     // row r's sum is its hi column r plus its lo column PLO + r
                     uint32_t oh[RH], ol[RH];
@@ -977,22 +996,32 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     ptx::tmem_ld<RH>(ob, oh);
                     ptx::tmem_ld<RH>(ob + Cfg::PLO, ol);
                     ptx::tmem_wait_ld();
+                    const int dd = mb * 128 + j;
+                    if (!direct) {
+                        float* const dst = part0 + dd;
 #pragma unroll
-                    for (int k = 0; k < RH; ++k) {
-                        const int r = r0 + k;
-                        if (r >= R) break;
-                        const int t = r / G, g = r - (r / G) * G;
-                        const bool bad = (bad_all >> t) & 1u;
-                        const int dd = mb * 128 + j;
-                        const float acc = __uint_as_float(oh[k]) + __uint_as_float(ol[k]);
-                        if (direct) {
-                            const size_t row = (static_cast<size_t>(epi.b) * T + t) * H + epi.kvh * G + g;
-                            const float lr = sm.epi_l[r];
-                            // no key at all: the empty sum (a NaN normaliser stays NaN)
-                            store_out(p, row * D + dd, bad ? nan : (lr == 0.0f ? 0.0f : acc / lr));
-                        } else {
-                            p.ws_acc[(static_cast<size_t>(epi.slot) * R + r) * D + dd] = bad ? nan : acc;
-                        }
+                        for (int k = 0; k < RH; ++k)
+                            if (r0 + k < R)
+                                dst[static_cast<size_t>(k) * D] =
+                                    (__uint_as_float(oh[k]) + __uint_as_float(ol[k])) * scale[k];
+                    } else if (p.out_f32) {
+                        float* const dst = static_cast<float*>(p.out) + out_row0 * D + dd;
+#pragma unroll
+                        for (int k = 0; k < RH; ++k)
+                            if (r0 + k < R) {
+                                const float acc = __uint_as_float(oh[k]) + __uint_as_float(ol[k]);
+                                dst[static_cast<size_t>((k / G) * H + k % G) * D] =
+                                    scale[k] == 0.0f ? 0.0f : acc * scale[k];
+                            }
+                    } else {
+                        __nv_bfloat16* const dst = static_cast<__nv_bfloat16*>(p.out) + out_row0 * D + dd;
+#pragma unroll
+                        for (int k = 0; k < RH; ++k)
+                            if (r0 + k < R) {
+                                const float acc = __uint_as_float(oh[k]) + __uint_as_float(ol[k]);
+                                dst[static_cast<size_t>((k / G) * H + k % G) * D] =
+                                    __float2bfloat16_rn(scale[k] == 0.0f ? 0.0f : acc * scale[k]);
+                            }
                     }
                 }
             }
