@@ -26,6 +26,10 @@ namespace gqa {
 
 constexpr int kCombineThreads = 128;    // float4 outputs per work item
 constexpr int kCombineBatch = 16;       // pieces whose loads are in flight together
+// Blocks per SM of a combine launch: each block merges its items one after the
+// other, one round trip of loads each, so more blocks shorten the kernel (4 per SM
+// left sliding T = 8 with ~13 items per block, ~15 us)
+constexpr int kCombineBlocksPerSm = 16;
 
 template <int G, int D>
 __global__ void __launch_bounds__(kCombineThreads)

@@ -215,6 +215,23 @@ struct alignas(1024) MqSmem {
     int abort_flag;
 };
 
+// The Q operand of segment (b, kvh) into the Q buffer at qdst, completing on bar: the
+// q rows of the KV head's group (elements, rows, ...), or over a K=V cache the scores
+// operand [B, KVH, 2 G, D] of the segment except its rotated column blocks.  Not
+// inlined: the producer services a pending Q load from every wait, and one out-of-line
+// copy keeps its code (fetched cold at the start of each CTA) small.
+template <class Cfg>
+__device__ __noinline__ void mq_load_q(uint32_t qdst, const CUtensorMap* tm_q, uint32_t bar, int b,
+                                       int kvh, uint64_t policy) {
+    for (int c = 0; c < Cfg::NSUB; ++c) {
+        if (Cfg::KEQV && (c == 0 || c == Cfg::NSUB / 2)) continue;
+        if (Cfg::KEQV)
+            ptx::tma_load_4d(qdst + c * Cfg::QATOM, tm_q, bar, 64 * c, 0, kvh, b, policy);
+        else
+            ptx::tma_load_4d(qdst + c * Cfg::QATOM, tm_q, bar, 64 * c, kvh * Cfg::G, 0, b, policy);
+    }
+}
+
 // Byte offset of P^T element (query row r, tile position j): K-major, no swizzle.
 __device__ __forceinline__ uint32_t mq_p_off(int r, int j) {
     return (j >> 3) * kMqPLbo + (r >> 3) * kMqPSbo + (r & 7) * 16 + (j & 7) * 2;
@@ -351,17 +368,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             auto service_q = [&]() {
                 // piece n (= q_issued) may overwrite Q once the last scores of piece n - 1 are done
                 if (q_pend && ptx::mbar_try_wait(q_empty_bar, (q_issued & 1u) ^ 1u)) {
-                    const uint32_t qdst = ptx::smem_addr(&sm.q[0]);
-                    for (int c = 0; c < NSUB; ++c) {
-                        // (elements, rows, ...): the q rows of the KV head's group, or the
-                        // K=V scores operand [B, KVH, 2 G, D] of the segment
-                        if (Cfg::KEQV && (c == 0 || c == NSUB / 2)) continue;
-                        if (Cfg::KEQV)
-                            ptx::tma_load_4d(qdst + c * Cfg::QATOM, &tm_q, q_bar, 64 * c, 0, q_kvh, q_b, policy);
-                        else
-                            ptx::tma_load_4d(qdst + c * Cfg::QATOM, &tm_q, q_bar, 64 * c, q_kvh * G, 0, q_b,
-                                             policy);
-                    }
+                    mq_load_q<Cfg>(ptx::smem_addr(&sm.q[0]), &tm_q, q_bar, q_b, q_kvh, policy);
                     q_pend = false;
                     ++q_issued;
                 }

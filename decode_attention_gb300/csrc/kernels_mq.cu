@@ -137,7 +137,7 @@ cudaError_t launch_mq_impl(const LaunchArgs& a) {
     const int segments = a.p.B * a.p.KVH;
     const int chunks_per_seg = (T * Cfg::G * Cfg::D / 4 + kCombineThreads - 1) / kCombineThreads;
     const int items = segments * chunks_per_seg;
-    const int cgrid = items < 4 * a.grid ? items : 4 * a.grid;
+    const int cgrid = items < kCombineBlocksPerSm * a.grid ? items : kCombineBlocksPerSm * a.grid;
     cudaLaunchConfig_t ccfg = {};
     ccfg.gridDim = dim3(static_cast<unsigned>(cgrid));
     ccfg.blockDim = dim3(kCombineThreads);

@@ -87,7 +87,7 @@ cudaError_t launch_decode(const LaunchArgs& a) {
     const int segments = a.p.B * a.p.KVH;
     constexpr int kChunksPerSeg = (Pol::G * Pol::D / 4 + kCombineThreads - 1) / kCombineThreads;
     const int items = segments * kChunksPerSeg;
-    const int cgrid = items < 4 * a.grid ? items : 4 * a.grid;
+    const int cgrid = items < kCombineBlocksPerSm * a.grid ? items : kCombineBlocksPerSm * a.grid;
     cudaLaunchConfig_t ccfg = {};
     ccfg.gridDim = dim3(static_cast<unsigned>(cgrid));
     ccfg.blockDim = dim3(kCombineThreads);
