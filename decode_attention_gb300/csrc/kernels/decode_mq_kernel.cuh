@@ -232,6 +232,52 @@ __device__ __noinline__ void mq_load_q(uint32_t qdst, const CUtensorMap* tm_q, u
     }
 }
 
+// The producer's pending Q load: the Q operand of the newest piece, issued once the
+// previous piece's last scores are done (q_empty), completing on that piece's first K
+// stage (bar).
+struct MqPendingQ {
+    bool pend;
+    uint32_t issued;      // pieces whose Q load was issued
+    int b, kvh;
+    uint32_t bar;         // full barrier the load completes on
+    uint32_t empty_bar;   // q_empty
+    uint32_t dst;         // the Q buffer
+    const CUtensorMap* map;
+    uint64_t policy;
+};
+
+// Issues the pending Q load if the Q buffer is free (piece n = issued may overwrite it
+// once the last scores of piece n - 1 are done).
+template <class Cfg>
+__device__ __forceinline__ void mq_service_q(MqPendingQ& qs) {
+    if (qs.pend && ptx::mbar_try_wait(qs.empty_bar, (qs.issued & 1u) ^ 1u)) {
+        mq_load_q<Cfg>(qs.dst, qs.map, qs.bar, qs.b, qs.kvh, qs.policy);
+        qs.pend = false;
+        ++qs.issued;
+    }
+}
+
+// The producer's bounded wait on barrier bar (or, with bar == 0, for the pending Q load
+// to go out), servicing the pending Q load meanwhile.  False when the CTA is aborting or
+// the wait timed out (which starts the abort).  Out of line: one copy serves every wait
+// site of the producer, whose code is fetched cold at the start of each CTA.
+template <class Cfg>
+__device__ __noinline__ bool mq_poll_servicing(uint32_t bar, uint32_t parity, MqPendingQ& qs,
+                                               volatile int* abort_flag, uint32_t* flags) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t round = 0;; ++round) {
+        mq_service_q<Cfg>(qs);
+        for (int i = 0; i < 8; ++i)
+            if (bar ? ptx::mbar_try_wait(bar, parity) : !qs.pend) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs || round > kWaitMaxRounds) {
+            *abort_flag = 1;
+            atomicOr(flags, kFlagWaitTimeout);
+            return false;
+        }
+    }
+}
+
 // Byte offset of P^T element (query row r, tile position j): K-major, no swizzle.
 __device__ __forceinline__ uint32_t mq_p_off(int r, int j) {
     return (j >> 3) * kMqPLbo + (r >> 3) * kMqPSbo + (r & 7) * 16 + (j & 7) * 2;
@@ -360,35 +406,39 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // last scores: the load completes on the full barrier of the piece's first K
             // stage, which already expects its bytes.  Every wait of the producer keeps
             // servicing it, so the K stages of the piece stream meanwhile.
-            bool q_pend = false;
-            uint32_t q_issued = 0;   // pieces whose Q load was issued
-            int q_b = 0, q_kvh = 0;
-            uint32_t q_bar = 0;
-            const uint32_t q_empty_bar = ptx::smem_addr(&sm.q_empty);
-            auto service_q = [&]() {
-                // piece n (= q_issued) may overwrite Q once the last scores of piece n - 1 are done
-                if (q_pend && ptx::mbar_try_wait(q_empty_bar, (q_issued & 1u) ^ 1u)) {
-                    mq_load_q<Cfg>(ptx::smem_addr(&sm.q[0]), &tm_q, q_bar, q_b, q_kvh, policy);
-                    q_pend = false;
-                    ++q_issued;
-                }
-            };
+            MqPendingQ qs;
+            qs.pend = false;
+            qs.issued = 0;
+            qs.b = qs.kvh = 0;
+            qs.bar = 0;
+            qs.empty_bar = ptx::smem_addr(&sm.q_empty);
+            qs.dst = ptx::smem_addr(&sm.q[0]);
+            qs.map = &tm_q;
+            qs.policy = policy;
+            auto service_q = [&]() { mq_service_q<Cfg>(qs); };
             // Bounded wait on a stage barrier (or, with bar == 0, for the pending Q to be
-            // issued) that services the pending Q while it waits.
+            // issued) that services the pending Q while it waits.  Over a K=V cache the
+            // polling loop is out of line (one copy for the producer's many wait sites:
+            // 1387 -> 1358 us on global_keqv_b16_s131072); the multi-query configurations
+            // keep it inline (out of line they were 4-6% slower, the pending-Q state then
+            // living in local memory).
             auto wait_servicing = [&](uint32_t bar, uint32_t parity) -> bool {
-                auto done = [&]() { return bar ? ptx::mbar_try_wait(bar, parity) : !q_pend; };
                 service_q();
-                if (done()) return true;
-                const uint64_t t0 = ptx::globaltimer_ns();
-                for (uint32_t round = 0;; ++round) {
-                    service_q();
-                    for (int i = 0; i < 8; ++i)
-                        if (done()) return true;
-                    if (sm.abort_flag) return false;
-                    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs || round > kWaitMaxRounds) {
-                        sm.abort_flag = 1;
-                        atomicOr(p.ws_flags, kFlagWaitTimeout);
-                        return false;
+                if (bar ? ptx::mbar_try_wait(bar, parity) : !qs.pend) return true;
+                if constexpr (Cfg::KEQV) {
+                    return mq_poll_servicing<Cfg>(bar, parity, qs, &sm.abort_flag, p.ws_flags);
+                } else {
+                    const uint64_t t0 = ptx::globaltimer_ns();
+                    for (uint32_t round = 0;; ++round) {
+                        service_q();
+                        for (int i = 0; i < 8; ++i)
+                            if (bar ? ptx::mbar_try_wait(bar, parity) : !qs.pend) return true;
+                        if (sm.abort_flag) return false;
+                        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs || round > kWaitMaxRounds) {
+                            sm.abort_flag = 1;
+                            atomicOr(p.ws_flags, kFlagWaitTimeout);
+                            return false;
+                        }
                     }
                 }
             };
@@ -433,10 +483,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         (with_q ? q_bytes : 0u);
                     ptx::mbar_arrive_expect_tx(full_bar, bytes);
                     if (with_q) {
-                        q_pend = true;
-                        q_b = d.b;
-                        q_kvh = d.kvh;
-                        q_bar = full_bar;
+                        qs.pend = true;
+                        qs.b = d.b;
+                        qs.kvh = d.kvh;
+                        qs.bar = full_bar;
                     }
                     const CUtensorMap* map = kind == kMqKindK ? &tm_k : &tm_v;
                     const uint32_t dst = stage0 + s * kMqStageBytes;
