@@ -129,6 +129,12 @@ struct MqCfg {
     // Over a K=V cache a second producer warp streams the V blocks, so that waits on the
     // V ring (paced by the P.V warp) never hold up the K and R rings.
     static constexpr bool SPLIT_V = KEQV;
+    // On a contiguous cache, a tile at the end of its sequence loads only the 16-row boxes
+    // that hold attended rows.  Sliding segments span at most W + T - 1 positions (1031
+    // for T = 8: 9 tiles, the last one 7 rows), so about a tenth of their tile rows would
+    // be unattended; global segments are long, and the extra branch in the producer's
+    // stage loop cost them more (3-7%) than it saved.
+    static constexpr bool RAGGED = (D == 256);
     static constexpr int V_WARP = PV_WARP + 1;          // the V producer (SPLIT_V)
     static constexpr int THREADS = 32 * (PV_WARP + 1 + (SPLIT_V ? 1 : 0));
     static constexpr int TMEM_COLS = tmem_cols_for(TMEM_TRIG + TRIG_COLS);
@@ -286,7 +292,8 @@ __device__ __forceinline__ uint32_t mq_p_off(int r, int j) {
 template <class Cfg, bool kPaged>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gqa_mq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k16,
+                  const __grid_constant__ CUtensorMap tm_v16, const DecodeParams p) {
     constexpr int D = Cfg::D, G = Cfg::G, NSUB = Cfg::NSUB, NB = Cfg::NB, STAGES = Cfg::STAGES;
     constexpr int KST = Cfg::KST, VST = Cfg::VST;
     constexpr int NMAX = Cfg::NMAX;
@@ -336,6 +343,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
+        if (!kPaged && Cfg::RAGGED) {
+            ptx::prefetch_tensormap(&tm_k16);
+            ptx::prefetch_tensormap(&tm_v16);
+        }
         ptx::prefetch_tensormap(&tm_q);
     }
     ptx::grid_dependency_wait();
@@ -478,8 +489,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (with_q && !wait_servicing(0u, 0u)) return false;
                     if (sub == 0 && ring == 0) sm.desc[s] = d;
                     if (sub == 0 && ring == 2) sm.rdesc[s - KST - VST] = d;
+                    // (RAGGED) a tile at the end of its sequence (fewer than 128 rows attended)
+                    // loads only the 16-row boxes that hold attended rows; the rows after them
+                    // keep stale data, which the masks and the P.V warp's fix-up exclude
+                    const int nrag =
+                        (!kPaged && Cfg::RAGGED && d.zhi < kMqTile) ? (d.zhi + kPageRows - 1) / kPageRows : 0;
                     const uint32_t bytes =
-                        (kPaged ? static_cast<uint32_t>(npage) * kPageBytes : kMqStageBytes) +
+                        (kPaged ? static_cast<uint32_t>(npage) * kPageBytes
+                                : (nrag > 0 ? static_cast<uint32_t>(nrag) * kPageBytes : kMqStageBytes)) +
                         (with_q ? q_bytes : 0u);
                     ptx::mbar_arrive_expect_tx(full_bar, bytes);
                     if (with_q) {
@@ -501,6 +518,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             if (page < 0 || page >= p.num_pages) page = 0;   // flagged by the softmax warps
                             ptx::tma_load_4d(dst + j * kPageBytes, map, full_bar, 0, 0, chunk, page, pol);
                         }
+                    } else if (Cfg::RAGGED && nrag > 0) {
+                        const CUtensorMap* map16 = kind == kMqKindK ? &tm_k16 : &tm_v16;
+                        for (int j = 0; j < nrag; ++j)
+                            ptx::tma_load_4d(dst + j * kPageBytes, map16, full_bar, 0, d.t + j * kPageRows,
+                                             chunk, d.b, pol);
                     } else {
                         // rows past the end of the cache read as zeros
                         ptx::tma_load_4d(dst, map, full_bar, 0, d.t, chunk, d.b, pol);
@@ -765,13 +787,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     kPaged ? p.block_table + static_cast<size_t>(d.b) * p.max_pages : nullptr;
                 // paged: the pages that hold attended positions of the sequence
                 const int npage = kPaged ? (d.zhi + kPageRows - 1) / kPageRows : 0;
+                // a tile at the end of its sequence: only the 16-row boxes with attended rows
+                const int nrag =
+                    (!kPaged && Cfg::RAGGED && d.zhi < kMqTile) ? (d.zhi + kPageRows - 1) / kPageRows : 0;
                 for (int sub = 0; sub < NSUB; ++sub) {
                     const int s = vst(vseq);
                     ok = wait_bounded(ptx::smem_addr(&sm.empty[s]), ((vseq / VST) & 1u) ^ 1u,
                                       &sm.abort_flag, p.ws_flags);
                     if (!ok) break;
                     const uint32_t vfull = ptx::smem_addr(&sm.full[s]);
-                    ptx::mbar_arrive_expect_tx(vfull, kPaged ? static_cast<uint32_t>(npage) * kPageBytes : kMqStageBytes);
+                    ptx::mbar_arrive_expect_tx(
+                        vfull, kPaged ? static_cast<uint32_t>(npage) * kPageBytes
+                                      : (nrag > 0 ? static_cast<uint32_t>(nrag) * kPageBytes : kMqStageBytes));
                     const uint32_t dst = stage0 + s * kMqStageBytes;
                     const int chunk = d.kvh * NSUB + sub;
                     if (kPaged) {
@@ -780,6 +807,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             if (page < 0 || page >= p.num_pages) page = 0;   // flagged by the softmax warps
                             ptx::tma_load_4d(dst + j * kPageBytes, &tm_v, vfull, 0, 0, chunk, page, policy);
                         }
+                    } else if (Cfg::RAGGED && nrag > 0) {
+                        for (int j = 0; j < nrag; ++j)
+                            ptx::tma_load_4d(dst + j * kPageBytes, &tm_v16, vfull, 0, d.t + j * kPageRows,
+                                             chunk, d.b, policy);
                     } else {
                         // rows past the end of the cache read as zeros
                         ptx::tma_load_4d(dst, &tm_v, vfull, 0, d.t, chunk, d.b, policy);

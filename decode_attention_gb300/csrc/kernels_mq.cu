@@ -7,16 +7,16 @@ namespace gqa {
 namespace {
 
 // K or V cache for the multi-query kernel: 4-D view (64 elements, row, 64-element
-// chunk of the KVH*D row (stride 128 B), outer), 128-byte swizzle; box (64, 128, 1, 1)
-// on a contiguous cache (one 16 KB stage: 128 rows of one chunk) or (64, 16, 1, 1) on
-// a paged pool (one page of one chunk, 2 KB).
+// chunk of the KVH*D row (stride 128 B), outer), 128-byte swizzle; box (64, box_rows,
+// 1, 1): on a contiguous cache 128 rows (one 16 KB stage of one chunk) or 16 rows (the
+// attended rows of a sequence's last tile, box by box), on a paged pool 16 rows (one
+// page of one chunk, 2 KB).
 bool encode_mq_kv_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t outer, int KVH,
-                      int D, bool paged) {
+                      int D, int box_rows) {
     const uint64_t row_bytes = static_cast<uint64_t>(KVH) * D * 2;
     cuuint64_t dims[4] = {64, rows, static_cast<cuuint64_t>(KVH) * (D / 64), outer};
     cuuint64_t strides[3] = {row_bytes, 128, row_bytes * rows};
-    cuuint32_t box[4] = {64, paged ? static_cast<cuuint32_t>(kPageRows) : static_cast<cuuint32_t>(kMqTile),
-                         1, 1};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return false;
@@ -101,9 +101,12 @@ cudaError_t launch_mq_impl(const LaunchArgs& a) {
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
 
     const int T = a.p.T > 1 ? a.p.T : 1;
-    CUtensorMap tm_k, tm_v, tm_q;
-    if (!encode_mq_kv_map(&tm_k, a.k, a.rows, a.outer, a.p.KVH, Cfg::D, kPaged) ||
-        !encode_mq_kv_map(&tm_v, a.v, a.rows, a.outer, a.p.KVH, Cfg::D, kPaged))
+    CUtensorMap tm_k, tm_v, tm_q, tm_k16, tm_v16;
+    const int rows_per_box = kPaged ? kPageRows : kMqTile;
+    if (!encode_mq_kv_map(&tm_k, a.k, a.rows, a.outer, a.p.KVH, Cfg::D, rows_per_box) ||
+        !encode_mq_kv_map(&tm_v, a.v, a.rows, a.outer, a.p.KVH, Cfg::D, rows_per_box) ||
+        !encode_mq_kv_map(&tm_k16, a.k, a.rows, a.outer, a.p.KVH, Cfg::D, kPageRows) ||
+        !encode_mq_kv_map(&tm_v16, a.v, a.rows, a.outer, a.p.KVH, Cfg::D, kPageRows))
         return cudaErrorInvalidValue;
     if (Cfg::KEQV ? !encode_keqv_operand_map(&tm_q, a.p.keqv_operand, a.p.B, a.p.KVH)
                   : !encode_mq_q_map(&tm_q, a.p.q, a.p.B, T, a.p.H, Cfg::D, Cfg::G))
@@ -131,7 +134,7 @@ cudaError_t launch_mq_impl(const LaunchArgs& a) {
     cfg.stream = a.stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gqa_mq_kernel<Cfg, kPaged>, tm_k, tm_v, tm_q, a.p);
+    e = cudaLaunchKernelEx(&cfg, gqa_mq_kernel<Cfg, kPaged>, tm_k, tm_v, tm_q, tm_k16, tm_v16, a.p);
     if (e != cudaSuccess) return e;
 
     const int segments = a.p.B * a.p.KVH;
