@@ -892,6 +892,9 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
     if constexpr (Pol::kKeqV) {
         if (warp == NC + 1) {
             // ====== helper: the rotation angles of every tile, a few stages ahead ======
+            // (its frequencies come from the parameters: the consumers' setup of the
+            // scratch tables is not ordered before this warp's first tile)
+            const double f[2] = {p.rope_freq[2 * lane], p.rope_freq[2 * lane + 1]};
             for (uint32_t t_idx = 0;; ++t_idx) {
                 const int s = t_idx % STAGES;
                 const uint32_t ph = (t_idx / STAGES) & 1u;
@@ -899,7 +902,7 @@ __global__ void __launch_bounds__(block_threads<Pol>(), 1)
                                                                     &sm.abort_flag, p.ws_flags));
                 if (!ok) return;
                 const TileDesc d = sm.desc[s];
-                if (!(d.flags & kDescDone)) Pol::tile_angles(sm.scratch, s, d.pos0, lane);
+                if (!(d.flags & kDescDone)) Pol::tile_angles(sm.scratch, s, d.pos0, f, lane);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sm.ready[s]));
                 if (d.flags & kDescDone) return;

@@ -61,7 +61,6 @@ struct MmaKeqV {
         alignas(16) float2 cs_base[STAGES][kRot];     // cos, sin of pos0 * f_i, per stage
         alignas(16) float2 cs_step[TP][kRot];         // cos, sin of j * f_i
         alignas(16) float w[D];                       // k_norm weight
-        double freq[kRot];                            // f_i = 1e6^(-2i/512)
     };
 
     struct State {
@@ -80,15 +79,14 @@ struct MmaKeqV {
                ((unit ^ (r & 7)) << 4);
     }
 
-    // Once per CTA (all consumer threads, then a consumer barrier): the weight, the
-    // frequencies and the table of cos/sin(j f_i).
+    // Once per CTA (all consumer threads, then a consumer barrier): the weight and the
+    // table of cos/sin(j f_i).  Only the consumers read them, after that barrier.
     __device__ static __forceinline__ void init(Scratch& sc, const DecodeParams& p, int tid) {
         constexpr int kThreads = NC * 32;
         for (int i = tid; i < D; i += kThreads) sc.w[i] = __bfloat162float(p.w_k[i]);
         for (int e = tid; e < TP * kRot; e += kThreads) {
             const int j = e / kRot, i = e - (e / kRot) * kRot;
             const double f = p.rope_freq[i];
-            if (j == 0) sc.freq[i] = f;
             float sn, cs;
             sincosf(static_cast<float>(static_cast<double>(j) * f), &sn, &cs);   // |angle| < 32
             sc.cs_step[j][i] = make_float2(cs, sn);
@@ -145,13 +143,16 @@ struct MmaKeqV {
     }
 
     // Helper warp: cos/sin of pos0 * f_i for the tile in stage `stage`, lane l taking
-    // i = 2l and 2l + 1.  pos0 * f_i reaches 2.6e5 rad, far past fp32's exact range,
-    // so the angle is reduced mod 2 pi in fp64 first.
-    __device__ static __forceinline__ void tile_angles(Scratch& sc, int stage, int pos0, int lane) {
+    // i = 2l and 2l + 1 (f = f_2l, f_2l+1, which the lane holds in registers: the helper
+    // runs from the first tile on, before the consumers' one-time setup has finished).
+    // pos0 * f_i reaches 2.6e5 rad, far past fp32's exact range, so the angle is reduced
+    // mod 2 pi in fp64 first.
+    __device__ static __forceinline__ void tile_angles(Scratch& sc, int stage, int pos0,
+                                                       const double (&f)[2], int lane) {
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             const int i = 2 * lane + t;
-            const double a = static_cast<double>(pos0) * sc.freq[i];
+            const double a = static_cast<double>(pos0) * f[t];
             const double turns = rint(a * 0.15915494309189535);   // 1 / (2 pi)
             const double r = fma(-turns, 6.283185307179586, a);
             float sn, cs;

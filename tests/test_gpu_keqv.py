@@ -123,3 +123,24 @@ def test_keqv_bf16_output_is_the_rounded_fp32_output(roomy):
     out16 = gqa.gqa_decode_keqv(c["q"], c["v"], c["w_k"], c["seq_lens"], out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     assert torch.equal(out16, out32.to(torch.bfloat16))
+
+
+@ROOMY
+def test_keqv_cold_calls_agree_with_the_oracle_every_time(roomy):
+    """Twelve calls in a row, each after a write larger than the L2 cache, so every
+    CTA's first tile comes from DRAM as fast as the one-time setup of its tables does.
+    Every call's output is checked: the rotation angles of the first tiles must not
+    depend on which of the two finishes first."""
+    lens = [2914, 1371]
+    c = case(lens, capacity(len(lens), 3000, roomy), seed=405)
+    ref = oracle_keqv(c, lens)
+    flush = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.empty((len(lens), H, D), dtype=torch.float32, device="cuda")
+    outs = []
+    for _ in range(12):
+        flush.add_(1)
+        gqa.gqa_decode_keqv(c["q"], c["v"], c["w_k"], c["seq_lens"], out=out)
+        outs.append(out.clone())
+    torch.cuda.synchronize()
+    for k, o in enumerate(outs):
+        check(o, ref, lens, f"keqv cold call {k}")
